@@ -1,0 +1,404 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test ties the oracle to something independent of it: numbers printed on
+the reference pages (``tests/golden/``), a library routine computing the same
+quantity on non-paged data (torch's float64 scaled-dot-product attention and
+logsumexp), closed forms and invariants of exact attention.  The last group
+plants plausible mistakes in a copy of the oracle's source and checks that
+the pins catch each one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_cache_151_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_sizing.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# sizes printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_kv_bytes_per_token_llama8b():
+    g = golden()["kv_per_token_llama8b"]
+    got = oracle.kv_bytes_per_token(g["num_layers"], g["num_kv_heads"],
+                                    g["head_dim"], g["dtype_bytes"])
+    assert got == g["kv_bytes_per_token"] == 128 * 1024
+
+
+def test_conversation_size():
+    g = golden()["conversation_2000_tokens"]
+    per_tok = oracle.kv_bytes_per_token(32, 8, 128, 2)
+    one = g["tokens"] * per_tok
+    assert round(one / 2**20) == g["approx_mib"]
+    assert round(g["conversations"] * one / 1e9) in (g["approx_gb_total"], 52)
+
+
+def test_block_budget_exercise():
+    g = golden()["block_budget_exercise"]
+    bpb = oracle.bytes_per_block(g["block_size"], g["num_layers"],
+                                 g["num_kv_heads"], g["head_dim"], g["dtype_bytes"])
+    blocks = (g["pool_gib"] * 1024**3) // bpb
+    assert blocks * g["block_size"] == g["token_slots"]
+
+
+def test_worked_pool_example():
+    g = golden()["worked_pool_example"]
+    bs = g["block_size"]
+    bpb = bs * g["kv_bytes_per_token"]
+    assert bpb == g["bytes_per_block"]
+    n = (g["pool_gib"] * 1024**3) // bpb
+    assert n == g["num_blocks"]
+    nb = oracle.blocks_for_tokens(g["short_request_tokens"], bs)
+    assert nb == g["short_request_blocks"] and n // nb == g["short_requests_fit"]
+    nb = oracle.blocks_for_tokens(g["reserved_tokens"], bs)
+    assert nb == g["reserved_blocks"] and n // nb == g["reserved_requests_fit"]
+    nb = oracle.blocks_for_tokens(g["long_chat_tokens"], bs)
+    assert nb == g["long_chat_blocks"] and n // nb == g["long_chats_fit"]
+    # only whole blocks of the shared prompt can be shared
+    full = g["shared_prompt_tokens"] // bs
+    assert full == g["shared_full_blocks"] and full * bs == g["shared_tokens_in_full_blocks"]
+    priv = g["long_chat_tokens"] - full * bs
+    assert priv == g["private_tokens_per_chat"]
+    pb = oracle.blocks_for_tokens(priv, bs)
+    assert pb == g["private_blocks_per_chat"]
+    assert (n - full) // pb == g["shared_chats_fit"]
+
+
+def test_waste_simulation_and_free_list():
+    """The pages' waste simulation: sizes from the oracle, block tables from
+    the generator's free list; both must reproduce the printed output."""
+    g = golden()["waste_simulation"]
+    per_tok = oracle.kv_bytes_per_token(32, 8, 128, 2)
+    rng = np.random.default_rng(g["seed"])
+    lengths = rng.integers(g["len_lo"], g["len_hi_exclusive"], size=g["num_requests"])
+    used = int(lengths.sum())
+    naive = g["max_len"] * len(lengths)
+    paged = sum(oracle.blocks_for_tokens(int(n), g["block_size"]) * g["block_size"]
+                for n in lengths)
+    assert f"{naive * per_tok / 2**30:5.2f}".strip() == g["naive_reserved_gib"]
+    assert f"{100 * (1 - used / naive):4.1f}".strip() == g["naive_waste_pct"]
+    assert f"{paged * per_tok / 2**30:5.2f}".strip() == g["paged_reserved_gib"]
+    assert f"{100 * (1 - used / paged):4.1f}".strip() == g["paged_waste_pct"]
+    fl = wl.FreeList(g["pool_blocks"], rng)
+    a = fl.allocate(g["table_a_tokens"], g["block_size"])
+    assert a == g["table_a"]
+    b = a[:g["table_b_shared_blocks"]] + fl.allocate(g["table_b_new_tokens"], g["block_size"])
+    assert b == g["table_b"]
+    ref = {blk: 1 for blk in a}
+    for blk in a[:g["table_b_shared_blocks"]]:
+        ref[blk] += 1
+    assert {str(k): v for k, v in ref.items() if v > 1} == g["shared_refcounts"]
+
+
+def test_startup_log_concurrency():
+    g = golden()["startup_log_concurrency"]
+    assert f"{g['kv_tokens'] / g['tokens_per_request']:.2f}" == g["concurrency"]
+
+
+# ---------------------------------------------------------------------------
+# decode attention against a library routine on non-paged data
+# ---------------------------------------------------------------------------
+
+def sdpa_reference(batch, s, scale=None):
+    """torch float64 SDPA over the contiguous ground truth of sequence s
+    (grouped-query attention through torch's own ``enable_gqa``)."""
+    q = batch.q[s].double()[None, :, None, :]               # [1, H, 1, D]
+    k = batch.seq_k[s].double().permute(1, 0, 2)[None]      # [1, Hkv, L, D]
+    v = batch.seq_v[s].double().permute(1, 0, 2)[None]
+    sc = batch.scale if scale is None else scale
+    sc = float(np.float32(sc))        # the scale crosses the boundary as fp32
+    o = F.scaled_dot_product_attention(q, k, v, scale=sc, enable_gqa=True)
+    return o[0, :, 0, :].numpy()
+
+
+def oracle_decode(batch, **kw):
+    return oracle.decode(batch.q, batch.k_cache, batch.v_cache,
+                         batch.block_tables, batch.seq_lens, batch.scale,
+                         batch.num_kv_heads, batch.dtype, **kw)
+
+
+CASES = [
+    dict(dtype="f32", num_heads=8, num_kv_heads=2, head_dim=64),
+    dict(dtype="bf16", num_heads=32, num_kv_heads=8, head_dim=128),
+    dict(dtype="f16", num_heads=8, num_kv_heads=1, head_dim=128),
+    dict(dtype="bf16", num_heads=16, num_kv_heads=2, head_dim=64),
+    dict(dtype="f32", num_heads=4, num_kv_heads=4, head_dim=64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c['dtype']}-{c['num_heads']}x{c['num_kv_heads']}x{c['head_dim']}")
+def test_decode_matches_sdpa(case):
+    b = wl.random_batch(11, num_seqs=5, max_len=70, new_in_pool=True, **case)
+    out = oracle_decode(b)
+    for s in range(b.num_seqs):
+        np.testing.assert_allclose(out[s], sdpa_reference(b, s), rtol=0, atol=1e-12)
+
+
+def test_tiny_config_matches_sdpa():
+    b = wl.tiny(new_in_pool=True)
+    out = oracle_decode(b, nthreads=3)
+    for s in range(b.num_seqs):
+        np.testing.assert_allclose(out[s], sdpa_reference(b, s), rtol=0, atol=1e-12)
+
+
+def test_large_scores_stay_finite():
+    """Keys scaled so that exp(z) overflows fp64 unless the maximum is
+    subtracted first; SDPA handles the same data."""
+    b = wl.random_batch(12, num_seqs=3, max_len=40, num_heads=4, num_kv_heads=2,
+                        head_dim=64, dtype="f32", new_in_pool=True, kv_std=1.0)
+    big = 400.0
+    out = oracle.decode(b.q, b.k_cache * big, b.v_cache, b.block_tables,
+                        b.seq_lens, b.scale, b.num_kv_heads, "f32")
+    assert np.isfinite(out).all()
+    for s in range(b.num_seqs):
+        q = b.q[s].double()[None, :, None, :]
+        k = (b.seq_k[s].double() * big).permute(1, 0, 2)[None]
+        v = b.seq_v[s].double().permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(q, k, v, scale=float(np.float32(b.scale)),
+                                             enable_gqa=True)
+        np.testing.assert_allclose(out[s], ref[0, :, 0].numpy(), rtol=0, atol=1e-10)
+
+
+def test_outlier_keys_long_context_shape():
+    """The long-context workload's 1% x8 keys, at a small size, against SDPA."""
+    b = wl.build_batch("outliers", ctx_lens=[300, 1000], num_heads=16,
+                       num_kv_heads=2, head_dim=128, dtype="bf16", num_blocks=90,
+                       tables=[list(range(0, 19)), list(range(19, 82))],
+                       seed=5, kv_std=0.5, outlier_frac=0.01, outlier_mult=8.0,
+                       keep_seq=True, new_in_pool=True)
+    out = oracle_decode(b)
+    for s in range(2):
+        np.testing.assert_allclose(out[s], sdpa_reference(b, s), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# closed forms and invariants
+# ---------------------------------------------------------------------------
+
+def test_seq_len_one_returns_v_exactly():
+    b = wl.random_batch(13, num_seqs=4, max_len=0, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype="bf16", new_in_pool=True)
+    assert (b.seq_lens == 1).all()
+    out = oracle_decode(b)
+    G = b.num_heads // b.num_kv_heads
+    for s in range(b.num_seqs):
+        for h in range(b.num_heads):
+            v = b.seq_v[s][0, h // G].double().numpy()
+            assert np.array_equal(out[s, h], v)
+
+
+def test_seq_len_zero_gives_zeros():
+    b = wl.random_batch(14, num_seqs=3, max_len=20, num_heads=4, num_kv_heads=2,
+                        head_dim=64, dtype="f32", new_in_pool=True)
+    sl = b.seq_lens.copy()
+    sl[1] = 0
+    out = oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, sl, b.scale,
+                        b.num_kv_heads, "f32")
+    assert np.array_equal(out[1], np.zeros_like(out[1]))
+
+
+def test_softmax_weights_sum_to_one():
+    b = wl.random_batch(15, num_seqs=4, max_len=90, num_heads=8, num_kv_heads=2,
+                        head_dim=128, dtype="bf16", new_in_pool=True)
+    pr = oracle.problem(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                        b.scale, b.num_kv_heads, "bf16")
+    for s in range(b.num_seqs):
+        for h in (0, 3, 7):
+            out, w = oracle.decode_one(s, h, None, None, None, None, None, None,
+                                       None, "bf16", problem=pr)
+            assert w.shape[0] == b.seq_lens[s]
+            assert (w >= 0).all()
+            assert abs(w.sum() - 1.0) < 1e-12
+            # the output is the weights applied to V
+            v = b.seq_v[s][:, h // 4].double().numpy()
+            np.testing.assert_allclose(out, w @ v, rtol=0, atol=1e-12)
+
+
+def test_block_permutation_invariance():
+    b = wl.random_batch(16, num_seqs=6, max_len=100, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype="bf16", new_in_pool=True, extra_blocks=20)
+    p = wl.permute_blocks(b, seed=99)
+    assert not np.array_equal(p.block_tables, b.block_tables)
+    assert np.array_equal(oracle_decode(b), oracle_decode(p))
+
+
+def test_shared_prefix_aliasing_equals_private_copies():
+    kw = dict(batch=5, prefix_blocks=6, lo=3, hi=40)
+    shared = wl.shared_prefix(new_in_pool=True, keep_seq=True, **kw)
+    private = wl.shared_prefix(new_in_pool=True, private_prefix=True, **kw)
+    # the shared layout really aliases: every table starts with the same blocks
+    assert (shared.block_tables[:, :6] == shared.block_tables[0, :6]).all()
+    assert len(set(private.block_tables[:, 0].tolist())) == 5
+    a, p = oracle_decode(shared), oracle_decode(private)
+    assert np.array_equal(a, p)
+    for s in range(shared.num_seqs):
+        np.testing.assert_allclose(a[s], sdpa_reference(shared, s), rtol=0, atol=1e-12)
+
+
+def test_constant_v_and_zero_q():
+    b = wl.random_batch(17, num_seqs=3, max_len=50, num_heads=4, num_kv_heads=2,
+                        head_dim=64, dtype="f32", new_in_pool=True)
+    row = torch.linspace(-2, 3, 64)
+    vc = b.v_cache.clone()
+    vc[:] = row
+    out = oracle.decode(b.q, b.k_cache, vc, b.block_tables, b.seq_lens, b.scale,
+                        b.num_kv_heads, "f32")
+    np.testing.assert_allclose(out, np.broadcast_to(row.double().numpy(), out.shape),
+                               rtol=0, atol=1e-12)
+    out = oracle.decode(torch.zeros_like(b.q), b.k_cache, b.v_cache,
+                        b.block_tables, b.seq_lens, b.scale, b.num_kv_heads, "f32")
+    for s in range(b.num_seqs):
+        mean = b.seq_v[s].double().mean(0).numpy()     # [Hkv, D]
+        for h in range(b.num_heads):
+            np.testing.assert_allclose(out[s, h], mean[h // 2], rtol=0, atol=1e-12)
+
+
+def test_table_padding_is_never_read():
+    b = wl.random_batch(18, num_seqs=4, max_len=60, num_heads=4, num_kv_heads=1,
+                        head_dim=64, dtype="f32", new_in_pool=True, table_slack=3)
+    assert (b.block_tables == wl.PAD).any()
+    out = oracle_decode(b)
+    assert np.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# split-KV partitions
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("psize", [16, 48, 64, 512])
+def test_partition_stats_against_library(psize):
+    b = wl.random_batch(19, num_seqs=3, max_len=300, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype="bf16", new_in_pool=True, kv_std=2.0)
+    pr = oracle.problem(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                        b.scale, b.num_kv_heads, "bf16")
+    full = oracle_decode(b)
+    for s in range(b.num_seqs):
+        L = int(b.seq_lens[s])
+        for h in (0, 5):
+            m, l, o = oracle.partition_stats(s, h, psize, None, None, None, None,
+                                             None, None, None, "bf16", problem=pr)
+            assert m.shape[0] == math.ceil(L / psize)
+            q = b.q[s, h].double()
+            k = b.seq_k[s][:, h // 4].double()
+            v = b.seq_v[s][:, h // 4].double()
+            z = float(np.float32(b.scale)) * (k @ q)
+            for p in range(m.shape[0]):
+                sl = slice(p * psize, min(L, (p + 1) * psize))
+                assert m[p] == pytest.approx(float(z[sl].max()), abs=1e-12)
+                assert m[p] + math.log(l[p]) == pytest.approx(
+                    float(torch.logsumexp(z[sl], 0)), abs=1e-12)
+                ref = F.scaled_dot_product_attention(
+                    q[None, None, None], k[sl][None, None], v[sl][None, None],
+                    scale=float(np.float32(b.scale)))[0, 0, 0].numpy()
+                np.testing.assert_allclose(o[p], ref, rtol=0, atol=1e-12)
+            merged = oracle.lse_merge(m, l, o)
+            np.testing.assert_allclose(merged, full[s, h], rtol=0, atol=1e-12)
+
+
+def test_lse_merge_single_partition_is_identity():
+    o = np.random.default_rng(0).normal(size=(1, 8))
+    out = oracle.lse_merge(np.array([3.0]), np.array([7.0]), o)
+    np.testing.assert_allclose(out, o[0], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# cache write against numpy's own indexing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reshape_and_cache_matches_index_assignment(dtype):
+    b = wl.random_batch(20, num_seqs=9, max_len=40, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype=dtype)
+    sm = b.slot_mapping.copy()
+    sm[3] = -1                        # padding token: skipped
+    kc, vc, bad = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache,
+                                           b.v_cache, sm, dtype)
+    assert bad == 0
+    for cache, new, got in ((b.k_cache, b.k_new, kc), (b.v_cache, b.v_new, vc)):
+        ref = oracle._host(cache).copy()
+        N, Hkv, bs, D = ref.shape
+        tokview = ref.transpose(0, 2, 1, 3).reshape(N * bs, Hkv, D).copy()
+        keep = sm >= 0
+        tokview[sm[keep]] = oracle._host(new)[keep]
+        ref = tokview.reshape(N, bs, Hkv, D).transpose(0, 2, 1, 3)
+        assert np.array_equal(got.view(np.uint8), np.ascontiguousarray(ref).view(np.uint8))
+
+
+def test_reshape_and_cache_rejects_out_of_range_slots():
+    b = wl.random_batch(21, num_seqs=3, max_len=10, num_heads=2, num_kv_heads=2,
+                        head_dim=64, dtype="f32")
+    sm = b.slot_mapping.copy()
+    sm[0] = b.num_blocks * b.block_size
+    kc, vc, bad = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache,
+                                           b.v_cache, sm, "f32")
+    assert bad == 1
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must make at least one pin fail
+# ---------------------------------------------------------------------------
+
+MUTATIONS = {
+    "gqa_map_modulo": ("const int32_t j = h / G;", "const int32_t j = h % a->num_kv_heads;"),
+    "row_offset": ("int64_t base = ((pb * a->num_kv_heads + j) * bs + t % bs) * D;",
+                   "int64_t base = ((pb * a->num_kv_heads + j) * bs + (t + 1) % bs) * D;"),
+    "no_scale": ("z[t] = a->scale * acc;", "z[t] = acc;"),
+    "no_max_subtract": ("for (int64_t t = 0; t < L; ++t) { z[t] = exp(z[t] - M); S += z[t]; }",
+                        "for (int64_t t = 0; t < L; ++t) { z[t] = exp(z[t]); S += z[t]; }"),
+    "drop_last_token": ("for (int64_t t = 0; t < L; ++t) {\n        double w = z[t] / S;",
+                        "for (int64_t t = 0; t + 1 < L; ++t) {\n        double w = z[t] / S;"),
+    "merge_sign": ("double c = l[p] * exp(m[p] - M);", "double c = l[p] * exp(M - m[p]);"),
+    "table_row_stride": ("int64_t pb = a->block_tables[s * a->max_blocks + lb];",
+                         "int64_t pb = a->block_tables[s + lb * a->num_seqs];"),
+}
+
+
+def _pins_hold() -> bool:
+    """A compact run of the pins above; False as soon as one fails."""
+    try:
+        b = wl.random_batch(31, num_seqs=4, max_len=60, num_heads=8,
+                            num_kv_heads=2, head_dim=64, dtype="f32",
+                            new_in_pool=True)
+        out = oracle_decode(b)
+        for s in range(b.num_seqs):
+            if not np.allclose(out[s], sdpa_reference(b, s), rtol=0, atol=1e-9):
+                return False
+        big = oracle.decode(b.q, b.k_cache * 400.0, b.v_cache, b.block_tables,
+                            b.seq_lens, b.scale, b.num_kv_heads, "f32")
+        if not np.isfinite(big).all():
+            return False
+        m, l, o = oracle.partition_stats(1, 3, 16, b.q, b.k_cache, b.v_cache,
+                                         b.block_tables, b.seq_lens, b.scale,
+                                         b.num_kv_heads, "f32")
+        if not np.allclose(oracle.lse_merge(m, l, o), out[1, 3], rtol=0, atol=1e-9):
+            return False
+    except ValueError:
+        return False
+    return True
+
+
+def test_unmodified_oracle_passes_compact_pins():
+    assert _pins_hold()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, name
+    lib = oracle.build_variant(src.replace(old, new), str(tmp_path))
+    with oracle.use_library(lib):
+        assert not _pins_hold(), f"planted mistake '{name}' was not caught"
