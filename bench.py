@@ -1,0 +1,541 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one pass of the hot path over the serving-mix batch: the cache
+write of one new token per sequence (pa_reshape_and_cache), then decode
+attention over the paged context (pa_decode).  The batch: 256 sequences,
+32 query / 8 KV heads x 128, bf16 cache in 16-token blocks, lengths lognormal
+(median 350, sigma 1) clipped to [1, 4096], pool 1.2x the blocks needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  ``value`` is sequences per second over all
+ranks with inputs resident in HBM (device time of the K steps, L2 flushed
+between steps); ``e2e`` is the same metric with each step's inputs copied
+from pinned host memory and its output copied back inside the timed region.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_151_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention: seqs/sec and achieved KV HBM GB/s (% of GB300 peak)"
+WORKLOAD = ("serving_mix: batch 256, 32 query / 8 KV heads x 128, bf16 KV cache, block 16, "
+            "seq_lens lognormal(median 350, sigma 1.0) clipped to [1, 4096], pool 1.2x; "
+            "step = reshape_and_cache of 1 token/seq + pa_decode")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (what a call must touch at least)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(b) -> dict:
+    es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
+    L = b.seq_lens.astype(np.int64)
+    kv = int(L.sum()) * 2 * b.num_kv_heads * b.head_dim * es
+    kv_full = int(np.ceil(L / 16).sum()) * 16 * 2 * b.num_kv_heads * b.head_dim * es
+    qo = 2 * b.num_seqs * b.num_heads * b.head_dim * es
+    tab = int(np.ceil(L / 16).sum()) * 4 + 4 * b.num_seqs
+    return {"kv": kv, "kv_full_blocks": kv_full, "total": kv + qo + tab}
+
+
+def cache_write_bytes(b) -> int:
+    es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
+    rows = b.num_seqs * b.num_kv_heads * b.head_dim * es
+    return 2 * 2 * rows + 8 * b.num_seqs          # K and V, read + write, slots
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    csrc = os.path.join(ROOT, "paged_kv_cache_151_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name: str):
+    """DRAM bytes per launch of `name` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[name]
+        if e.get("kernel_src_sha") != kernel_source_digest():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def make_flush(device):
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n = max(2 * l2, 256 << 20)
+    buf = torch.empty(n // 4, dtype=torch.int32, device=device)
+
+    def flush():
+        buf.fill_(1)
+    return flush, n
+
+
+def time_calls(fn, iters, flush, stream):
+    """Device time (ms) of each call, L2 flushed before each."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def gpu_arm(args, rank, world, device):
+    from paged_kv_cache_151_gb300 import pa
+
+    torch.cuda.set_device(device)
+    pa.load()
+    stream = torch.cuda.current_stream()
+    flush, flush_bytes = make_flush(device)
+
+    b = wl.serving_mix(device=device, canary=False)
+    bt, sl, sm = b.torch_tables(device)
+    bt, sl, sm = bt.contiguous(), sl.contiguous(), sm.contiguous()
+    kc, vc = b.k_cache, b.v_cache
+    out = torch.empty_like(b.q)
+    nbytes = decode_bytes(b)
+    wbytes = cache_write_bytes(b)
+
+    def step():
+        pa.pa_reshape_and_cache(b.k_new, b.v_new, kc, vc, sm)
+        pa.pa_decode(out, b.q, kc, vc, bt, sl, b.scale, b.num_kv_heads)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    pa.pa_device_error(clear=True)
+
+    # ---- the K timed steps ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t_wall = time.perf_counter()
+    for e0, e1, e2 in ev:
+        flush()
+        e0.record(stream)
+        pa.pa_reshape_and_cache(b.k_new, b.v_new, kc, vc, sm)
+        e1.record(stream)
+        pa.pa_decode(out, b.q, kc, vc, bt, sl, b.scale, b.num_kv_heads)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    write_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    dec_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flags = pa.pa_device_error(clear=True)
+
+    dec_mean = statistics.mean(dec_ms)
+    achieved = nbytes["total"] / (dec_mean * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = e2e_arm(args, b, device, flush, pa)
+
+    result = {
+        "metric": METRIC,
+        "value": world * b.num_seqs * args.steps / (total_ms * 1e-3),
+        "unit": "seqs/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; no dataset)",
+        "config": {
+            "workload": WORKLOAD,
+            "global_batch": world * b.num_seqs,
+            "tokens_attended": int(b.seq_lens.sum()),
+            "num_blocks": b.num_blocks,
+            "l2": f"flushed between steps ({flush_bytes >> 20} MiB write, outside the events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "decode_splits": "auto",
+        },
+        "kv_gbs": nbytes["kv"] / (dec_mean * 1e-3) / 1e9,
+        "decode_us": dec_mean * 1e3,
+        "decode_us_median": statistics.median(dec_ms) * 1e3,
+        "cache_write_us": statistics.mean(write_ms) * 1e3,
+        "cache_write_gbs": wbytes / (statistics.mean(write_ms) * 1e-3) / 1e9,
+        "decode_bytes": nbytes,
+        "roofline": {
+            "kernel": "decode_kernel<bf16,128,4> (pa_decode)",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "frac_of_nominal_8tbs": achieved / 8000.0,
+            "traffic": recorded_traffic("decode_serving_mix"),
+        },
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "device_error_flags": flags,
+        "wall_s_timed_region": t_wall,
+    }
+    if not args.no_extras and world == 1:
+        result["long_context"] = long_context_arm(args, device, flush, pa)
+        result["paging_overhead"] = paging_overhead_arm(args, device, flush, pa)
+    return result, b
+
+
+def e2e_arm(args, b, device, flush, pa):
+    """Same step, inputs from pinned host memory, output back to the host."""
+    stream = torch.cuda.current_stream()
+    h = {
+        "q": b.q.cpu().pin_memory(), "k_new": b.k_new.cpu().pin_memory(),
+        "v_new": b.v_new.cpu().pin_memory(),
+        "slot_mapping": torch.from_numpy(b.slot_mapping).pin_memory(),
+        "block_tables": torch.from_numpy(b.block_tables).pin_memory(),
+        "seq_lens": torch.from_numpy(b.seq_lens).pin_memory(),
+    }
+    d = {k: torch.empty_like(v, device=device) for k, v in h.items()}
+    out = torch.empty_like(b.q)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    kc, vc = b.k_cache, b.v_cache
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        pa.pa_reshape_and_cache(d["k_new"], d["v_new"], kc, vc, d["slot_mapping"])
+        pa.pa_decode(out, d["q"], kc, vc, d["block_tables"], d["seq_lens"], b.scale,
+                     b.num_kv_heads)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    n = max(10, args.steps // 4)
+    ms = time_calls(step, n, flush, stream)
+    h2d = sum(v.numel() * v.element_size() for v in h.values())
+    return {"value": b.num_seqs / (statistics.mean(ms) * 1e-3), "unit": "seqs/s",
+            "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()),
+            "ms_per_step": statistics.mean(ms), "steps": n}
+
+
+def long_context_arm(args, device, flush, pa):
+    """Split-KV decode on the long-context batch: 8 seqs x 32k..128k tokens,
+    64 query / 8 KV heads x 128 bf16, 512-token partitions."""
+    b = wl.long_context(device=device, canary=False)
+    bt, sl, _ = b.torch_tables(device)
+    msl = 131072
+    ws = torch.empty(pa.pa_decode_partitioned_workspace_size(b.num_seqs, b.num_heads,
+                                                             b.head_dim, msl, 512),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(b.q)
+
+    def call():
+        pa.pa_decode_partitioned(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                 b.num_kv_heads, 512, msl, ws)
+    for _ in range(3):
+        call()
+    ms = time_calls(call, 20, flush, torch.cuda.current_stream())
+    nb = decode_bytes(b)
+    t = statistics.mean(ms) * 1e-3
+    peak, kind = measured_peak()
+    del b, ws
+    torch.cuda.empty_cache()
+    return {"workload": "long_context: batch 8, 64/8 x 128 bf16, seq_lens U[32768,131072], "
+                        "1% keys x8, 512-token partitions (pa_decode_partitioned + merge)",
+            "seqs_per_s": 8 / t, "us_per_call": t * 1e6, "kv_gbs": nb["kv"] / t / 1e9,
+            "achieved_gbs": nb["total"] / t / 1e9, "frac_of_peak": nb["total"] / t / 1e9 / peak,
+            "peak_kind": kind, "bytes": nb}
+
+
+def paging_overhead_arm(args, device, flush, pa):
+    """Decode time with a random block table over the same time with the
+    same data in contiguous blocks (an identity table), batch 64 x 512..2048."""
+    b = wl.llama8b_uniform(device=device, canary=False)
+    nbk = [math.ceil(int(L) / 16) for L in b.seq_lens]
+    ident = np.full_like(b.block_tables, wl.PAD)
+    kc = torch.zeros_like(b.k_cache)
+    vc = torch.zeros_like(b.v_cache)
+    nxt = 0
+    for s, n in enumerate(nbk):
+        src = torch.from_numpy(b.block_tables[s, :n].astype(np.int64)).to(device)
+        kc[nxt:nxt + n] = b.k_cache[src]
+        vc[nxt:nxt + n] = b.v_cache[src]
+        ident[s, :n] = np.arange(nxt, nxt + n)
+        nxt += n
+    out = torch.empty_like(b.q)
+    sl = torch.from_numpy(b.seq_lens).to(device)
+    bt_r = torch.from_numpy(b.block_tables).to(device)
+    bt_i = torch.from_numpy(ident).to(device)
+    res = {}
+    for name, (bt, k, v) in {"random": (bt_r, b.k_cache, b.v_cache),
+                             "identity": (bt_i, kc, vc)}.items():
+        def call(bt=bt, k=k, v=v):
+            pa.pa_decode(out, b.q, k, v, bt, sl, b.scale, b.num_kv_heads)
+        for _ in range(3):
+            call()
+        res[name] = statistics.median(time_calls(call, 30, flush, torch.cuda.current_stream()))
+    del b, kc, vc
+    torch.cuda.empty_cache()
+    return {"workload": "llama8b_uniform: batch 64, 32/8 x 128 bf16, seq_lens U[512,2048]",
+            "random_table_us": res["random"] * 1e3, "identity_table_us": res["identity"] * 1e3,
+            "overhead": res["random"] / res["identity"] - 1.0}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(n_seqs: int):
+    """The first n_seqs sequences of the serving-mix batch (same seeded
+    lengths), built on the host, plus the full batch's total token count."""
+    rng = np.random.default_rng(3)
+    lens = wl.lognormal_lengths(rng, 256)
+    sel = lens[:n_seqs]
+    fl = wl.FreeList(int(sum(math.ceil(int(x) / 16) for x in sel)) + 8,
+                     np.random.default_rng(33))
+    tables = [fl.allocate(int(x)) for x in sel]
+    b = wl.build_batch("serving_mix_sample", ctx_lens=sel - 1, num_heads=32,
+                       num_kv_heads=8, head_dim=128, dtype="bf16",
+                       num_blocks=len(fl.free) + sum(map(len, tables)), tables=tables,
+                       seed=3, device="cpu", canary=False, new_in_pool=True,
+                       q_std=1.0, kv_std=0.5)
+    return b, int(lens.sum())
+
+
+def run_oracle_timed(b, batch_tokens: int, budget_s: float, threads: int):
+    """Repeat the oracle's decode of the sample until `budget_s` elapsed;
+    scale time per attended token to the full 256-sequence batch."""
+    import oracle
+    pr = (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale, b.num_kv_heads,
+          b.dtype)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(*pr, nthreads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    sample_tokens = int(b.seq_lens.sum())
+    t_batch = el / reps * batch_tokens / sample_tokens
+    return 256 / t_batch, reps, el
+
+
+def cpu_baseline(budget_s: float, n_seqs: int = 32):
+    import oracle
+    oracle.build()
+    b, batch_tokens = oracle_sample(n_seqs)
+    cores = os.cpu_count() or 1
+    v, reps, el = run_oracle_timed(b, batch_tokens, budget_s, cores)
+    v1, reps1, el1 = run_oracle_timed(b, batch_tokens, max(1.0, budget_s / 4), 1)
+    return {"value": v, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n_seqs} of the 256 serving-mix sequences "
+                      f"({int(b.seq_lens.sum())} of {batch_tokens} tokens), decode only, "
+                      f"{reps} repetitions in {el:.1f} s, scaled per attended token to the "
+                      f"full batch",
+            "single_thread_value": v1}
+
+
+def reference_arm(args):
+    """The oracle as the reference implementation, on the host cores.  Each
+    step decodes a sample of the batch, sized so that the whole run takes
+    about --ref-budget seconds."""
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    probe, _ = oracle_sample(4)
+    t0 = time.perf_counter()
+    oracle.decode(probe.q, probe.k_cache, probe.v_cache, probe.block_tables, probe.seq_lens,
+                  probe.scale, probe.num_kv_heads, probe.dtype, nthreads=cores)
+    per_tok = (time.perf_counter() - t0) / int(probe.seq_lens.sum())
+    mean_tokens = 149625 / 256
+    per_step = args.ref_budget / (args.steps + args.warmup)
+    n = int(max(2, min(args.ref_seqs, per_step / (per_tok * mean_tokens))))
+    b, batch_tokens = oracle_sample(n)
+    for _ in range(args.warmup):
+        oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
+                      b.num_kv_heads, b.dtype, nthreads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
+                      b.num_kv_heads, b.dtype, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    per_tok = sum(times) / int(b.seq_lens.sum()) / len(times)
+    t_step = per_tok * batch_tokens                 # one full 256-sequence step
+    value = 256 / t_step
+    sample = (f"first {n} of the 256 serving-mix sequences "
+              f"({int(b.seq_lens.sum())} of {batch_tokens} tokens) per step, fp64 oracle "
+              f"decode with {cores} threads, scaled per attended token to the full batch")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; no dataset)",
+        "config": {"workload": WORKLOAD, "global_batch": 256},
+        "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--ref-seqs", type=int, default=32,
+                    help="at most this many sequences per reference-arm step")
+    ap.add_argument("--ref-budget", type=float, default=90.0,
+                    help="approximate seconds of oracle work for the reference arm")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the long-context and paging-overhead measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl" if torch.cuda.is_available() else "gloo")
+    device = torch.device("cuda", local)
+    result, _ = gpu_arm(args, rank, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) PagedAttention decode library.
+ *
+ * The library implements the data-parallel hot path of a paged KV cache as
+ * described in "vLLM: Architecture, PagedAttention & Internals" (LLM stack
+ * book 7.3) and "vLLM: High-Throughput Serving with PagedAttention" (lesson 13.15):
+ *
+ *   pa_reshape_and_cache   scatter each step's new K/V rows into their slots
+ *   pa_decode              one query token per sequence attends over its
+ *                          paged context, walking the block table
+ *   pa_decode_partitioned  the same attention split into fixed token
+ *                          partitions whose results are merged by
+ *                          log-sum-exp (for long contexts)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every pointer argument except `workspace_bytes`-style sizes is a
+ * DEVICE pointer on the current CUDA device.  The caller owns all memory,
+ * including the workspace of pa_decode_partitioned; the library allocates
+ * nothing and frees nothing.
+ *
+ * Layouts (elements, row-major):
+ *   k_cache, v_cache : [num_blocks, num_kv_heads, block_size, head_dim],
+ *                      contiguous; a (physical block, KV head) tile is one
+ *                      contiguous run of block_size * head_dim elements.
+ *   q                : [num_seqs, num_heads, head_dim]; heads contiguous,
+ *                      sequence stride q_seq_stride (>= num_heads*head_dim).
+ *   out              : [num_seqs, num_heads, head_dim], contiguous.
+ *   k, v (new rows)  : [num_tokens, num_kv_heads, head_dim]; heads
+ *                      contiguous, token stride k_token_stride /
+ *                      v_token_stride.
+ *   block_tables     : int32 [num_seqs, max_blocks_per_seq]; entry
+ *                      [s][i] is the physical block holding tokens
+ *                      16*i .. 16*i+15 of sequence s.  Entries at and past
+ *                      ceil(seq_lens[s] / block_size) are never read.
+ *   seq_lens         : int32 [num_seqs], tokens each sequence attends over.
+ *   slot_mapping     : int64 [num_tokens]; slot = block * block_size + row;
+ *                      a negative slot marks a padding token (skipped).
+ *
+ * Query head h reads KV head h / (num_heads / num_kv_heads) (grouped-query
+ * attention with consecutive query heads sharing a KV head).  A sequence
+ * with seq_len 0 produces zeros.
+ *
+ * dtype (pa_dtype) is the storage type of q, out, k, v and both caches (all
+ * the same).  Arithmetic is fp32; out is rounded to nearest-even.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Every call only enqueues kernels on it and never synchronises, except
+ * pa_device_error, which reads device memory synchronously.
+ *
+ * Errors.  Calls return PA_OK (0) or a negative pa_status; nothing is
+ * launched when the host-side checks fail.  Contents of device arrays are not
+ * inspected on the host.  Instead the kernels range-check every block id,
+ * slot and sequence length they read, skip the offending access and set a bit
+ * in a sticky device-side error word (PA_DEVERR_*), read and cleared with
+ * pa_device_error.  No input can make a kernel read or write outside the
+ * buffers described by the arguments.
+ *
+ * Thread safety.  Calls may be made from any host thread; the only shared
+ * state is the device error word.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_F32 = 0,
+    PA_BF16 = 1,
+    PA_F16 = 2
+} pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,   /* NULL pointer, bad size, misaligned pointer */
+    PA_ERR_UNSUPPORTED = -2,   /* head_dim, GQA group, block_size or dtype not built */
+    PA_ERR_WORKSPACE = -3,     /* workspace missing or too small */
+    PA_ERR_CUDA = -4           /* a CUDA runtime call or launch failed */
+} pa_status;
+
+/* bits of the device error word */
+#define PA_DEVERR_BLOCK_ID   0x1u  /* a block-table entry outside [0, num_blocks) was skipped */
+#define PA_DEVERR_SEQ_LEN    0x2u  /* a seq_len < 0 or > max_blocks_per_seq*block_size (or past
+                                      max_seq_len in the partitioned call) was clamped */
+#define PA_DEVERR_SLOT       0x4u  /* a slot >= num_blocks*block_size was skipped */
+#define PA_DEVERR_TIMEOUT    0x8u  /* a wait on an asynchronous copy exceeded its limit */
+
+/*
+ * pa_reshape_and_cache -- write the step's new keys and values into the cache.
+ *
+ * Defined in "vLLM: Architecture, PagedAttention & Internals", *The forward
+ * step in detail*: the runner computes, for each token being written, the
+ * physical slot (block * block_size + offset) and the attention layer first
+ * scatters the fresh K and V there.  For every token t with slot_mapping[t]
+ * >= 0, the rows k[t][j][:] and v[t][j][:] of every KV head j are copied bit
+ * for bit to k_cache[slot/bs][j][slot%bs][:] and v_cache[...]; nothing else
+ * in the caches changes.  Two tokens with the same slot race (last writer
+ * wins, per element).
+ *
+ * Requirements: num_tokens >= 0 (0 launches nothing); block_size == 16;
+ * head_dim * element size a multiple of 16 bytes; the token strides >=
+ * num_kv_heads*head_dim.
+ */
+int pa_reshape_and_cache(const void *k, const void *v, void *k_cache,
+                         void *v_cache, const int64_t *slot_mapping,
+                         int64_t num_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, int64_t k_token_stride,
+                         int64_t v_token_stride, int64_t num_blocks,
+                         int32_t block_size, int32_t dtype, void *stream);
+
+/*
+ * pa_decode -- decode-step paged attention.
+ *
+ * Defined in "vLLM: Architecture, PagedAttention & Internals", *PagedAttention
+ * in one paragraph* (the kernel gathers K and V block by block through the
+ * block table; the arithmetic of attention is unchanged) and "vLLM:
+ * High-Throughput Serving with PagedAttention", *PagedAttention, the core
+ * idea* (step 4, attend through the table).
+ * For every sequence s and query head h:
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . K_s[t]) * V_s[t],
+ *     t = 0 .. seq_lens[s]-1, K_s[t] = k_cache[bt[s][t/16]][h/G][t%16].
+ * The softmax is evaluated online (running maximum and sum in fp32), which is
+ * exact up to rounding.
+ *
+ * Requirements: block_size == 16; head_dim in {64, 128}; num_heads a
+ * multiple of num_kv_heads with G = num_heads/num_kv_heads in {1, 2, 4, 8};
+ * num_seqs <= 65535; num_kv_heads <= 65535; k_cache and v_cache 16-byte
+ * aligned.  num_seqs == 0 launches nothing.
+ */
+int pa_decode(void *out, const void *q, const void *k_cache,
+              const void *v_cache, const int32_t *block_tables,
+              const int32_t *seq_lens, int32_t num_seqs, int32_t num_heads,
+              int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+              int32_t block_size, int32_t max_blocks_per_seq,
+              int64_t q_seq_stride, float scale, int32_t dtype, void *stream);
+
+/*
+ * pa_decode_split -- pa_decode with an explicit work split: each (sequence,
+ * KV head) is processed by a cluster of `splits` thread blocks (1, 2, 4 or 8)
+ * whose partial results are merged on chip.  splits == 0 picks the split from
+ * the problem shape (what pa_decode does).  The result does not depend on the
+ * thread count within a block, but its rounding may differ between split
+ * counts.
+ */
+int pa_decode_split(void *out, const void *q, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables,
+                    const int32_t *seq_lens, int32_t num_seqs,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int64_t num_blocks, int32_t block_size,
+                    int32_t max_blocks_per_seq, int64_t q_seq_stride,
+                    float scale, int32_t dtype, int32_t splits, void *stream);
+
+/*
+ * pa_decode_partitioned_workspace_size -- bytes of workspace that
+ * pa_decode_partitioned needs for these sizes.  Returns 0 on invalid sizes.
+ *
+ * Workspace layout (fp32, documented so that callers and tests can read the
+ * per-partition results; P = ceil(max_seq_len / partition_size)):
+ *   o_part [num_seqs][num_heads][P][head_dim]   normalised partial outputs
+ *   m_part [num_seqs][num_heads][P]             max of scale*q.k in the
+ *                                               partition (natural units)
+ *   l_part [num_seqs][num_heads][P]             sum of exp(scale*q.k - m)
+ * each array starting on a 256-byte boundary in that order.  Entries of
+ * partitions past a sequence's last one are not written.
+ */
+size_t pa_decode_partitioned_workspace_size(int32_t num_seqs,
+                                            int32_t num_heads,
+                                            int32_t head_dim,
+                                            int32_t max_seq_len,
+                                            int32_t partition_size);
+
+/*
+ * pa_decode_partitioned -- split-KV decode for long contexts.
+ *
+ * Same result as pa_decode.  The tokens of each sequence are cut into
+ * partitions of partition_size tokens (a multiple of 16); one thread block
+ * per (sequence, KV head, partition) writes that partition's softmax
+ * statistics (m_p, l_p) and normalised output o_p to the workspace, and a
+ * second kernel merges them:  M = max_p m_p,  c_p = l_p exp(m_p - M),
+ * out = sum_p c_p o_p / sum_p c_p.  The streaming softmax this rests on is
+ * named in "vLLM" (stanleyjacob.dev), Part IV, *Stage 6: The forward pass*
+ * (the kernel streams through a sequence it never holds in one piece).
+ *
+ * max_seq_len bounds seq_lens (it sizes the grid and the workspace); a
+ * larger seq_len is clamped and flagged PA_DEVERR_SEQ_LEN.
+ * Requirements as pa_decode, plus partition_size a positive multiple of 16
+ * and workspace_bytes >= pa_decode_partitioned_workspace_size(...); the
+ * workspace must be 256-byte aligned.
+ */
+int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int32_t num_seqs,
+                          int32_t num_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int64_t num_blocks,
+                          int32_t block_size, int32_t max_blocks_per_seq,
+                          int64_t q_seq_stride, float scale, int32_t dtype,
+                          int32_t partition_size, int32_t max_seq_len,
+                          void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* Human-readable text of a pa_status (static storage). */
+const char *pa_status_string(int status);
+
+/*
+ * pa_device_error -- read the sticky device error word of the current device
+ * into *flags (PA_DEVERR_* bits) and clear it when `clear` is non-zero.
+ * Synchronises the device first.  Returns PA_OK or PA_ERR_CUDA.
+ */
+int pa_device_error(uint32_t *flags, int clear);
+
+/* ABI version of this header (increments on any signature change). */
+int pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

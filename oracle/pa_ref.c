@@ -14,7 +14,7 @@
  *
  *  - Decode attention (same page, *PagedAttention in one paragraph*: "the
  *    arithmetic of attention is unchanged -- only the addressing is
- *    indirected"; "How does vLLM work", *PagedAttention, the core idea*,
+ *    indirected"; "vLLM: High-Throughput Serving with PagedAttention" (lesson 13.15), *PagedAttention, the core idea*,
  *    step 4): for sequence s and query head h, gather K and V of tokens
  *    0..L_s-1 through the block table into contiguous fp64 arrays, then run
  *    textbook softmax attention:
@@ -79,7 +79,7 @@ static double load_elem(const void *base, int64_t idx, int dtype) {
 
 static int elem_bytes(int dtype) { return dtype == REF_F32 ? 4 : 2; }
 
-/* ---- sizes ("How does vLLM work", *The problem: the KV cache eats GPU
+/* ---- sizes ("vLLM: High-Throughput Serving with PagedAttention" (lesson 13.15), *The problem: the KV cache eats GPU
  * memory*; "vLLM: Architecture, PagedAttention & Internals", *How many blocks
  * exist?*) --------------------------------------------------------------- */
 

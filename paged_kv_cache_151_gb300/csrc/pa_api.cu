@@ -1,0 +1,291 @@
+// pa_api.cu -- the C ABI (include/pa.h): host-side argument checks, launch
+// configuration and dispatch.  No entry point allocates, frees or
+// synchronises (except pa_device_error).
+#include <atomic>
+#include <cstring>
+
+#include "../../include/pa.h"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+int sm_count_of_current_device() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace pa
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elem_size(int32_t dtype) {
+    switch (dtype) {
+        case PA_F32: return 4;
+        case PA_BF16: return 2;
+        case PA_F16: return 2;
+        default: return 0;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Checks shared by the decode entry points.
+int check_decode_args(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                      int64_t q_seq_stride, float scale, int32_t dtype) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        num_blocks < 0 || max_blocks_per_seq < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (elem_size(dtype) == 0) return PA_ERR_UNSUPPORTED;
+    if (num_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (q_seq_stride < (int64_t)num_heads * head_dim) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+    if (!(scale == scale)) return PA_ERR_INVALID_ARG;        // NaN scale
+    if (num_blocks > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+cudaError_t run_decode(const pa::DecodeParams &p, int dtype, int D, int G, bool partial,
+                       dim3 grid, int splits, cudaStream_t st) {
+    switch (dtype) {
+        case PA_F32: return pa::decode_f32(p, D, G, partial, grid, splits, st);
+        case PA_BF16: return pa::decode_bf16(p, D, G, partial, grid, splits, st);
+        default: return pa::decode_f16(p, D, G, partial, grid, splits, st);
+    }
+}
+
+cudaError_t run_merge(const pa::MergeParams &p, int dtype, int num_seqs, cudaStream_t st) {
+    switch (dtype) {
+        case PA_F32: return pa::merge_f32(p, num_seqs, st);
+        case PA_BF16: return pa::merge_bf16(p, num_seqs, st);
+        default: return pa::merge_f16(p, num_seqs, st);
+    }
+}
+
+// Cluster split of one (sequence, KV head) when the caller leaves it open:
+// enough thread blocks to fill the GPU a few times over, and no more than
+// about 64 blocks (1024 tokens) of the longest possible sequence per split.
+int auto_splits(int32_t num_seqs, int32_t num_kv_heads, int32_t max_blocks_per_seq) {
+    int sms = pa::sm_count_of_current_device();
+    if (sms <= 0) sms = 152;
+    const int64_t units = (int64_t)num_seqs * num_kv_heads;
+    const int64_t slots = (int64_t)sms * 2;        // resident thread blocks at 2 per SM
+    int c = 1;
+    while (c < 8 && (units * c < 2 * slots || max_blocks_per_seq / c > 64)) c *= 2;
+    return c;
+}
+
+int decode_common(void *out, const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                  int64_t q_seq_stride, float scale, int32_t dtype, int32_t splits,
+                  void *stream) {
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_seq_stride, scale, dtype);
+    if (rc != PA_OK || num_seqs == 0) return rc;
+    if (splits < 0 || splits > 8 || (splits & (splits - 1))) return PA_ERR_INVALID_ARG;
+    if (splits == 0) splits = auto_splits(num_seqs, num_kv_heads, max_blocks_per_seq);
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.block_tables = block_tables; p.seq_lens = seq_lens;
+    p.num_blocks = num_blocks; p.q_seq_stride = q_seq_stride;
+    p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_log2 = scale * pa::LOG2E;
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    const int G = num_heads / num_kv_heads;
+    dim3 grid((unsigned)splits, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    cudaError_t e = run_decode(p, dtype, head_dim, G, false, grid, splits,
+                               static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+struct WorkspaceLayout {
+    size_t o, m, l, total;
+};
+
+bool workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                      int32_t max_seq_len, int32_t partition_size, WorkspaceLayout *w) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+        partition_size <= 0 || partition_size % 16)
+        return false;
+    const size_t P = (size_t)((max_seq_len + (int64_t)partition_size - 1) / partition_size);
+    const size_t rows = (size_t)num_seqs * num_heads * (P > 0 ? P : 1);
+    w->o = 0;
+    w->m = align_up(rows * head_dim * sizeof(float));
+    w->l = w->m + align_up(rows * sizeof(float));
+    w->total = w->l + align_up(rows * sizeof(float));
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_abi_version(void) { return 1; }
+
+const char *pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_WORKSPACE: return "workspace missing or too small";
+        case PA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens,
+                         int32_t num_kv_heads, int32_t head_dim, int64_t k_token_stride,
+                         int64_t v_token_stride, int64_t num_blocks, int32_t block_size,
+                         int32_t dtype, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (es == 0) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (k_token_stride < row || v_token_stride < row) return PA_ERR_INVALID_ARG;
+    const int64_t row_bytes = (int64_t)head_dim * es;
+    if (row_bytes % 16 || row_bytes > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) %
+        es)
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = pa::reshape_and_cache(
+        k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, (int)row_bytes,
+        k_token_stride * es, v_token_stride * es, num_blocks * block_size,
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+              int32_t block_size, int32_t max_blocks_per_seq, int64_t q_seq_stride,
+              float scale, int32_t dtype, void *stream) {
+    return decode_common(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, q_seq_stride, scale, dtype, 0, stream);
+}
+
+int pa_decode_split(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                    int64_t q_seq_stride, float scale, int32_t dtype, int32_t splits,
+                    void *stream) {
+    return decode_common(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, q_seq_stride, scale, dtype, splits, stream);
+}
+
+size_t pa_decode_partitioned_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                            int32_t head_dim, int32_t max_seq_len,
+                                            int32_t partition_size) {
+    WorkspaceLayout w;
+    if (!workspace_layout(num_seqs, num_heads, head_dim, max_seq_len, partition_size, &w))
+        return 0;
+    return w.total;
+}
+
+int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int32_t num_seqs, int32_t num_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                          int32_t block_size, int32_t max_blocks_per_seq,
+                          int64_t q_seq_stride, float scale, int32_t dtype,
+                          int32_t partition_size, int32_t max_seq_len, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_seq_stride, scale, dtype);
+    if (rc != PA_OK) return rc;
+    if (partition_size <= 0 || partition_size % 16 || max_seq_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    WorkspaceLayout w;
+    if (!workspace_layout(num_seqs, num_heads, head_dim, max_seq_len, partition_size, &w))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < w.total ||
+        (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+        return PA_ERR_WORKSPACE;
+    const int64_t P64 = ((int64_t)max_seq_len + partition_size - 1) / partition_size;
+    const int P = (int)(P64 > 0 ? P64 : 1);
+    if (P64 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.block_tables = block_tables; p.seq_lens = seq_lens;
+    p.part_o = reinterpret_cast<float *>(ws + w.o);
+    p.part_m = reinterpret_cast<float *>(ws + w.m);
+    p.part_l = reinterpret_cast<float *>(ws + w.l);
+    p.num_blocks = num_blocks; p.q_seq_stride = q_seq_stride;
+    p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.partition_blocks = partition_size / 16;
+    p.max_parts = P;
+    p.max_seq_len = max_seq_len;
+    p.scale_log2 = scale * pa::LOG2E;
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int G = num_heads / num_kv_heads;
+    dim3 grid((unsigned)P, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    cudaError_t e = run_decode(p, dtype, head_dim, G, true, grid, 1, st);
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+
+    pa::MergeParams mp;
+    mp.out = out;
+    mp.part_o = p.part_o; mp.part_m = p.part_m; mp.part_l = p.part_l;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads; mp.head_dim = head_dim;
+    mp.max_parts = P; mp.partition_size = partition_size;
+    const int64_t cap = (int64_t)max_blocks_per_seq * 16;
+    mp.seq_cap = (int)(max_seq_len < cap ? max_seq_len : cap);
+    e = run_merge(mp, dtype, num_seqs, st);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_device_error(uint32_t *flags, int clear) {
+    if (!flags) return PA_ERR_INVALID_ARG;
+    unsigned int f = 0;
+    cudaError_t e = pa::read_device_error(&f, clear != 0);
+    *flags = f;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"

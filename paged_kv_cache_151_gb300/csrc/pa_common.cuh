@@ -1,0 +1,206 @@
+// pa_common.cuh -- device helpers shared by the kernels: element types,
+// mbarrier / bulk-copy / cluster PTX wrappers, the exp2 instruction and the
+// device error word.  Written for sm_103a (GB300).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// ---- device error word (sticky; read and cleared by pa_device_error) ------
+// Kernels receive its address as a parameter (it lives in one translation
+// unit; the library is built without relocatable device code).
+__device__ __forceinline__ void set_error(unsigned int *err, unsigned int bits) {
+    atomicOr(err, bits);
+}
+
+constexpr unsigned ERR_BLOCK_ID = 0x1u;
+constexpr unsigned ERR_SEQ_LEN = 0x2u;
+constexpr unsigned ERR_SLOT = 0x4u;
+constexpr unsigned ERR_TIMEOUT = 0x8u;
+
+// Wall-clock limit of any wait on an asynchronous copy (ns).
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+// ---- element types --------------------------------------------------------
+// Each 16-byte chunk holds E elements; to_f32 widens them exactly.
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int E = 4;
+    __device__ __forceinline__ static void to_f32(const uint4 &c, float *f) {
+        f[0] = __uint_as_float(c.x); f[1] = __uint_as_float(c.y);
+        f[2] = __uint_as_float(c.z); f[3] = __uint_as_float(c.w);
+    }
+    __device__ __forceinline__ static float load1(const float *p) { return *p; }
+    __device__ __forceinline__ static void store1(float *p, float v) { *p = v; }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int E = 8;
+    // bf16 is the top half of a binary32: widening is a shift / mask.
+    __device__ __forceinline__ static void pair(uint32_t w, float &lo, float &hi) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static void to_f32(const uint4 &c, float *f) {
+        pair(c.x, f[0], f[1]); pair(c.y, f[2], f[3]);
+        pair(c.z, f[4], f[5]); pair(c.w, f[6], f[7]);
+    }
+    __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    __device__ __forceinline__ static void store1(__nv_bfloat16 *p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+template <> struct Elem<__half> {
+    static constexpr int E = 8;
+    __device__ __forceinline__ static void pair(uint32_t w, float &lo, float &hi) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        float2 f = __half22float2(h);
+        lo = f.x; hi = f.y;
+    }
+    __device__ __forceinline__ static void to_f32(const uint4 &c, float *f) {
+        pair(c.x, f[0], f[1]); pair(c.y, f[2], f[3]);
+        pair(c.z, f[4], f[5]); pair(c.w, f[6], f[7]);
+    }
+    __device__ __forceinline__ static float load1(const __half *p) {
+        return __half2float(*p);
+    }
+    __device__ __forceinline__ static void store1(__half *p, float v) {
+        *p = __float2half_rn(v);
+    }
+};
+
+// ---- math -----------------------------------------------------------------
+// 2^x with the hardware approximation instruction (MUFU.EX2): relative error
+// about 2^-22, ex2(-inf) = 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;   // log2(e)
+constexpr float LN2 = 0.6931471805599453f;     // ln(2)
+
+// ---- time -----------------------------------------------------------------
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- shared-memory addresses and mbarriers --------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// make barrier initialisation visible to the async proxy and the cluster
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this thread's prior generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+        :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most WAIT_LIMIT_NS.
+// Returns false (and sets ERR_TIMEOUT) if the limit was reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            set_error(err, ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes`
+// transaction bytes on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once per call (the streamed K/V tiles).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---- clusters -------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// address of the same shared-memory variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+    return out;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+}  // namespace pa

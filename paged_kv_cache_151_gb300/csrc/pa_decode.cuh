@@ -1,0 +1,590 @@
+// pa_decode.cuh -- decode-step paged attention kernels for sm_103a.
+//
+// One thread block handles one (sequence, KV head) -- or one split of it --
+// and all G query heads that share that KV head ("vLLM: Architecture,
+// PagedAttention & Internals", *PagedAttention in one paragraph*: the kernel
+// gathers K and V block by block through the block table; the arithmetic of
+// attention is unchanged).
+//
+// Data movement.  Each warp owns a ring of S stages.  For each 16-token block
+// of its share, lane 0 issues two 1-D bulk copies (cp.async.bulk, the TMA
+// engine without a tensor map) of the block's K and V tiles -- each a
+// contiguous run of rows*head_dim elements in the [block][kv_head][row][d]
+// cache -- into the stage, completing on the stage's mbarrier.  Only the
+// valid rows of a partial last block are copied.  Blocks are dealt to the
+// warps of all CTAs of a cluster round-robin by logical block index, so the
+// reduction order depends only on logical positions, never on where the
+// blocks sit in the pool.
+//
+// Arithmetic per block (fp32):
+//   scores   lane (r, c) reads 16-byte chunk c of row r + RPW*i of the K tile
+//            and multiplies it with the matching slice of the G query
+//            vectors held in registers; the per-lane partial dot products are
+//            summed across the NCH lanes of a row by a shuffle
+//            reduce-scatter (recursive halving), leaving each lane a few
+//            complete scores.  Scores carry scale*log2(e) so that the
+//            softmax can use exp2.
+//   softmax  online: per head a running maximum m and sum l (fp32);
+//            m_new = max(m, block max), alpha = 2^(m - m_new),
+//            p_t = 2^(s_t - m_new), l = alpha*l + sum p_t  ("vLLM"
+//            (stanleyjacob.dev), Part IV, *Stage 6: The forward pass*: the
+//            kernel streams through a sequence it never holds in one piece).
+//   P.V      acc[g][:] = alpha[g]*acc[g][:] + sum_t p[g][t] V[t][:], lane (r, c)
+//            owning chunk c of the output for the rows of its row group.
+// At the end the warps' (m, l, acc) are merged in shared memory and, when the
+// (sequence, KV head) is split over a cluster, across the cluster through
+// distributed shared memory; out = acc / l, rounded to the storage type.
+//
+// The partitioned variant (PARTIAL) gives each thread block one fixed token
+// partition and writes the partition's (m, l, acc/l) to a workspace instead;
+// a second kernel merges the partitions by log-sum-exp.
+#pragma once
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+struct DecodeParams {
+    void *out;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float *part_o;            // PARTIAL: [B][H][max_parts][D]
+    float *part_m;            // PARTIAL: [B][H][max_parts]
+    float *part_l;            // PARTIAL: [B][H][max_parts]
+    long long num_blocks;
+    long long q_seq_stride;   // elements
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int max_blocks;           // block-table row length
+    int partition_blocks;     // PARTIAL: 16-token blocks per partition
+    int max_parts;            // PARTIAL: partitions the workspace holds
+    int max_seq_len;          // PARTIAL: bound on seq_len
+    float scale_log2;         // scale * log2(e)
+    unsigned int *err;        // device error word
+};
+
+template <typename T, int D>
+struct Shape {
+    static constexpr int E = Elem<T>::E;            // elements per 16-byte chunk
+    static constexpr int NCH = D / E;               // chunks per row
+    static constexpr int RPW = 32 / NCH;            // rows per warp-wide chunk load
+    static constexpr int STEPS = 16 / RPW;          // chunk loads per 16-row tile
+    static constexpr int ROW_BYTES = D * (int)sizeof(T);
+    static constexpr int TILE_BYTES = 16 * ROW_BYTES;
+    static constexpr int LOG_NCH = NCH == 8 ? 3 : NCH == 16 ? 4 : 5;
+    static_assert(NCH == 8 || NCH == 16 || NCH == 32, "unsupported head_dim/type");
+};
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Stages per warp: about 24 KiB of K+V in flight per warp, at least 2.
+template <typename T, int D>
+__host__ __device__ constexpr int stages_for() {
+    constexpr int per = 2 * Shape<T, D>::TILE_BYTES;
+    constexpr int s = 24576 / per;
+    return s < 2 ? 2 : (s > 8 ? 8 : s);
+}
+
+template <int G>
+__host__ __device__ constexpr int warp_scratch_floats() {   // scores[16][G], probs[16][G], alpha[G]
+    return ((33 * G + 3) / 4) * 4;
+}
+
+// The stage buffers; after the block loop the same bytes hold the merge data.
+template <typename T, int D, int G, int NW, int S>
+__host__ __device__ constexpr size_t stage_region_bytes() {
+    constexpr size_t stages = (size_t)NW * S * 2 * Shape<T, D>::TILE_BYTES;
+    constexpr size_t merge = (size_t)(NW * (2 * G + G * D) + 2 * G + G * D) * 4;
+    constexpr size_t region = stages > merge ? stages : merge;
+    return (region + 127) / 128 * 128;
+}
+
+// stage region | mbarriers [NW*S] | q [G*D] fp32 | per-warp scratch
+template <typename T, int D, int G, int NW, int S>
+__host__ __device__ constexpr size_t decode_smem_bytes() {
+    return stage_region_bytes<T, D, G, NW, S>() + (size_t)NW * S * 8 +
+           (size_t)G * D * 4 + (size_t)NW * warp_scratch_floats<G>() * 4;
+}
+
+// Shuffle reduce-scatter of N partial sums across the lanes whose chunk
+// index c differs in the bits of MASK, MASK/2, ..., 1.  At each level a lane
+// keeps half of its values (the upper half when its bit of c is set), adds
+// the partner's copy of that half, and the count halves; once one value is
+// left the remaining levels are a plain butterfly sum.
+template <int N, int MASK>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float *v, int c) {
+        if constexpr (MASK == 0) {
+            return;
+        } else if constexpr (N > 1) {
+            constexpr int H = N / 2;
+            const bool upper = (c & MASK) != 0;
+#pragma unroll
+            for (int i = 0; i < H; ++i) {
+                const float send = upper ? v[i] : v[i + H];
+                const float keep = upper ? v[i + H] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+            }
+            ReduceScatter<H, MASK / 2>::run(v, c);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
+            ReduceScatter<1, MASK / 2>::run(v, c);
+        }
+    }
+};
+
+template <typename T, int D, int G, int NW, int S, bool PARTIAL>
+__global__ void __launch_bounds__(NW * 32)
+decode_kernel(const DecodeParams p) {
+    using Sh = Shape<T, D>;
+    constexpr int E = Sh::E, NCH = Sh::NCH, RPW = Sh::RPW, STEPS = Sh::STEPS;
+    constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
+    // score pass in sub-passes of SUB chunk loads: SUB*G partial sums a lane
+    constexpr int SUB = (STEPS * G <= 32) ? STEPS : (32 / G);
+    constexpr int NSUB = STEPS / SUB;
+    constexpr int NV = SUB * G;
+    constexpr int NVF = NV >= NCH ? NV / NCH : 1;           // scores a lane ends with
+    constexpr int NL = ilog2(NV / NVF);                      // scatter levels
+    // softmax layout: 16*G scores over 32 lanes, VPL rows of one head per lane
+    constexpr int VPL = (16 * G) / 32 >= 1 ? (16 * G) / 32 : 1;
+    constexpr int LPH = 16 / VPL;                            // lanes per head
+    constexpr int WS = warp_scratch_floats<G>();
+    static_assert(STEPS % SUB == 0, "sub-pass split");
+    static_assert(S <= 32, "stage count");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr size_t STAGE_REGION = stage_region_bytes<T, D, G, NW, S>();
+    unsigned char *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGE_REGION);
+    float *qs = reinterpret_cast<float *>(bars + NW * S);
+    float *wscr_all = qs + G * D;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = blockIdx.y, s = blockIdx.z;
+    const int H = p.num_heads, Hkv = p.num_kv_heads;
+
+    // ---- which tokens this block handles ----------------------------------
+    int L = p.seq_lens[s];
+    const int cap = PARTIAL ? min(p.max_seq_len, p.max_blocks * 16) : p.max_blocks * 16;
+    if (L < 0 || L > cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    const int nb = (L + 15) >> 4;
+    int lb_begin = 0, lb_end = nb, rank = 0, nrank = 1;
+    if constexpr (PARTIAL) {
+        lb_begin = blockIdx.x * p.partition_blocks;
+        if (lb_begin >= nb) return;                    // no such partition
+        lb_end = min(nb, lb_begin + p.partition_blocks);
+    } else {
+        rank = (int)cluster_ctarank();
+        nrank = (int)cluster_nctarank();
+    }
+
+    // ---- set-up: barriers and the G query vectors (pre-scaled) -------------
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    {
+        const T *qp = reinterpret_cast<const T *>(p.q) + (long long)s * p.q_seq_stride +
+                      (long long)j * G * D;
+        for (int i = threadIdx.x; i < G * D; i += NW * 32)
+            qs[i] = Elem<T>::load1(qp + i) * p.scale_log2;
+    }
+    __syncthreads();
+
+    const int r = lane / NCH, c = lane % NCH;
+    float qreg[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < E; ++e) qreg[g][e] = qs[g * D + c * E + e];
+
+    float *Sc = wscr_all + warp * WS;         // [16][G] scores (log2 units)
+    float *Pb = Sc + 16 * G;                  // [16][G] probabilities
+    float *Al = Pb + 16 * G;                  // [G] rescale factors
+
+    // ---- this warp's share of the blocks ------------------------------------
+    const int worker = rank * NW + warp, nwk = nrank * NW;
+    const int span = lb_end - lb_begin;
+    const int n_mine = span > worker ? (span - worker + nwk - 1) / nwk : 0;
+    const int32_t *bt_row = p.block_tables + (long long)s * p.max_blocks;
+    auto table_entry = [&](int k) -> int {
+        return k < n_mine ? bt_row[lb_begin + worker + k * nwk] : 0;
+    };
+    // lane i holds the table entry of this warp's block c0 + i (and c0+32+i)
+    int c0 = 0;
+    int tab_cur = table_entry(lane), tab_nxt = table_entry(32 + lane);
+    auto pb_of = [&](int k) -> int {                  // warp-uniform k
+        const int kk = k - c0;
+        const int a = __shfl_sync(0xffffffffu, tab_cur, kk & 31);
+        const int b = __shfl_sync(0xffffffffu, tab_nxt, kk & 31);
+        return kk < 32 ? a : b;
+    };
+    unsigned char *my_stages = stages + (size_t)warp * S * 2 * TILE;
+    uint64_t *my_bars = bars + warp * S;
+    const uint64_t pol = policy_evict_first();
+    const unsigned char *kbase = reinterpret_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vbase = reinterpret_cast<const unsigned char *>(p.v_cache);
+
+    auto rows_of = [&](int k) -> int {
+        const int lb = lb_begin + worker + k * nwk;
+        return min(16, L - lb * 16);
+    };
+    auto issue = [&](int k, int pbk) {                // lane 0 only
+        uint64_t *bar = &my_bars[k % S];
+        if (pbk < 0 || (long long)pbk >= p.num_blocks) {
+            set_error(p.err, ERR_BLOCK_ID);
+            mbar_arrive(bar);                          // completes the phase, no data
+            return;
+        }
+        const uint32_t bytes = (uint32_t)(rows_of(k) * ROWB);
+        const size_t off = ((size_t)pbk * Hkv + j) * TILE;
+        unsigned char *dst = my_stages + (size_t)(k % S) * 2 * TILE;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s(dst, kbase + off, bytes, bar, pol);
+        bulk_g2s(dst + TILE, vbase + off, bytes, bar, pol);
+    };
+
+    // prologue: fill the ring
+    const int pre = n_mine < S ? n_mine : S;
+    for (int k = 0; k < pre; ++k) {
+        const int pbk = pb_of(k);
+        if (lane == 0) issue(k, pbk);
+    }
+
+    // softmax-layout identity of this lane
+    const int idx0 = (lane * VPL) % (16 * G);
+    const int g_sm = idx0 / 16, row0 = idx0 % 16;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+
+    int k_done = 0;
+    bool ok = true;
+    for (int k = 0; k < n_mine; ++k) {
+        if (k - c0 == 32) {
+            c0 += 32;
+            tab_cur = tab_nxt;
+            tab_nxt = table_entry(c0 + 32 + lane);
+        }
+        const int st = k % S;
+        const int pbk = pb_of(k);
+        const int rows = rows_of(k);
+        const bool waited = mbar_wait_bounded(&my_bars[st], (uint32_t)((k / S) & 1), p.err);
+        if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
+        k_done = k + 1;
+        if (pbk >= 0 && (long long)pbk < p.num_blocks) {
+            const unsigned char *Kt = my_stages + (size_t)st * 2 * TILE;
+            const unsigned char *Vt = Kt + TILE;
+
+            // -- scores: s[row][g] = sum_d qs[g][d] * K[row][d]
+#pragma unroll
+            for (int sp = 0; sp < NSUB; ++sp) {
+                float v[NV];
+#pragma unroll
+                for (int i = 0; i < SUB; ++i) {
+                    const int row = (sp * SUB + i) * RPW + r;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(Kt + row * ROWB + c * 16);
+                    float kf[E];
+                    Elem<T>::to_f32(raw, kf);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) a = fmaf(qreg[g][e], kf[e], a);
+                        v[i * G + g] = a;
+                    }
+                }
+                ReduceScatter<NV, NCH / 2>::run(v, c);
+                constexpr int LOWB = Sh::LOG_NCH - NL;   // c bits not used by the scatter
+                if ((c & ((1 << LOWB) - 1)) == 0) {
+                    const int cidx = c >> LOWB;
+#pragma unroll
+                    for (int f = 0; f < NVF; ++f) {
+                        const int vi = cidx * NVF + f;
+                        const int il = vi / G, g = vi % G;
+                        const int row = (sp * SUB + il) * RPW + r;
+                        Sc[row * G + g] = v[f];
+                    }
+                }
+            }
+            __syncwarp();
+
+            // -- online softmax
+            {
+                float sc[VPL];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    const int row = row0 + u;
+                    const float x = Sc[row * G + g_sm];
+                    sc[u] = row < rows ? x : -INFINITY;
+                    mx = fmaxf(mx, sc[u]);
+                }
+#pragma unroll
+                for (int m = 1; m < LPH; m <<= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+                const float m_new = fmaxf(m_run, mx);
+                const float alpha = ex2(m_run - m_new);
+                float psum = 0.f;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    const float pv = ex2(sc[u] - m_new);
+                    Pb[(row0 + u) * G + g_sm] = pv;
+                    psum += pv;
+                }
+                l_run = l_run * alpha + psum;
+                m_run = m_new;
+                if ((lane % LPH) == 0) Al[g_sm] = alpha;
+            }
+            __syncwarp();
+
+            // -- P.V
+            {
+                float al[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) al[g] = Al[g];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[g][e] *= al[g];
+#pragma unroll
+                for (int i = 0; i < STEPS; ++i) {
+                    const int row = i * RPW + r;
+                    if (row < rows) {
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(Vt + row * ROWB + c * 16);
+                        float vf[E];
+                        Elem<T>::to_f32(raw, vf);
+                        float pr[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) pr[g] = Pb[row * G + g];
+#pragma unroll
+                        for (int g = 0; g < G; ++g)
+#pragma unroll
+                            for (int e = 0; e < E; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        // -- refill the stage just consumed
+        const int kn = k + S;
+        if (kn < n_mine) {
+            const int pbn = pb_of(kn);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(kn, pbn);
+            }
+        }
+    }
+
+    // ---- after a timeout: wait (bounded) for this warp's copies in flight ----
+    bool drained = true;
+    if (!ok) {
+        const int issued = min(n_mine, k_done + S);
+        for (int k = k_done; k < issued; ++k)
+            drained &= mbar_wait_bounded(&my_bars[k % S], (uint32_t)((k / S) & 1), p.err);
+        drained = __all_sync(0xffffffffu, drained);
+    }
+    const bool cta_ok = __syncthreads_and(drained ? 1 : 0) != 0;
+
+    // ---- warp totals ---------------------------------------------------------
+#pragma unroll
+    for (int m = NCH; m < 32; m <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], m);
+#pragma unroll
+    for (int m = 1; m < LPH; m <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, m);
+
+    // merge region (reuses the stage buffers: every copy has landed)
+    float *Mw = reinterpret_cast<float *>(stages);      // [NW][G]
+    float *Lw = Mw + NW * G;                            // [NW][G]
+    float *Aw = Lw + NW * G;                            // [NW][G][D]
+    float *Mc = Aw + NW * G * D;                        // [G]
+    float *Lc = Mc + G;                                 // [G]
+    float *Oc = Lc + G;                                 // [G][D]
+    if (cta_ok) {
+        if ((lane % LPH) == 0) {
+            Mw[warp * G + g_sm] = m_run;
+            Lw[warp * G + g_sm] = l_run;
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int e = 0; e < E; ++e) Aw[(warp * G + g) * D + c * E + e] = acc[g][e];
+        }
+    }
+    __syncthreads();
+
+    const int h0 = j * G;
+    for (int idx = threadIdx.x; idx < G * D && cta_ok; idx += NW * 32) {
+        const int g = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, Mw[w * G + g]);
+        float O = 0.f, Ls = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float mw = Mw[w * G + g];
+                const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+                O = fmaf(f, Aw[(w * G + g) * D + d], O);
+                Ls = fmaf(f, Lw[w * G + g], Ls);
+            }
+        }
+        if constexpr (PARTIAL) {
+            const long long row = ((long long)s * H + h0 + g) * p.max_parts + blockIdx.x;
+            p.part_o[row * D + d] = O / Ls;
+            if (d == 0) {
+                p.part_m[row] = M * LN2;               // natural units
+                p.part_l[row] = Ls;
+            }
+        } else {
+            if (nrank == 1) {
+                T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
+                Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
+            } else {
+                Oc[idx] = O;
+                if (d == 0) { Mc[g] = M; Lc[g] = Ls; }
+            }
+        }
+    }
+
+    if constexpr (!PARTIAL) {
+        if (nrank > 1) {
+            // cross-CTA merge through distributed shared memory: rank r
+            // finalises outputs [r*G*D/n, (r+1)*G*D/n) from every rank's (M, L, O)
+            cluster_sync();
+            const int per = (G * D + nrank - 1) / nrank;
+            const int beg = rank * per, end = min(G * D, beg + per);
+            for (int idx = beg + threadIdx.x; idx < end; idx += NW * 32) {
+                const int g = idx / D, d = idx % D;
+                float M = -INFINITY;
+                for (int q = 0; q < nrank; ++q)
+                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(&Mc[g], q)));
+                float O = 0.f, Ls = 0.f;
+                if (M != -INFINITY) {
+                    for (int q = 0; q < nrank; ++q) {
+                        const float mq = ld_dsmem_f32(map_to_rank(&Mc[g], q));
+                        const float f = mq == -INFINITY ? 0.f : ex2(mq - M);
+                        O = fmaf(f, ld_dsmem_f32(map_to_rank(&Oc[idx], q)), O);
+                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(&Lc[g], q)), Ls);
+                    }
+                }
+                if (cta_ok) {
+                    T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
+                    Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
+                }
+            }
+            cluster_sync();     // keep this CTA's shared memory alive for the peers
+        }
+    }
+}
+
+// ---- log-sum-exp merge of the partitions -----------------------------------
+struct MergeParams {
+    void *out;
+    const float *part_o;
+    const float *part_m;
+    const float *part_l;
+    const int32_t *seq_lens;
+    int num_heads;
+    int head_dim;
+    int max_parts;
+    int partition_size;
+    int seq_cap;              // min(max_seq_len, max_blocks*16)
+};
+
+template <typename T>
+__global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
+    const int h = blockIdx.x, s = blockIdx.y;
+    int L = p.seq_lens[s];
+    L = L < 0 ? 0 : (L > p.seq_cap ? p.seq_cap : L);
+    const int n = (L + p.partition_size - 1) / p.partition_size;
+    const long long row = ((long long)s * p.num_heads + h) * p.max_parts;
+    const float *m = p.part_m + row;
+    const float *l = p.part_l + row;
+    const float *o = p.part_o + row * p.head_dim;
+    float M = -INFINITY;
+    for (int q = 0; q < n; ++q) M = fmaxf(M, m[q]);
+    T *out = reinterpret_cast<T *>(p.out) + ((long long)s * p.num_heads + h) * p.head_dim;
+    for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
+        float O = 0.f, S = 0.f;
+        for (int q = 0; q < n; ++q) {
+            const float cq = l[q] * ex2((m[q] - M) * LOG2E);
+            S += cq;
+            O = fmaf(cq, o[(long long)q * p.head_dim + d], O);
+        }
+        Elem<T>::store1(out + d, n > 0 ? O / S : 0.f);
+    }
+}
+
+// ---- host-side launch helpers ------------------------------------------------
+int sm_count_of_current_device();
+
+template <typename T, int D, int G, bool PARTIAL>
+cudaError_t launch_decode(const DecodeParams &p, dim3 grid, int splits, cudaStream_t st) {
+    constexpr int NW = 4;
+    constexpr int S = stages_for<T, D>();
+    constexpr size_t smem = decode_smem_bytes<T, D, G, NW, S>();
+    auto kern = decode_kernel<T, D, G, NW, S, PARTIAL>;
+    static_assert(smem <= 227 * 1024, "shared memory");
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    if (PARTIAL || splits <= 1) {
+        kern<<<grid, NW * 32, smem, st>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NW * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_merge(const MergeParams &p, int num_seqs, cudaStream_t st) {
+    lse_merge_kernel<T><<<dim3(p.num_heads, num_seqs, 1), 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// Dispatch over (head_dim, group size) for one storage type.  Returns
+// cudaErrorNotSupported for shapes that are not built.
+template <typename T>
+cudaError_t dispatch_decode(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
+                            int splits, cudaStream_t st) {
+#define PA_CASE(DD, GG)                                                         \
+    if (D == DD && G == GG)                                                     \
+        return partial ? launch_decode<T, DD, GG, true>(p, grid, splits, st)    \
+                       : launch_decode<T, DD, GG, false>(p, grid, splits, st);
+    PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
+    PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
+#undef PA_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace pa

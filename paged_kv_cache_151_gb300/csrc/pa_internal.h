@@ -1,0 +1,36 @@
+// pa_internal.h -- declarations shared by the translation units of the
+// library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+struct DecodeParams;
+struct MergeParams;
+
+// per storage type: decode kernels (D in {64,128}, G in {1,2,4,8}) and merge
+cudaError_t decode_f32(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
+                       int splits, cudaStream_t st);
+cudaError_t decode_bf16(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
+                        int splits, cudaStream_t st);
+cudaError_t decode_f16(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
+                       int splits, cudaStream_t st);
+cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
+cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
+cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);
+
+// cache write
+cudaError_t reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                              const int64_t *slot_mapping, int64_t num_tokens,
+                              int num_kv_heads, int row_bytes, int64_t k_tok_stride_bytes,
+                              int64_t v_tok_stride_bytes, int64_t num_slots,
+                              cudaStream_t st);
+
+// device error word
+cudaError_t device_error_ptr(unsigned int **out);
+cudaError_t read_device_error(unsigned int *flags, bool clear);
+int sm_count_of_current_device();
+
+}  // namespace pa

@@ -19,7 +19,7 @@ Layout (the pages leave it open; this is the reading used throughout):
 
 The free-list allocator follows the pages' pattern (a seeded permutation of
 the pool, blocks popped from its end, one block per ``block_size`` tokens;
-"How does vLLM work", *PagedAttention, the core idea*, ``paged_kv.py``), and
+"vLLM: High-Throughput Serving with PagedAttention" (lesson 13.15), *PagedAttention, the core idea*, ``paged_kv.py``), and
 the five named workloads follow the configurations the build is measured on.
 """
 from __future__ import annotations

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_cache_151_gb300 import build as pabuild
+from paged_kv_cache_151_gb300 import pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pabuild.build()
+    return pa.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_decode_partitioned",
+              "pa_decode_partitioned_workspace_size", "pa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_status_strings_and_version(lib):
+    assert pa.pa_abi_version() == 1
+    assert pa.pa_status_string(0) == "ok"
+    assert "invalid" in pa.pa_status_string(-1)
+    assert "unsupported" in pa.pa_status_string(-2)
+    assert "workspace" in pa.pa_status_string(-3)
+
+
+def test_workspace_size_formula(lib):
+    def up(x):
+        return (x + 255) // 256 * 256
+    B, H, D, L, P = 8, 64, 128, 131072, 512
+    parts = L // P
+    rows = B * H * parts
+    expect = up(rows * D * 4) + 2 * up(rows * 4)
+    assert pa.pa_decode_partitioned_workspace_size(B, H, D, L, P) == expect
+    assert pa.pa_decode_partitioned_workspace_size(B, H, D, L, 100) == 0   # not a multiple of 16
+    assert pa.pa_decode_partitioned_workspace_size(0, H, D, L, P) == 0
+
+
+def _decode_status(lib, **kw):
+    args = dict(out=1, q=1, k_cache=16, v_cache=16, block_tables=1, seq_lens=1,
+                num_seqs=4, num_heads=8, num_kv_heads=2, head_dim=64, num_blocks=10,
+                block_size=16, max_blocks=4, q_seq_stride=512, scale=0.125, dtype=0)
+    args.update(kw)
+    a = args
+    return lib.pa_decode(a["out"], a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                         a["seq_lens"], a["num_seqs"], a["num_heads"], a["num_kv_heads"],
+                         a["head_dim"], a["num_blocks"], a["block_size"], a["max_blocks"],
+                         a["q_seq_stride"], a["scale"], a["dtype"], None)
+
+
+def test_host_side_argument_checks(lib):
+    # each of these fails its host check before anything is launched
+    assert _decode_status(lib, out=None) == -1
+    assert _decode_status(lib, num_heads=7) == -1              # not a multiple of H_kv
+    assert _decode_status(lib, head_dim=96) == -2
+    assert _decode_status(lib, block_size=32) == -2
+    assert _decode_status(lib, num_heads=32, num_kv_heads=2, q_seq_stride=32 * 64) == -2  # G=16
+    assert _decode_status(lib, dtype=7) == -2
+    assert _decode_status(lib, q_seq_stride=100) == -1
+    assert _decode_status(lib, k_cache=8) == -1                # not 16-byte aligned
+    assert _decode_status(lib, scale=float("nan")) == -1
+    assert _decode_status(lib, num_seqs=0) == 0                # nothing to do
+    assert _decode_status(lib, num_seqs=-1) == -1
+    rc = lib.pa_reshape_and_cache(1, 1, 1, 1, 1, 0, 2, 64, 128, 128, 10, 16, 0, None)
+    assert rc == 0                                              # zero tokens
+    rc = lib.pa_reshape_and_cache(1, 1, 1, 1, 1, 3, 2, 64, 100, 128, 10, 16, 0, None)
+    assert rc == -1                                             # stride < row
+    rc = lib.pa_reshape_and_cache(1, 1, 1, 1, 1, 3, 2, 4, 8, 8, 10, 16, 1, None)
+    assert rc == -2                                             # 8-byte rows
+    ws = ctypes.c_void_p(256)
+    rc = lib.pa_decode_partitioned(1, 1, 16, 16, 1, 1, 4, 8, 2, 64, 10, 16, 4, 512,
+                                   0.125, 0, 512, 64, ws, 16, None)
+    assert rc == -3                                             # workspace too small
+    rc = lib.pa_decode_partitioned(1, 1, 16, 16, 1, 1, 4, 8, 2, 64, 10, 16, 4, 512,
+                                   0.125, 0, 100, 64, ws, 1 << 20, None)
+    assert rc == -1                                             # partition not x16
