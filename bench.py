@@ -264,7 +264,7 @@ def gpu_arm(args, rank, world, device):
             "num_blocks": b.num_blocks,
             "l2": f"flushed between steps ({flush_bytes >> 20} MiB write, outside the events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "decode_splits": "auto",
+            "decode_kernel": "persistent (LPT-sorted units, per-warp bulk-copy rings)",
         },
         "kv_gbs": nbytes["kv"] / (dec_mean * 1e-3) / 1e9,
         "decode_us": dec_mean * 1e3,
@@ -273,7 +273,7 @@ def gpu_arm(args, rank, world, device):
         "cache_write_gbs": wbytes / (statistics.mean(write_ms) * 1e-3) / 1e9,
         "decode_bytes": nbytes,
         "roofline": {
-            "kernel": "decode_kernel<bf16,128,4> (pa_decode)",
+            "kernel": "decode_persistent_kernel<bf16,128,4> (pa_decode)",
             "bound": "hbm",
             "achieved": achieved,
             "peak": peak,
@@ -495,6 +495,45 @@ def reference_arm(args):
 
 # ---------------------------------------------------------------------------
 
+def single_kernel(args, device):
+    """Launch one kernel alone (for profilers): warm-up, then --steps launches
+    timed with CUDA events, L2 flushed before each.  Prints a short JSON line
+    (not a benchmark line)."""
+    from paged_kv_cache_151_gb300 import pa
+    torch.cuda.set_device(device)
+    pa.load()
+    flush, _ = make_flush(device)
+    if args.only == "partitioned":
+        b = wl.long_context(device=device, canary=False)
+        bt, sl, _ = b.torch_tables(device)
+        msl = 131072
+        ws = torch.empty(pa.pa_decode_partitioned_workspace_size(
+            b.num_seqs, b.num_heads, b.head_dim, msl, 512), dtype=torch.uint8, device=device)
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode_partitioned(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale,
+                                     b.num_kv_heads, 512, msl, ws)
+    else:
+        b = wl.serving_mix(device=device, canary=False)
+        bt, sl, sm = b.torch_tables(device)
+        out = torch.empty_like(b.q)
+        if args.only == "decode":
+            def call():
+                pa.pa_decode(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale, b.num_kv_heads)
+        else:
+            def call():
+                pa.pa_reshape_and_cache(b.k_new, b.v_new, b.k_cache, b.v_cache, sm)
+    for _ in range(args.warmup):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    ms = time_calls(call, args.steps, flush, torch.cuda.current_stream())
+    nb = decode_bytes(b)
+    print(json.dumps({"only": args.only, "workload": b.name, "us": [m * 1e3 for m in ms],
+                      "bytes": nb, "device_error_flags": pa.pa_device_error(clear=True)}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -511,6 +550,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the long-context and paging-overhead measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["decode", "partitioned", "cache_write"],
+                    help="launch one kernel alone (for profiling); prints timings only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -522,6 +563,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    if args.only:
+        single_kernel(args, torch.device("cuda", local))
         return
 
     if world > 1:

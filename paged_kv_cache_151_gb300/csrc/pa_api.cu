@@ -3,6 +3,10 @@
 // synchronises (except pa_device_error).
 #include <atomic>
 #include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "../../include/pa.h"
 #include "pa_decode.cuh"
@@ -69,13 +73,72 @@ int check_decode_args(void *out, const void *q, const void *k_cache, const void 
     return PA_OK;
 }
 
-cudaError_t run_decode(const pa::DecodeParams &p, int dtype, int D, int G, bool partial,
-                       dim3 grid, int splits, cudaStream_t st) {
+cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 grid,
+                      int splits, cudaStream_t st) {
     switch (dtype) {
-        case PA_F32: return pa::decode_f32(p, D, G, partial, grid, splits, st);
-        case PA_BF16: return pa::decode_bf16(p, D, G, partial, grid, splits, st);
-        default: return pa::decode_f16(p, D, G, partial, grid, splits, st);
+        case PA_F32: return pa::decode_split_f32(p, D, G, grid, splits, st);
+        case PA_BF16: return pa::decode_split_bf16(p, D, G, grid, splits, st);
+        default: return pa::decode_split_f16(p, D, G, grid, splits, st);
     }
+}
+
+cudaError_t run_persistent(const pa::DecodeParams &p, int dtype, int D, int G, bool partial,
+                           long long unit_bound, cudaStream_t st) {
+    switch (dtype) {
+        case PA_F32: return pa::decode_persistent_f32(p, D, G, partial, unit_bound, st);
+        case PA_BF16: return pa::decode_persistent_bf16(p, D, G, partial, unit_bound, st);
+        default: return pa::decode_persistent_f16(p, D, G, partial, unit_bound, st);
+    }
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// A 16-bit cache [num_blocks][H_kv][16][D] as the 3-D tensor
+// (D, 16 rows, num_blocks*H_kv), read in boxes of 128 bytes x 16 rows with
+// the 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *m, const void *base, int64_t num_blocks, int32_t hkv,
+                      int32_t head_dim, int32_t dtype) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, 16, (cuuint64_t)(num_blocks * hkv)};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * 2 * 16};
+    const cuuint32_t box[3] = {64, 16, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Fill the tensor maps the persistent kernel needs for 16-bit caches.
+bool prepare_maps(pa::DecodeParams &p, int32_t dtype, int32_t head_dim) {
+    if (dtype == PA_F32) return true;
+    if (p.num_blocks <= 0) return true;            // nothing can be read
+    return encode_cache_map(&p.tmap_k, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                            dtype) &&
+           encode_cache_map(&p.tmap_v, p.v_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                            dtype);
+}
+
+// The persistent kernel reads each query row with 16-byte loads.
+bool q_rows_aligned(const void *q, int64_t q_seq_stride, int32_t dtype) {
+    return aligned16(q) && ((q_seq_stride * elem_size(dtype)) % 16) == 0;
 }
 
 cudaError_t run_merge(const pa::MergeParams &p, int dtype, int num_seqs, cudaStream_t st) {
@@ -110,7 +173,6 @@ int decode_common(void *out, const void *q, const void *k_cache, const void *v_c
                                max_blocks_per_seq, q_seq_stride, scale, dtype);
     if (rc != PA_OK || num_seqs == 0) return rc;
     if (splits < 0 || splits > 8 || (splits & (splits - 1))) return PA_ERR_INVALID_ARG;
-    if (splits == 0) splits = auto_splits(num_seqs, num_kv_heads, max_blocks_per_seq);
     pa::DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
@@ -121,9 +183,16 @@ int decode_common(void *out, const void *q, const void *k_cache, const void *v_c
     p.scale_log2 = scale * pa::LOG2E;
     if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
     const int G = num_heads / num_kv_heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorNotSupported;
+    if (splits == 0 && q_rows_aligned(q, q_seq_stride, dtype) && aligned16(out) &&
+        prepare_maps(p, dtype, head_dim)) {
+        e = run_persistent(p, dtype, head_dim, G, false, (long long)num_seqs * num_kv_heads, st);
+        if (e != cudaErrorNotSupported) return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+    if (splits == 0) splits = auto_splits(num_seqs, num_kv_heads, max_blocks_per_seq);
     dim3 grid((unsigned)splits, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    cudaError_t e = run_decode(p, dtype, head_dim, G, false, grid, splits,
-                               static_cast<cudaStream_t>(stream));
+    e = run_split(p, dtype, head_dim, G, grid, splits, st);
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -263,8 +332,10 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
     if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = num_heads / num_kv_heads;
-    dim3 grid((unsigned)P, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    cudaError_t e = run_decode(p, dtype, head_dim, G, true, grid, 1, st);
+    if (!q_rows_aligned(q, q_seq_stride, dtype)) return PA_ERR_UNSUPPORTED;
+    if (!prepare_maps(p, dtype, head_dim)) return PA_ERR_CUDA;
+    cudaError_t e = run_persistent(p, dtype, head_dim, G, true,
+                                   (long long)num_seqs * num_kv_heads * P, st);
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return PA_ERR_CUDA;
 

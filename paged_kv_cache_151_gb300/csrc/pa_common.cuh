@@ -164,6 +164,19 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Tensor-map bulk copy of one 3-D box (coordinates x, y, z in elements) to
+// this CTA's shared memory, completing on `bar`.  x * element size must be a
+// multiple of 16 bytes; dst must be 1024-byte aligned for the 128-byte swizzle.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        :: "r"(smem_u32(dst)), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+           "l"(policy)
+        : "memory");
+}
+
 // L2 policy for data read once per call (the streamed K/V tiles).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -34,13 +34,16 @@
 // At the end the warps' (m, l, acc) are merged in shared memory and, when the
 // (sequence, KV head) is split over a cluster, across the cluster through
 // distributed shared memory; out = acc / l, rounded to the storage type.
+// (The arithmetic is WarpAttn in pa_math.cuh; pa_persistent.cuh holds the
+// persistent kernel that pa_decode and pa_decode_partitioned use by default.)
 //
-// The partitioned variant (PARTIAL) gives each thread block one fixed token
-// partition and writes the partition's (m, l, acc/l) to a workspace instead;
-// a second kernel merges the partitions by log-sum-exp.
+// This file also holds the log-sum-exp merge of split-KV partitions.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (a plain 128-byte descriptor; no driver calls here)
+
 #include "pa_common.cuh"
+#include "pa_math.cuh"
 
 namespace pa {
 
@@ -65,21 +68,12 @@ struct DecodeParams {
     int max_seq_len;          // PARTIAL: bound on seq_len
     float scale_log2;         // scale * log2(e)
     unsigned int *err;        // device error word
+    // 16-bit caches, persistent kernel: the caches as 3-D tensors
+    // [num_blocks*num_kv_heads][16 rows][head_dim], read in swizzled boxes
+    // of 16 rows x 128 bytes
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
 };
-
-template <typename T, int D>
-struct Shape {
-    static constexpr int E = Elem<T>::E;            // elements per 16-byte chunk
-    static constexpr int NCH = D / E;               // chunks per row
-    static constexpr int RPW = 32 / NCH;            // rows per warp-wide chunk load
-    static constexpr int STEPS = 16 / RPW;          // chunk loads per 16-row tile
-    static constexpr int ROW_BYTES = D * (int)sizeof(T);
-    static constexpr int TILE_BYTES = 16 * ROW_BYTES;
-    static constexpr int LOG_NCH = NCH == 8 ? 3 : NCH == 16 ? 4 : 5;
-    static_assert(NCH == 8 || NCH == 16 || NCH == 32, "unsupported head_dim/type");
-};
-
-__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 // Stages per warp: about 24 KiB of K+V in flight per warp, at least 2.
 template <typename T, int D>
@@ -87,11 +81,6 @@ __host__ __device__ constexpr int stages_for() {
     constexpr int per = 2 * Shape<T, D>::TILE_BYTES;
     constexpr int s = 24576 / per;
     return s < 2 ? 2 : (s > 8 ? 8 : s);
-}
-
-template <int G>
-__host__ __device__ constexpr int warp_scratch_floats() {   // scores[16][G], probs[16][G], alpha[G]
-    return ((33 * G + 3) / 4) * 4;
 }
 
 // The stage buffers; after the block loop the same bytes hold the merge data.
@@ -110,50 +99,16 @@ __host__ __device__ constexpr size_t decode_smem_bytes() {
            (size_t)G * D * 4 + (size_t)NW * warp_scratch_floats<G>() * 4;
 }
 
-// Shuffle reduce-scatter of N partial sums across the lanes whose chunk
-// index c differs in the bits of MASK, MASK/2, ..., 1.  At each level a lane
-// keeps half of its values (the upper half when its bit of c is set), adds
-// the partner's copy of that half, and the count halves; once one value is
-// left the remaining levels are a plain butterfly sum.
-template <int N, int MASK>
-struct ReduceScatter {
-    static __device__ __forceinline__ void run(float *v, int c) {
-        if constexpr (MASK == 0) {
-            return;
-        } else if constexpr (N > 1) {
-            constexpr int H = N / 2;
-            const bool upper = (c & MASK) != 0;
-#pragma unroll
-            for (int i = 0; i < H; ++i) {
-                const float send = upper ? v[i] : v[i + H];
-                const float keep = upper ? v[i + H] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
-            }
-            ReduceScatter<H, MASK / 2>::run(v, c);
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
-            ReduceScatter<1, MASK / 2>::run(v, c);
-        }
-    }
-};
-
-template <typename T, int D, int G, int NW, int S, bool PARTIAL>
+// One thread block per (split, KV head, sequence); the splits of one
+// (sequence, KV head) form a thread-block cluster and merge through
+// distributed shared memory.
+template <typename T, int D, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32)
-decode_kernel(const DecodeParams p) {
+decode_split_kernel(const DecodeParams p) {
+    using W = WarpAttn<T, D, G>;
     using Sh = Shape<T, D>;
-    constexpr int E = Sh::E, NCH = Sh::NCH, RPW = Sh::RPW, STEPS = Sh::STEPS;
     constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
-    // score pass in sub-passes of SUB chunk loads: SUB*G partial sums a lane
-    constexpr int SUB = (STEPS * G <= 32) ? STEPS : (32 / G);
-    constexpr int NSUB = STEPS / SUB;
-    constexpr int NV = SUB * G;
-    constexpr int NVF = NV >= NCH ? NV / NCH : 1;           // scores a lane ends with
-    constexpr int NL = ilog2(NV / NVF);                      // scatter levels
-    // softmax layout: 16*G scores over 32 lanes, VPL rows of one head per lane
-    constexpr int VPL = (16 * G) / 32 >= 1 ? (16 * G) / 32 : 1;
-    constexpr int LPH = 16 / VPL;                            // lanes per head
     constexpr int WS = warp_scratch_floats<G>();
-    static_assert(STEPS % SUB == 0, "sub-pass split");
     static_assert(S <= 32, "stage count");
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -169,21 +124,14 @@ decode_kernel(const DecodeParams p) {
 
     // ---- which tokens this block handles ----------------------------------
     int L = p.seq_lens[s];
-    const int cap = PARTIAL ? min(p.max_seq_len, p.max_blocks * 16) : p.max_blocks * 16;
+    const int cap = p.max_blocks * 16;
     if (L < 0 || L > cap) {
         if (threadIdx.x == 0 && blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
         L = L < 0 ? 0 : cap;
     }
     const int nb = (L + 15) >> 4;
-    int lb_begin = 0, lb_end = nb, rank = 0, nrank = 1;
-    if constexpr (PARTIAL) {
-        lb_begin = blockIdx.x * p.partition_blocks;
-        if (lb_begin >= nb) return;                    // no such partition
-        lb_end = min(nb, lb_begin + p.partition_blocks);
-    } else {
-        rank = (int)cluster_ctarank();
-        nrank = (int)cluster_nctarank();
-    }
+    const int rank = (int)cluster_ctarank();
+    const int nrank = (int)cluster_nctarank();
 
     // ---- set-up: barriers and the G query vectors (pre-scaled) -------------
     if (threadIdx.x == 0) {
@@ -198,26 +146,21 @@ decode_kernel(const DecodeParams p) {
     }
     __syncthreads();
 
-    const int r = lane / NCH, c = lane % NCH;
-    float qreg[G][E];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < E; ++e) qreg[g][e] = qs[g * D + c * E + e];
+    W wa;
+    wa.init(lane);
+    wa.load_q_smem(qs);
+    float *Sc = wscr_all + warp * WS;
+    float *Pb = Sc + 16 * G;
+    float *Al = Pb + 16 * G;
 
-    float *Sc = wscr_all + warp * WS;         // [16][G] scores (log2 units)
-    float *Pb = Sc + 16 * G;                  // [16][G] probabilities
-    float *Al = Pb + 16 * G;                  // [G] rescale factors
-
-    // ---- this warp's share of the blocks ------------------------------------
+    // ---- this warp's share of the blocks: logical blocks worker, worker +
+    // nwk, ... (dealt round-robin over the warps of all CTAs of the cluster)
     const int worker = rank * NW + warp, nwk = nrank * NW;
-    const int span = lb_end - lb_begin;
-    const int n_mine = span > worker ? (span - worker + nwk - 1) / nwk : 0;
+    const int n_mine = nb > worker ? (nb - worker + nwk - 1) / nwk : 0;
     const int32_t *bt_row = p.block_tables + (long long)s * p.max_blocks;
     auto table_entry = [&](int k) -> int {
-        return k < n_mine ? bt_row[lb_begin + worker + k * nwk] : 0;
+        return k < n_mine ? bt_row[worker + k * nwk] : 0;
     };
-    // lane i holds the table entry of this warp's block c0 + i (and c0+32+i)
     int c0 = 0;
     int tab_cur = table_entry(lane), tab_nxt = table_entry(32 + lane);
     auto pb_of = [&](int k) -> int {                  // warp-uniform k
@@ -231,11 +174,7 @@ decode_kernel(const DecodeParams p) {
     const uint64_t pol = policy_evict_first();
     const unsigned char *kbase = reinterpret_cast<const unsigned char *>(p.k_cache);
     const unsigned char *vbase = reinterpret_cast<const unsigned char *>(p.v_cache);
-
-    auto rows_of = [&](int k) -> int {
-        const int lb = lb_begin + worker + k * nwk;
-        return min(16, L - lb * 16);
-    };
+    auto rows_of = [&](int k) -> int { return min(16, L - (worker + k * nwk) * 16); };
     auto issue = [&](int k, int pbk) {                // lane 0 only
         uint64_t *bar = &my_bars[k % S];
         if (pbk < 0 || (long long)pbk >= p.num_blocks) {
@@ -251,23 +190,11 @@ decode_kernel(const DecodeParams p) {
         bulk_g2s(dst + TILE, vbase + off, bytes, bar, pol);
     };
 
-    // prologue: fill the ring
     const int pre = n_mine < S ? n_mine : S;
     for (int k = 0; k < pre; ++k) {
         const int pbk = pb_of(k);
         if (lane == 0) issue(k, pbk);
     }
-
-    // softmax-layout identity of this lane
-    const int idx0 = (lane * VPL) % (16 * G);
-    const int g_sm = idx0 / 16, row0 = idx0 % 16;
-
-    float m_run = -INFINITY, l_run = 0.f;
-    float acc[G][E];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
 
     int k_done = 0;
     bool ok = true;
@@ -279,105 +206,14 @@ decode_kernel(const DecodeParams p) {
         }
         const int st = k % S;
         const int pbk = pb_of(k);
-        const int rows = rows_of(k);
         const bool waited = mbar_wait_bounded(&my_bars[st], (uint32_t)((k / S) & 1), p.err);
         if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
         k_done = k + 1;
         if (pbk >= 0 && (long long)pbk < p.num_blocks) {
             const unsigned char *Kt = my_stages + (size_t)st * 2 * TILE;
-            const unsigned char *Vt = Kt + TILE;
-
-            // -- scores: s[row][g] = sum_d qs[g][d] * K[row][d]
-#pragma unroll
-            for (int sp = 0; sp < NSUB; ++sp) {
-                float v[NV];
-#pragma unroll
-                for (int i = 0; i < SUB; ++i) {
-                    const int row = (sp * SUB + i) * RPW + r;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(Kt + row * ROWB + c * 16);
-                    float kf[E];
-                    Elem<T>::to_f32(raw, kf);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        float a = 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) a = fmaf(qreg[g][e], kf[e], a);
-                        v[i * G + g] = a;
-                    }
-                }
-                ReduceScatter<NV, NCH / 2>::run(v, c);
-                constexpr int LOWB = Sh::LOG_NCH - NL;   // c bits not used by the scatter
-                if ((c & ((1 << LOWB) - 1)) == 0) {
-                    const int cidx = c >> LOWB;
-#pragma unroll
-                    for (int f = 0; f < NVF; ++f) {
-                        const int vi = cidx * NVF + f;
-                        const int il = vi / G, g = vi % G;
-                        const int row = (sp * SUB + il) * RPW + r;
-                        Sc[row * G + g] = v[f];
-                    }
-                }
-            }
-            __syncwarp();
-
-            // -- online softmax
-            {
-                float sc[VPL];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u) {
-                    const int row = row0 + u;
-                    const float x = Sc[row * G + g_sm];
-                    sc[u] = row < rows ? x : -INFINITY;
-                    mx = fmaxf(mx, sc[u]);
-                }
-#pragma unroll
-                for (int m = 1; m < LPH; m <<= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-                const float m_new = fmaxf(m_run, mx);
-                const float alpha = ex2(m_run - m_new);
-                float psum = 0.f;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u) {
-                    const float pv = ex2(sc[u] - m_new);
-                    Pb[(row0 + u) * G + g_sm] = pv;
-                    psum += pv;
-                }
-                l_run = l_run * alpha + psum;
-                m_run = m_new;
-                if ((lane % LPH) == 0) Al[g_sm] = alpha;
-            }
-            __syncwarp();
-
-            // -- P.V
-            {
-                float al[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) al[g] = Al[g];
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) acc[g][e] *= al[g];
-#pragma unroll
-                for (int i = 0; i < STEPS; ++i) {
-                    const int row = i * RPW + r;
-                    if (row < rows) {
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(Vt + row * ROWB + c * 16);
-                        float vf[E];
-                        Elem<T>::to_f32(raw, vf);
-                        float pr[G];
-#pragma unroll
-                        for (int g = 0; g < G; ++g) pr[g] = Pb[row * G + g];
-#pragma unroll
-                        for (int g = 0; g < G; ++g)
-#pragma unroll
-                            for (int e = 0; e < E; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
-                    }
-                }
-            }
+            wa.block(Kt, Kt + TILE, rows_of(k), Sc, Pb, Al);
         }
         __syncwarp();
-        // -- refill the stage just consumed
         const int kn = k + S;
         if (kn < n_mine) {
             const int pbn = pb_of(kn);
@@ -397,16 +233,7 @@ decode_kernel(const DecodeParams p) {
         drained = __all_sync(0xffffffffu, drained);
     }
     const bool cta_ok = __syncthreads_and(drained ? 1 : 0) != 0;
-
-    // ---- warp totals ---------------------------------------------------------
-#pragma unroll
-    for (int m = NCH; m < 32; m <<= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], m);
-#pragma unroll
-    for (int m = 1; m < LPH; m <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, m);
+    wa.finish();
 
     // merge region (reuses the stage buffers: every copy has landed)
     float *Mw = reinterpret_cast<float *>(stages);      // [NW][G]
@@ -415,18 +242,7 @@ decode_kernel(const DecodeParams p) {
     float *Mc = Aw + NW * G * D;                        // [G]
     float *Lc = Mc + G;                                 // [G]
     float *Oc = Lc + G;                                 // [G][D]
-    if (cta_ok) {
-        if ((lane % LPH) == 0) {
-            Mw[warp * G + g_sm] = m_run;
-            Lw[warp * G + g_sm] = l_run;
-        }
-        if (r == 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int e = 0; e < E; ++e) Aw[(warp * G + g) * D + c * E + e] = acc[g][e];
-        }
-    }
+    if (cta_ok) wa.store_partial(Mw + warp * G, Lw + warp * G, Aw + warp * G * D);
     __syncthreads();
 
     const int h0 = j * G;
@@ -445,52 +261,39 @@ decode_kernel(const DecodeParams p) {
                 Ls = fmaf(f, Lw[w * G + g], Ls);
             }
         }
-        if constexpr (PARTIAL) {
-            const long long row = ((long long)s * H + h0 + g) * p.max_parts + blockIdx.x;
-            p.part_o[row * D + d] = O / Ls;
-            if (d == 0) {
-                p.part_m[row] = M * LN2;               // natural units
-                p.part_l[row] = Ls;
-            }
+        if (nrank == 1) {
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
+            Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
         } else {
-            if (nrank == 1) {
-                T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
-                Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
-            } else {
-                Oc[idx] = O;
-                if (d == 0) { Mc[g] = M; Lc[g] = Ls; }
-            }
+            Oc[idx] = O;
+            if (d == 0) { Mc[g] = M; Lc[g] = Ls; }
         }
     }
 
-    if constexpr (!PARTIAL) {
-        if (nrank > 1) {
-            // cross-CTA merge through distributed shared memory: rank r
-            // finalises outputs [r*G*D/n, (r+1)*G*D/n) from every rank's (M, L, O)
-            cluster_sync();
-            const int per = (G * D + nrank - 1) / nrank;
-            const int beg = rank * per, end = min(G * D, beg + per);
-            for (int idx = beg + threadIdx.x; idx < end; idx += NW * 32) {
-                const int g = idx / D, d = idx % D;
-                float M = -INFINITY;
-                for (int q = 0; q < nrank; ++q)
-                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(&Mc[g], q)));
-                float O = 0.f, Ls = 0.f;
-                if (M != -INFINITY) {
-                    for (int q = 0; q < nrank; ++q) {
-                        const float mq = ld_dsmem_f32(map_to_rank(&Mc[g], q));
-                        const float f = mq == -INFINITY ? 0.f : ex2(mq - M);
-                        O = fmaf(f, ld_dsmem_f32(map_to_rank(&Oc[idx], q)), O);
-                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(&Lc[g], q)), Ls);
-                    }
-                }
-                if (cta_ok) {
-                    T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
-                    Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
+    if (nrank > 1) {
+        // rank q finalises outputs [q*G*D/n, (q+1)*G*D/n) from every rank's (M, L, O)
+        cluster_sync();
+        const int per = (G * D + nrank - 1) / nrank;
+        const int beg = rank * per, end = min(G * D, beg + per);
+        for (int idx = beg + threadIdx.x; idx < end; idx += NW * 32) {
+            const int g = idx / D, d = idx % D;
+            float M = -INFINITY;
+            for (int q = 0; q < nrank; ++q) M = fmaxf(M, ld_dsmem_f32(map_to_rank(&Mc[g], q)));
+            float O = 0.f, Ls = 0.f;
+            if (M != -INFINITY) {
+                for (int q = 0; q < nrank; ++q) {
+                    const float mq = ld_dsmem_f32(map_to_rank(&Mc[g], q));
+                    const float f = mq == -INFINITY ? 0.f : ex2(mq - M);
+                    O = fmaf(f, ld_dsmem_f32(map_to_rank(&Oc[idx], q)), O);
+                    Ls = fmaf(f, ld_dsmem_f32(map_to_rank(&Lc[g], q)), Ls);
                 }
             }
-            cluster_sync();     // keep this CTA's shared memory alive for the peers
+            if (cta_ok) {
+                T *o = reinterpret_cast<T *>(p.out) + ((long long)s * H + h0 + g) * D + d;
+                Elem<T>::store1(o, Ls > 0.f ? O / Ls : 0.f);
+            }
         }
+        cluster_sync();     // keep this CTA's shared memory alive for the peers
     }
 }
 
@@ -535,17 +338,17 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
 // ---- host-side launch helpers ------------------------------------------------
 int sm_count_of_current_device();
 
-template <typename T, int D, int G, bool PARTIAL>
-cudaError_t launch_decode(const DecodeParams &p, dim3 grid, int splits, cudaStream_t st) {
+template <typename T, int D, int G>
+cudaError_t launch_split(const DecodeParams &p, dim3 grid, int splits, cudaStream_t st) {
     constexpr int NW = 4;
     constexpr int S = stages_for<T, D>();
     constexpr size_t smem = decode_smem_bytes<T, D, G, NW, S>();
-    auto kern = decode_kernel<T, D, G, NW, S, PARTIAL>;
+    auto kern = decode_split_kernel<T, D, G, NW, S>;
     static_assert(smem <= 227 * 1024, "shared memory");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    if (PARTIAL || splits <= 1) {
+    if (splits <= 1) {
         kern<<<grid, NW * 32, smem, st>>>(p);
         return cudaGetLastError();
     }
@@ -572,15 +375,13 @@ cudaError_t launch_merge(const MergeParams &p, int num_seqs, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// Dispatch over (head_dim, group size) for one storage type.  Returns
-// cudaErrorNotSupported for shapes that are not built.
+// Dispatch of the cluster-split kernel over (head_dim, group size) for one
+// storage type.  Returns cudaErrorNotSupported for shapes that are not built.
 template <typename T>
-cudaError_t dispatch_decode(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
-                            int splits, cudaStream_t st) {
-#define PA_CASE(DD, GG)                                                         \
-    if (D == DD && G == GG)                                                     \
-        return partial ? launch_decode<T, DD, GG, true>(p, grid, splits, st)    \
-                       : launch_decode<T, DD, GG, false>(p, grid, splits, st);
+cudaError_t dispatch_split(const DecodeParams &p, int D, int G, dim3 grid, int splits,
+                           cudaStream_t st) {
+#define PA_CASE(DD, GG) \
+    if (D == DD && G == GG) return launch_split<T, DD, GG>(p, grid, splits, st);
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
 #undef PA_CASE

@@ -10,13 +10,22 @@ namespace pa {
 struct DecodeParams;
 struct MergeParams;
 
-// per storage type: decode kernels (D in {64,128}, G in {1,2,4,8}) and merge
-cudaError_t decode_f32(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
-                       int splits, cudaStream_t st);
-cudaError_t decode_bf16(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
-                        int splits, cudaStream_t st);
-cudaError_t decode_f16(const DecodeParams &p, int D, int G, bool partial, dim3 grid,
-                       int splits, cudaStream_t st);
+// per storage type: cluster-split decode, persistent decode (whole sequences
+// or partitions) and the partition merge; D in {64,128}, G in {1,2,4,8}.
+// cudaErrorNotSupported: shape not built (or too many sequences for the
+// persistent kernel's in-block sort).
+cudaError_t decode_split_f32(const DecodeParams &p, int D, int G, dim3 grid, int splits,
+                             cudaStream_t st);
+cudaError_t decode_split_bf16(const DecodeParams &p, int D, int G, dim3 grid, int splits,
+                              cudaStream_t st);
+cudaError_t decode_split_f16(const DecodeParams &p, int D, int G, dim3 grid, int splits,
+                             cudaStream_t st);
+cudaError_t decode_persistent_f32(const DecodeParams &p, int D, int G, bool partial,
+                                  long long unit_bound, cudaStream_t st);
+cudaError_t decode_persistent_bf16(const DecodeParams &p, int D, int G, bool partial,
+                                   long long unit_bound, cudaStream_t st);
+cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
+                                  long long unit_bound, cudaStream_t st);
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

@@ -1,0 +1,218 @@
+// pa_mma.cuh -- per-warp decode arithmetic on the tensor cores for 16-bit
+// caches (bf16, f16), over one 16-token block whose K and V tiles were
+// placed in shared memory by tensor-map bulk copies with the 128-byte
+// swizzle.
+//
+// With G query heads sharing a KV head, one block's scores are the product
+// S^T[heads x 16 tokens] = Q[heads x d] . K^T[d x 16 tokens] and its value
+// update is O[heads x d] += P[heads x 16 tokens] . V[16 tokens x d]: the
+// grouped heads turn the step into two small dense contractions.  Each is a
+// run of mma.sync.m16n8k16 (16-bit inputs, fp32 accumulation) with the heads
+// on the M side (rows G..15 are zero), so:
+//   - Q stays in registers as A fragments for the whole unit;
+//   - K^T and V arrive as B fragments through ldmatrix (V transposed), which
+//     reads the swizzled tiles without bank conflicts;
+//   - the fp32 score fragment of the first product has exactly the layout of
+//     the A fragment of the second, so P never leaves registers (it is
+//     rounded to the input type, as the tensor cores require);
+//   - the online-softmax statistics of head g live in the four lanes that
+//     hold row g, so a block needs two shuffles for its maximum.
+// Everything else follows WarpAttn in pa_math.cuh: scores carry
+// scale*log2(e), the softmax uses exp2, and the running sum is accumulated
+// from the same rounded P that multiplies V, so the weights applied to V are
+// exactly normalised.
+#pragma once
+
+#include "pa_common.cuh"
+#include "pa_math.cuh"
+
+namespace pa {
+
+// smem byte offset of 16-byte chunk `chunk` (0..D/8-1) of row `row` (0..15)
+// in a tile stored as D/64 boxes of [16 rows][128 bytes], each box swizzled
+// with the 128-byte pattern (chunk position XOR row mod 8).
+__device__ __forceinline__ uint32_t swz_offset(int row, int chunk) {
+    const int h = chunk >> 3, cc = chunk & 7;
+    return (uint32_t)(h * 2048 + row * 128 + ((cc ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+template <typename T> struct Mma;
+
+template <> struct Mma<__nv_bfloat16> {
+    // d = a . b + d, a: rows 0-7 only (a1 = a3 = 0)
+    __device__ __forceinline__ static void run(float *d, uint32_t a0, uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(uint32_t w, float &lo, float &hi) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    }
+};
+
+template <> struct Mma<__half> {
+    __device__ __forceinline__ static void run(float *d, uint32_t a0, uint32_t a2, uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(uint32_t w, float &lo, float &hi) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        const float2 f = __half22float2(h);
+        lo = f.x;
+        hi = f.y;
+    }
+};
+
+template <typename T, int D, int G>
+struct WarpAttnTC {
+    static_assert(sizeof(T) == 2, "tensor-core path is for 16-bit caches");
+    static_assert(G >= 1 && G <= 8, "group size");
+    static constexpr int KS = D / 16;     // k-steps of the score product
+    static constexpr int NT = D / 8;      // n-tiles of the value product
+    static constexpr int TILE_BYTES = 16 * D * 2;
+
+    int lane, g, t;
+    bool head_ok;                          // this lane's row g is a real head
+    uint32_t qa0[KS], qa2[KS];             // A fragments of Q (rows 0..7)
+    float acc[NT][4];                      // O fragments ([2],[3]: rows 8..15, unused)
+    float m_run, l_run;
+
+    __device__ __forceinline__ void init(int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        head_ok = g < G;
+        reset();
+    }
+
+    __device__ __forceinline__ void reset() {
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    }
+
+    // q points at the first of the G heads ([G][D] of T); rows >= G are zero
+    __device__ __forceinline__ void load_q_global(const T *q) {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(q + (head_ok ? g : 0) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qa0[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t) / 2) : 0u;
+            qa2[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t + 8) / 2) : 0u;
+        }
+    }
+
+    // One block: kt, vt are shared-memory addresses of the swizzled tiles.
+    // rows in 1..16; rows past `rows` may hold anything and are ignored.
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int rows, float scale_log2) {
+        // -- scores S^T[g][tok] for tok in {2t, 2t+1} (s0) and {8+2t, 9+2t} (s1)
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int rr = lane & 7, mi = lane >> 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            // matrices: (tok 0-7, chunk 2ks), (tok 0-7, 2ks+1), (tok 8-15, 2ks), (tok 8-15, 2ks+1)
+            const int tok = (mi >> 1) * 8 + rr, chunk = 2 * ks + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            Mma<T>::run(s0, qa0[ks], qa2[ks], b0, b1);
+            Mma<T>::run(s1, qa0[ks], qa2[ks], b2, b3);
+        }
+        float sc[4] = {s0[0] * scale_log2, s0[1] * scale_log2, s1[0] * scale_log2,
+                       s1[1] * scale_log2};
+        const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = tk[e] < rows ? sc[e] : -INFINITY;
+
+        // -- online softmax for head g (the four lanes g*4 .. g*4+3)
+        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = ex2(m_run - m_new);
+        const uint32_t pa0 = Mma<T>::pack(ex2(sc[0] - m_new), ex2(sc[1] - m_new));
+        const uint32_t pa2 = Mma<T>::pack(ex2(sc[2] - m_new), ex2(sc[3] - m_new));
+        float p0, p1, p2, p3;
+        Mma<T>::unpack(pa0, p0, p1);
+        Mma<T>::unpack(pa2, p2, p3);
+        l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
+        m_run = m_new;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                acc[j][0] *= alpha;
+                acc[j][1] *= alpha;
+            }
+        }
+
+        // -- P.V: for each pair of 8-wide d tiles, V^T fragments via ldmatrix.trans
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+            // matrices: (tok 0-7, chunk j), (tok 8-15, j), (tok 0-7, j+1), (tok 8-15, j+1)
+            const int tok = (mi & 1) * 8 + rr, chunk = j + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            Mma<T>::run(acc[j], pa0, pa2, b0, b1);
+            Mma<T>::run(acc[j + 1], pa0, pa2, b2, b3);
+        }
+    }
+
+    // Zero V rows [rows, 16) of a tile (all chunks); call before block() on a
+    // partial block whose tail rows hold data of other tokens.
+    __device__ __forceinline__ static void zero_rows(unsigned char *vt, int rows, int lane) {
+        const int n = (16 - rows) * (D / 8);
+        for (int i = lane; i < n; i += 32) {
+            const int row = rows + i / (D / 8), chunk = i % (D / 8);
+            *reinterpret_cast<uint4 *>(vt + swz_offset(row, chunk)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // Sum the per-lane partial sums of each head (the four lanes of row g).
+    __device__ __forceinline__ void finish() {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    }
+
+    // Write this warp's (m, l, acc) into a merge slot: Mw[G], Lw[G], Aw[G][D].
+    __device__ __forceinline__ void store_partial(float *Mw, float *Lw, float *Aw) const {
+        if (!head_ok) return;
+        if (t == 0) {
+            Mw[g] = m_run;
+            Lw[g] = l_run;
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+            *reinterpret_cast<float2 *>(Aw + g * D + 8 * j + 2 * t) = make_float2(acc[j][0], acc[j][1]);
+    }
+};
+
+}  // namespace pa

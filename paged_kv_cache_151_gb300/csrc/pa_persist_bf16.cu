@@ -1,0 +1,13 @@
+// pa_persist_bf16.cu -- persistent decode kernels (whole sequences and split-KV
+// partitions), bf16 storage.
+#include "pa_internal.h"
+#include "pa_persistent.cuh"
+
+namespace pa {
+
+cudaError_t decode_persistent_bf16(const DecodeParams &p, int D, int G, bool partial,
+                                long long unit_bound, cudaStream_t st) {
+    return dispatch_persistent<__nv_bfloat16>(p, D, G, partial, unit_bound, st);
+}
+
+}  // namespace pa

@@ -1,0 +1,13 @@
+// pa_persist_f16.cu -- persistent decode kernels (whole sequences and split-KV
+// partitions), f16 storage.
+#include "pa_internal.h"
+#include "pa_persistent.cuh"
+
+namespace pa {
+
+cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
+                                long long unit_bound, cudaStream_t st) {
+    return dispatch_persistent<__half>(p, D, G, partial, unit_bound, st);
+}
+
+}  // namespace pa

@@ -1,0 +1,550 @@
+// pa_persistent.cuh -- persistent decode kernel: one resident thread block
+// per SM slot streams a balanced list of work units end to end.
+//
+// A work unit is (sequence, KV head) for pa_decode, or (sequence, KV head,
+// token partition) for pa_decode_partitioned.  Every block:
+//
+//  1. reads all seq_lens and sorts the sequences by block count, longest
+//     first (bitonic sort in shared memory; ties by index, so the order is
+//     deterministic);
+//  2. numbers the units in that order and takes ranks p, 2P-1-p, 2P+p, ...
+//     (P blocks in the grid, "snake" order), which deals the longest units
+//     out first and evens the per-block totals (longest-processing-time
+//     first);
+//  3. concatenates the 16-token blocks of its units into one stream and
+//     deals the stream round-robin to its warps: stream position f goes to
+//     warp f mod NW.  Each warp keeps a ring of S stages filled with 1-D bulk
+//     copies (cp.async.bulk on an mbarrier) of its next blocks' K and V
+//     tiles, running ahead across unit boundaries, so the copy engine never
+//     waits for a unit to be merged;
+//  4. when a warp leaves a unit it parks its (m, l, acc) in one of R merge
+//     slots; the last of the unit's warps to arrive merges them and writes
+//     the unit's output (pa_decode) or its partition statistics
+//     (pa_decode_partitioned), while the other warps stream on.
+//
+// Everything a unit's result depends on -- the unit order, the warp that
+// handles each block, the merge order -- is a function of seq_lens and the
+// logical block index only, never of where the blocks sit in the pool, so
+// outputs are bit-identical under any permutation of physical blocks and
+// under prefix aliasing.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_decode.cuh"
+#include "pa_math.cuh"
+#include "pa_mma.cuh"
+
+namespace pa {
+
+struct UnitRec {
+    int s, j, lb0, nb, L, part;
+};
+
+template <typename T, int D, int G, int NW, int S>
+struct PersistentLayout {
+    using Sh = Shape<T, D>;
+    static constexpr int R = 2;                           // merge slots in flight
+    static constexpr int NU_MAX = 160;                    // units per block
+    static constexpr size_t STAGES = (size_t)NW * S * 2 * Sh::TILE_BYTES;
+    static constexpr size_t SLOT_FLOATS = (size_t)NW * (G * D + 2 * G);
+    static constexpr size_t OFF_BARS = STAGES;
+    static constexpr size_t OFF_SCR = OFF_BARS + (size_t)NW * S * 8;
+    static constexpr size_t OFF_SLOTS = OFF_SCR + (size_t)NW * warp_scratch_floats<G>() * 4;
+    static constexpr size_t OFF_UNITS = OFF_SLOTS + (size_t)R * SLOT_FLOATS * 4;
+    static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
+    static constexpr size_t OFF_CTL = OFF_CUM + (size_t)(NU_MAX + 1) * 4;
+    static constexpr size_t BYTES = OFF_CTL + 64 + 1024;   // + alignment of the base
+    // the sort scratch (keys, padded to a power of two, + scan) lives in the
+    // stage region before streaming: at most 12 bytes per sequence
+    static constexpr int MAX_SEQS = (int)(STAGES / 12) > 65535 ? 65535 : (int)(STAGES / 12);
+};
+
+// Exclusive scan of one int per thread across the block; returns this
+// thread's exclusive prefix and writes the total to *total.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const int t = wtot[w];
+        if (w < warp) before += t;
+        all += t;
+    }
+    __syncthreads();
+    *total = all;
+    return before + x - v;
+}
+
+// 16-bit caches use the tensor cores (pa_mma.cuh) on swizzled tiles placed
+// by tensor-map copies of whole 16-row blocks; fp32 caches use the CUDA-core
+// path (pa_math.cuh) on tiles placed by 1-D copies of the valid rows.
+template <typename T>
+__host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
+
+template <typename T, int D, int G, int NW, int S, bool PARTIAL>
+__global__ void __launch_bounds__(NW * 32)
+decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr bool TC = use_tc<T>();
+    using W = std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>;
+    using Lay = PersistentLayout<T, D, G, NW, S>;
+    using Sh = Shape<T, D>;
+    constexpr int E = Sh::E, NCH = Sh::NCH;
+    constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
+    constexpr int NT = NW * 32;
+    constexpr int R = Lay::R, NU_MAX = Lay::NU_MAX;
+    constexpr int WS = warp_scratch_floats<G>();
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the 128-byte swizzle pattern is tied to 1024-byte aligned addresses
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);
+    float *scr = reinterpret_cast<float *>(smem + Lay::OFF_SCR);
+    float *slots = reinterpret_cast<float *>(smem + Lay::OFF_SLOTS);
+    UnitRec *units = reinterpret_cast<UnitRec *>(smem + Lay::OFF_UNITS);
+    int *cum = reinterpret_cast<int *>(smem + Lay::OFF_CUM);
+    int *ctl = reinterpret_cast<int *>(smem + Lay::OFF_CTL);
+    volatile int *slot_cnt = ctl;          // [R] warps that parked in the slot
+    volatile int *slot_done = ctl + R;     // [R] last unit merged from the slot
+    int *nu_sh = ctl + 2 * R;              // units of this block
+    int *wtot = ctl + 2 * R + 1;           // [NW] scan scratch
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
+    const int cap = PARTIAL ? min(p.max_seq_len, p.max_blocks * 16) : p.max_blocks * 16;
+    const int PB = PARTIAL ? p.partition_blocks : 1;
+
+    auto seq_len = [&](int s) -> int {
+        int L = p.seq_lens[s];
+        return L < 0 ? 0 : (L > cap ? cap : L);
+    };
+
+    // ---- 1. sort the sequences by block count (longest first) ----------------
+    int Bp = 1;
+    while (Bp < B) Bp <<= 1;
+    uint32_t *keys = reinterpret_cast<uint32_t *>(stages);
+    int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);
+    for (int i = tid; i < Bp; i += NT) {
+        uint32_t key = 0xffffffffu;
+        if (i < B) {
+            const int L0 = p.seq_lens[i];
+            if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
+            const int nb = (seq_len(i) + 15) >> 4;
+            key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
+        }
+        keys[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= Bp; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int i = tid; i < Bp; i += NT) {
+                const int ixj = i ^ jj;
+                if (ixj > i) {
+                    const uint32_t a = keys[i], b = keys[ixj];
+                    const bool up = (i & k) == 0;
+                    if ((a > b) == up) { keys[i] = b; keys[ixj] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // ---- 2. number the units: exclusive scan of units per sorted sequence -----
+    auto units_of = [&](int pos) -> int {          // pos < B
+        const int nb = 0xffff - (int)(keys[pos] >> 16);
+        return PARTIAL ? Hkv * ((nb + PB - 1) / PB) : Hkv;
+    };
+    int U = 0;
+    {
+        const int per = (B + NT - 1) / NT;
+        const int lo = min(B, tid * per), hi = min(B, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += units_of(i);
+        int run = block_exclusive_scan<NT>(sum, wtot, &U);
+        for (int i = lo; i < hi; ++i) {
+            start[i] = run;
+            run += units_of(i);
+        }
+    }
+    __syncthreads();
+
+    // ---- 3. this block's units (snake over the ranks) -------------------------
+    const int P = gridDim.x, me = blockIdx.x;
+    auto rank_of = [&](int q) -> long long {
+        return (long long)q * P + ((q & 1) ? (P - 1 - me) : me);
+    };
+    int nu = 0;
+    while (rank_of(nu) < U) ++nu;
+    if (nu > NU_MAX) {
+        if (tid == 0) set_error(p.err, ERR_SEQ_LEN);
+        nu = NU_MAX;
+    }
+    for (int q = tid; q < nu; q += NT) {
+        const int r = (int)rank_of(q);
+        int lo = 0, hi = B - 1;                    // last pos with start[pos] <= r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        const int s = (int)(keys[lo] & 0xffffu);
+        const int nb = 0xffff - (int)(keys[lo] >> 16);
+        const int local = r - start[lo];
+        UnitRec u;
+        u.s = s;
+        u.L = seq_len(s);
+        if (PARTIAL) {
+            const int ps = (nb + PB - 1) / PB;
+            u.j = local / ps;
+            u.part = local % ps;
+            u.lb0 = u.part * PB;
+            u.nb = min(PB, nb - u.lb0);
+        } else {
+            u.j = local;
+            u.part = 0;
+            u.lb0 = 0;
+            u.nb = nb;
+        }
+        units[q] = u;
+    }
+    __syncthreads();
+    if (warp == 0) {                               // cum[q] = blocks before unit q
+        int run = 0;
+        for (int base = 0; base < nu; base += 32) {
+            const int q = base + lane;
+            const int v = q < nu ? units[q].nb : 0;
+            int x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (q < nu) cum[q] = run + x - v;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) {
+            cum[nu] = run;
+            *nu_sh = nu;
+        }
+    }
+    if (tid == 0) {
+        for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        for (int i = 0; i < R; ++i) {
+            slot_cnt[i] = 0;
+            slot_done[i] = i - R;
+        }
+    }
+    // the sort scratch in the stage region is overwritten by bulk copies next
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // units with no tokens (pa_decode only): their output is zero
+    if (!PARTIAL && warp == NW - 1) {
+        for (int q = 0; q < nu; ++q) {
+            const UnitRec u = units[q];
+            if (u.nb != 0) continue;
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G) * D;
+            for (int i = lane; i < G * D / E; i += 32) {
+                float z[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) z[e] = 0.f;
+                store_chunk<T>(o + i * E, z);
+            }
+        }
+    }
+
+    // ---- 4. stream this warp's blocks: positions warp, warp+NW, ... ---------
+    const int F = cum[nu];
+    const int n_mine = F > warp ? (F - warp + NW - 1) / NW : 0;
+    auto locate = [&](int f) -> int {              // unit holding stream position f
+        int lo = 0, hi = nu - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] <= f) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+    // lane i holds (unit, physical block) of this warp's block c0 + i and c0 + 32 + i
+    auto fetch = [&](int k, int &ui, int &pb) {
+        ui = -1;
+        pb = 0;
+        if (k < n_mine) {
+            const int f = warp + k * NW;
+            ui = locate(f);
+            const UnitRec &u = units[ui];
+            const int lb = u.lb0 + (f - cum[ui]);
+            pb = p.block_tables[(long long)u.s * p.max_blocks + lb];
+        }
+    };
+    int c0 = 0, ui_cur, pb_cur, ui_nxt, pb_nxt;
+    fetch(lane, ui_cur, pb_cur);
+    fetch(32 + lane, ui_nxt, pb_nxt);
+    auto of = [&](int k, int &ui, int &pb) {      // warp-uniform k
+        const int kk = k - c0;
+        const int a = __shfl_sync(0xffffffffu, ui_cur, kk & 31);
+        const int b = __shfl_sync(0xffffffffu, ui_nxt, kk & 31);
+        const int x = __shfl_sync(0xffffffffu, pb_cur, kk & 31);
+        const int y = __shfl_sync(0xffffffffu, pb_nxt, kk & 31);
+        ui = kk < 32 ? a : b;
+        pb = kk < 32 ? x : y;
+    };
+    auto rows_of = [&](int k, int ui) -> int {
+        const UnitRec &u = units[ui];
+        const int lb = u.lb0 + (warp + k * NW - cum[ui]);
+        return min(16, u.L - lb * 16);
+    };
+
+    unsigned char *my_stages = stages + (size_t)warp * S * 2 * TILE;
+    uint64_t *my_bars = bars + warp * S;
+    const uint64_t pol = policy_evict_first();
+    const unsigned char *kbase = reinterpret_cast<const unsigned char *>(p.k_cache);
+    const unsigned char *vbase = reinterpret_cast<const unsigned char *>(p.v_cache);
+    auto issue = [&](int k, int ui, int pbk) {     // lane 0 only
+        uint64_t *bar = &my_bars[k % S];
+        if (pbk < 0 || (long long)pbk >= p.num_blocks) {
+            set_error(p.err, ERR_BLOCK_ID);
+            mbar_arrive(bar);
+            return;
+        }
+        unsigned char *dst = my_stages + (size_t)(k % S) * 2 * TILE;
+        if constexpr (TC) {
+            // whole 16-row tiles, D/64 boxes each for K and V
+            const int z = pbk * Hkv + units[ui].j;
+            mbar_arrive_expect_tx(bar, 2 * TILE);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                tma_load_3d(dst + h * 2048, &p.tmap_k, h * 64, 0, z, bar, pol);
+                tma_load_3d(dst + TILE + h * 2048, &p.tmap_v, h * 64, 0, z, bar, pol);
+            }
+        } else {
+            const uint32_t bytes = (uint32_t)(rows_of(k, ui) * ROWB);
+            const size_t off = ((size_t)pbk * Hkv + units[ui].j) * TILE;
+            mbar_arrive_expect_tx(bar, 2 * bytes);
+            bulk_g2s(dst, kbase + off, bytes, bar, pol);
+            bulk_g2s(dst + TILE, vbase + off, bytes, bar, pol);
+        }
+    };
+
+    const int pre = n_mine < S ? n_mine : S;
+    for (int k = 0; k < pre; ++k) {
+        int ui, pbk;
+        of(k, ui, pbk);
+        if (lane == 0) issue(k, ui, pbk);
+    }
+
+    W wa;
+    wa.init(lane);
+    float *Sc = scr + warp * WS;
+    float *Pb = Sc + 16 * G;
+    float *Al = Pb + 16 * G;
+
+    // Leave unit `ui`: park this warp's partial in the unit's slot; the last
+    // of the unit's warps merges the slot and writes the result.
+    auto leave_unit = [&](int ui) -> bool {
+        wa.finish();
+        const int slot = ui % R;
+        float *base = slots + (size_t)slot * Lay::SLOT_FLOATS;
+        float *Mw = base, *Lw = base + NW * G, *Aw = base + 2 * NW * G;
+        // wait (bounded) until the slot's previous unit has been merged
+        bool ok = true;
+        if (slot_done[slot] != ui - R) {
+            const unsigned long long t0 = globaltimer();
+            while (slot_done[slot] != ui - R) {
+                if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+                    if (lane == 0) set_error(p.err, ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return false;
+        wa.store_partial(Mw + warp * G, Lw + warp * G, Aw + warp * G * D);
+        __threadfence_block();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd((int *)&slot_cnt[slot], 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        const UnitRec u = units[ui];
+        const int contributors = min(u.nb, NW);
+        if (old == contributors - 1) {
+            __threadfence_block();
+            const int first = cum[ui] % NW;        // warp of the unit's first block
+            for (int ch = lane; ch < G * (D / E); ch += 32) {
+                const int g = ch / (D / E), d0 = (ch % (D / E)) * E;
+                float M = -INFINITY;
+                for (int i = 0; i < contributors; ++i) {
+                    const int w = (first + i) % NW;
+                    M = fmaxf(M, Mw[w * G + g]);
+                }
+                float O[E], Ls = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) O[e] = 0.f;
+                if (M != -INFINITY) {
+                    for (int i = 0; i < contributors; ++i) {
+                        const int w = (first + i) % NW;
+                        const float mw = Mw[w * G + g];
+                        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+                        Ls = fmaf(f, Lw[w * G + g], Ls);
+                        const float *a = Aw + (w * G + g) * D + d0;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) O[e] = fmaf(f, a[e], O[e]);
+                    }
+                }
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                if constexpr (PARTIAL) {
+                    const long long row = ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
+                    float *po = p.part_o + row * D + d0;
+#pragma unroll
+                    for (int e = 0; e < E; e += 4)
+                        *reinterpret_cast<float4 *>(po + e) =
+                            make_float4(O[e] * inv, O[e + 1] * inv, O[e + 2] * inv, O[e + 3] * inv);
+                    if (d0 == 0) {
+                        p.part_m[row] = M * LN2;      // natural units
+                        p.part_l[row] = Ls;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) O[e] *= inv;
+                    T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d0;
+                    store_chunk<T>(o, O);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                slot_cnt[slot] = 0;
+                __threadfence_block();
+                slot_done[slot] = ui;
+            }
+        }
+        wa.reset();
+        return true;
+    };
+
+    int cur = -1;
+    int k_done = 0;
+    bool ok = true;
+    for (int k = 0; k < n_mine; ++k) {
+        if (k - c0 == 32) {
+            c0 += 32;
+            ui_cur = ui_nxt;
+            pb_cur = pb_nxt;
+            fetch(c0 + 32 + lane, ui_nxt, pb_nxt);
+        }
+        int ui, pbk;
+        of(k, ui, pbk);
+        if (ui != cur) {
+            if (cur >= 0 && !leave_unit(cur)) { ok = false; break; }
+            cur = ui;
+            const UnitRec &u = units[ui];
+            const T *qp = reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
+                          (long long)u.j * G * D;
+            if constexpr (TC) wa.load_q_global(qp);
+            else wa.load_q_global(qp, p.scale_log2);
+        }
+        const int st = k % S;
+        const bool waited = mbar_wait_bounded(&my_bars[st], (uint32_t)((k / S) & 1), p.err);
+        if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
+        k_done = k + 1;
+        if (pbk >= 0 && (long long)pbk < p.num_blocks) {
+            unsigned char *Kt = my_stages + (size_t)st * 2 * TILE;
+            const int rows = rows_of(k, ui);
+            if constexpr (TC) {
+                if (rows < 16) {                   // tail rows hold other tokens' data
+                    W::zero_rows(Kt + TILE, rows, lane);
+                    __syncwarp();
+                }
+                wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, p.scale_log2);
+            } else {
+                wa.block(Kt, Kt + TILE, rows, Sc, Pb, Al);
+            }
+        }
+        fence_proxy_async_smem();                  // generic accesses before the next copy
+        __syncwarp();
+        const int kn = k + S;
+        if (kn < n_mine) {
+            int uin, pbn;
+            of(kn, uin, pbn);
+            if (lane == 0) issue(kn, uin, pbn);
+        }
+    }
+    if (ok && cur >= 0) ok = leave_unit(cur);
+
+    // after a timeout: wait (bounded) for this warp's copies still in flight
+    if (!ok) {
+        const int issued = min(n_mine, k_done + S);
+        for (int k = k_done; k < issued; ++k)
+            mbar_wait_bounded(&my_bars[k % S], (uint32_t)((k / S) & 1), p.err);
+    }
+}
+
+// Stages per warp: about 16 KiB of K+V in flight per warp, at least 2.
+template <typename T, int D>
+__host__ __device__ constexpr int persistent_stages() {
+    constexpr int s = 16384 / (2 * Shape<T, D>::TILE_BYTES);
+    return s < 2 ? 2 : (s > 6 ? 6 : s);
+}
+
+template <typename T, int D, int G, bool PARTIAL>
+struct PersistentConfig {
+    static constexpr int NW = 4;
+    static constexpr int S = persistent_stages<T, D>();
+    using Lay = PersistentLayout<T, D, G, NW, S>;
+};
+
+// Largest num_seqs the persistent kernel sorts in shared memory.
+template <typename T, int D, int G, bool PARTIAL>
+constexpr int persistent_max_seqs() {
+    return PersistentConfig<T, D, G, PARTIAL>::Lay::MAX_SEQS;
+}
+
+template <typename T, int D, int G, bool PARTIAL>
+cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, cudaStream_t st) {
+    using C = PersistentConfig<T, D, G, PARTIAL>;
+    constexpr size_t smem = C::Lay::BYTES;
+    static_assert(smem <= 227 * 1024, "shared memory");
+    auto kern = decode_persistent_kernel<T, D, G, C::NW, C::S, PARTIAL>;
+    if (p.num_seqs > C::Lay::MAX_SEQS) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NW * 32, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int sms = sm_count_of_current_device();
+    if (sms <= 0) sms = 152;
+    long long P = (long long)sms * per_sm;
+    const long long need = (unit_bound + C::Lay::NU_MAX - 1) / C::Lay::NU_MAX;
+    if (need > P) P = need;
+    if (P > unit_bound) P = unit_bound > 0 ? unit_bound : 1;
+    if (P > 0x7fffffff) return cudaErrorNotSupported;
+    kern<<<(unsigned)P, C::NW * 32, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_persistent(const DecodeParams &p, int D, int G, bool partial,
+                                long long unit_bound, cudaStream_t st) {
+#define PA_CASE(DD, GG)                                                              \
+    if (D == DD && G == GG)                                                          \
+        return partial ? launch_persistent<T, DD, GG, true>(p, unit_bound, st)      \
+                       : launch_persistent<T, DD, GG, false>(p, unit_bound, st);
+    PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
+    PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
+#undef PA_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace pa
