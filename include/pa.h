@@ -203,6 +203,42 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
                           void *workspace, size_t workspace_bytes,
                           void *stream);
 
+/*
+ * pa_decode_partitioned_noalloc -- pa_decode_partitioned without a caller
+ * workspace, for callers that cannot allocate device memory where they
+ * decode (for example while another stream is being captured into a CUDA
+ * graph, under an allocator that forbids allocation after start-up, or in a
+ * plug-in whose host program owns all device memory).  It is an addition of
+ * this library with no counterpart on the reference pages.
+ *
+ * Same arguments, result and requirements as pa_decode_partitioned, minus
+ * `workspace` and `workspace_bytes`: the partition workspace is a fixed
+ * array of PA_NOALLOC_SCRATCH_BYTES compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  Problems whose
+ * pa_decode_partitioned_workspace_size(...) exceeds that size are rejected
+ * with PA_ERR_WORKSPACE before anything is launched.  Nothing is allocated
+ * or freed (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array, which keeps whatever
+ * the last call left in it (every entry a call reads is first written by the
+ * same call, so nothing needs clearing): calls whose kernels may overlap on
+ * the GPU -- on different streams, or from several host threads -- race on
+ * it and must be serialised by the caller.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+int pa_decode_partitioned_noalloc(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int64_t num_blocks,
+                                  int32_t block_size, int32_t max_blocks_per_seq,
+                                  int64_t q_seq_stride, float scale, int32_t dtype,
+                                  int32_t partition_size, int32_t max_seq_len,
+                                  void *stream);
+
 /* Human-readable text of a pa_status (static storage). */
 const char *pa_status_string(int status);
 

@@ -351,6 +351,70 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+}  // extern "C"
+
+// ---- split-KV decode without any allocation ---------------------------------
+//
+// Some callers cannot call cudaMalloc at the point where they decode: code
+// running while a CUDA graph is being captured on another stream, allocators
+// that forbid allocations after warm-up, or plug-ins handed device buffers
+// by a host program that owns all memory.  For them this entry point runs
+// the split-KV decode with its partition workspace in a fixed array compiled
+// into the library instead of a caller buffer.
+
+// The built-in workspace.  Every GPU that loads the library holds these
+// PA_NOALLOC_SCRATCH_BYTES until the process exits; every call on a device
+// shares them.
+static __device__ __align__(256) unsigned char noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.  In host code the
+// array's name is only a host-side stand-in, never a device address.
+cudaError_t noalloc_scratch_ptr(void **out) {
+    static std::mutex mu;
+    static void *cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev]) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cache[dev] = ptr;
+    *out = ptr;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_partitioned_noalloc(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+    int32_t block_size, int32_t max_blocks_per_seq, int64_t q_seq_stride, float scale,
+    int32_t dtype, int32_t partition_size, int32_t max_seq_len, void *stream) {
+    if (num_seqs == 0) return PA_OK;
+    const size_t need = pa_decode_partitioned_workspace_size(num_seqs, num_heads, head_dim,
+                                                             max_seq_len, partition_size);
+    if (need == 0) return PA_ERR_INVALID_ARG;
+    if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (noalloc_scratch_ptr(&scratch) != cudaSuccess) return PA_ERR_CUDA;
+    return pa_decode_partitioned(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                 num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                                 max_blocks_per_seq, q_seq_stride, scale, dtype,
+                                 partition_size, max_seq_len, scratch,
+                                 (size_t)PA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" {
+
 int pa_device_error(uint32_t *flags, int clear) {
     if (!flags) return PA_ERR_INVALID_ARG;
     unsigned int f = 0;

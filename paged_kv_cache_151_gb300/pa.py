@@ -67,6 +67,8 @@ def load():
         lib.pa_decode_partitioned_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.pa_decode_partitioned.restype = ctypes.c_int
         lib.pa_decode_partitioned.argtypes = dec + [i32, i32, P, sz, P]
+        lib.pa_decode_partitioned_noalloc.restype = ctypes.c_int
+        lib.pa_decode_partitioned_noalloc.argtypes = dec + [i32, i32, P]
         lib.pa_device_error.restype = ctypes.c_int
         lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         _lib = lib
@@ -198,6 +200,26 @@ def pa_decode_partitioned(out, q, k_cache, v_cache, block_tables, seq_lens, scal
     _check("pa_decode_partitioned", rc)
 
 
+# Bytes of the workspace built into the library for the call below.
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def pa_decode_partitioned_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                                  num_kv_heads, partition_size, max_seq_len, stream=None):
+    """Split-KV decode for callers that cannot allocate device memory: the
+    partition workspace is the library's built-in array of
+    PA_NOALLOC_SCRATCH_BYTES (shared by every call on the device, so calls
+    that may overlap on the GPU must be serialised).  The first call on a
+    device looks up that array; make it before any stream capture."""
+    args = _decode_args(out, q, k_cache, v_cache, block_tables, seq_lens)
+    if num_kv_heads != k_cache.shape[1]:
+        raise ValueError("num_kv_heads does not match the cache")
+    rc = load().pa_decode_partitioned_noalloc(*args, float(scale), _DTYPE[q.dtype],
+                                              int(partition_size), int(max_seq_len),
+                                              _stream(stream))
+    _check("pa_decode_partitioned_noalloc", rc)
+
+
 def workspace_views(workspace, num_seqs, num_heads, head_dim, max_seq_len, partition_size):
     """(o_part, m_part, l_part) fp32 views of a partitioned-decode workspace,
     following the layout documented in include/pa.h."""
@@ -226,6 +248,7 @@ __all__ = [
     "PAError", "load", "library_path", "pa_status_string", "pa_abi_version",
     "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_partitioned_workspace_size", "pa_decode_partitioned",
+    "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",
     "pa_device_error", "workspace_views",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SEQ_LEN", "PA_DEVERR_SLOT", "PA_DEVERR_TIMEOUT",
 ]
