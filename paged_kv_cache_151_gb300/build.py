@@ -56,9 +56,9 @@ def _digest(src: str, flags) -> str:
     return h.hexdigest()
 
 
-def _compile(src_name: str, force: bool, verbose: bool, extra) -> str:
+def _compile(src_name: str, force: bool, verbose: bool, extra, out_dir: str) -> str:
     src = os.path.join(CSRC, src_name)
-    obj = os.path.join(BUILD, src_name[:-3] + ".o")
+    obj = os.path.join(out_dir, src_name[:-3] + ".o")
     flags = ARCH + NVCC_FLAGS + list(extra)
     stamp = obj + ".sha"
     dig = _digest(src, flags)
@@ -79,23 +79,26 @@ def _compile(src_name: str, force: bool, verbose: bool, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = None) -> str:
+    """Compile and link the library; returns its path.  ``out_dir`` builds a
+    separate copy (for example with extra -D flags) instead of the default."""
+    out_dir = BUILD if out_dir is None else out_dir
+    lib_path = os.path.join(out_dir, LIB_NAME)
+    os.makedirs(out_dir, exist_ok=True)
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, force, verbose, extra_flags), srcs))
+        objs = list(ex.map(lambda s: _compile(s, force, verbose, extra_flags, out_dir), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or not os.path.exists(lib_path) or os.path.getmtime(lib_path) < newest:
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 def main(argv=None):

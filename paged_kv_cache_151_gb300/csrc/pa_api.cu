@@ -82,12 +82,20 @@ cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 g
     }
 }
 
+// Blocks per cluster of the persistent kernel.  Whole-sequence decode shares
+// each cluster's block stream over several SMs so that long sequences
+// spread out; partitions are already uniform work units.
+#ifndef PA_DECODE_CLUSTER
+#define PA_DECODE_CLUSTER 4
+#endif
+
 cudaError_t run_persistent(const pa::DecodeParams &p, int dtype, int D, int G, bool partial,
                            long long unit_bound, cudaStream_t st) {
+    const int cluster = partial ? 1 : PA_DECODE_CLUSTER;
     switch (dtype) {
-        case PA_F32: return pa::decode_persistent_f32(p, D, G, partial, unit_bound, st);
-        case PA_BF16: return pa::decode_persistent_bf16(p, D, G, partial, unit_bound, st);
-        default: return pa::decode_persistent_f16(p, D, G, partial, unit_bound, st);
+        case PA_F32: return pa::decode_persistent_f32(p, D, G, partial, unit_bound, cluster, st);
+        case PA_BF16: return pa::decode_persistent_bf16(p, D, G, partial, unit_bound, cluster, st);
+        default: return pa::decode_persistent_f16(p, D, G, partial, unit_bound, cluster, st);
     }
 }
 

@@ -210,6 +210,46 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
     return out;
 }
 
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int ld_acquire_dsmem_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.acquire.cluster.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_dsmem_s32(uint32_t addr, int v) {
+    asm volatile("st.release.cluster.shared::cluster.s32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+// monotonic publish: *addr = max(*addr, v), release at cluster scope
+__device__ __forceinline__ void red_max_release_dsmem(uint32_t addr, int v) {
+    asm volatile("red.release.cluster.shared::cluster.max.s32 [%0], %1;" :: "r"(addr), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_dsmem_s32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+// atomic add on a cluster-shared int with acquire-release ordering at
+// cluster scope; returns the old value
+__device__ __forceinline__ int atom_add_acq_rel_dsmem(uint32_t addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.cluster.shared::cluster.add.s32 %0, [%1], %2;"
+                 : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

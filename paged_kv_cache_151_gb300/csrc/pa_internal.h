@@ -21,11 +21,11 @@ cudaError_t decode_split_bf16(const DecodeParams &p, int D, int G, dim3 grid, in
 cudaError_t decode_split_f16(const DecodeParams &p, int D, int G, dim3 grid, int splits,
                              cudaStream_t st);
 cudaError_t decode_persistent_f32(const DecodeParams &p, int D, int G, bool partial,
-                                  long long unit_bound, cudaStream_t st);
+                                  long long unit_bound, int cluster, cudaStream_t st);
 cudaError_t decode_persistent_bf16(const DecodeParams &p, int D, int G, bool partial,
-                                   long long unit_bound, cudaStream_t st);
+                                   long long unit_bound, int cluster, cudaStream_t st);
 cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
-                                  long long unit_bound, cudaStream_t st);
+                                  long long unit_bound, int cluster, cudaStream_t st);
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

@@ -6,8 +6,8 @@
 namespace pa {
 
 cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
-                                long long unit_bound, cudaStream_t st) {
-    return dispatch_persistent<__half>(p, D, G, partial, unit_bound, st);
+                                long long unit_bound, int cluster, cudaStream_t st) {
+    return dispatch_persistent<__half>(p, D, G, partial, unit_bound, cluster, st);
 }
 
 }  // namespace pa

@@ -6,8 +6,8 @@
 namespace pa {
 
 cudaError_t decode_persistent_f32(const DecodeParams &p, int D, int G, bool partial,
-                                long long unit_bound, cudaStream_t st) {
-    return dispatch_persistent<float>(p, D, G, partial, unit_bound, st);
+                                long long unit_bound, int cluster, cudaStream_t st) {
+    return dispatch_persistent<float>(p, D, G, partial, unit_bound, cluster, st);
 }
 
 }  // namespace pa

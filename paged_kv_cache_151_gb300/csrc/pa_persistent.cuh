@@ -1,5 +1,6 @@
-// pa_persistent.cuh -- persistent decode kernel: one resident thread block
-// per SM slot streams a balanced list of work units end to end.
+// pa_persistent.cuh -- persistent decode kernel: resident thread blocks,
+// grouped in thread-block clusters, stream a balanced list of work units end
+// to end.
 //
 // A work unit is (sequence, KV head) for pa_decode, or (sequence, KV head,
 // token partition) for pa_decode_partitioned.  Every block:
@@ -7,26 +8,32 @@
 //  1. reads all seq_lens and sorts the sequences by block count, longest
 //     first (bitonic sort in shared memory; ties by index, so the order is
 //     deterministic);
-//  2. numbers the units in that order and takes ranks p, 2P-1-p, 2P+p, ...
-//     (P blocks in the grid, "snake" order), which deals the longest units
-//     out first and evens the per-block totals (longest-processing-time
-//     first);
-//  3. concatenates the 16-token blocks of its units into one stream and
-//     deals the stream round-robin to its warps: stream position f goes to
-//     warp f mod NW.  Each warp keeps a ring of S stages filled with 1-D bulk
-//     copies (cp.async.bulk on an mbarrier) of its next blocks' K and V
-//     tiles, running ahead across unit boundaries, so the copy engine never
-//     waits for a unit to be merged;
-//  4. when a warp leaves a unit it parks its (m, l, acc) in one of R merge
-//     slots; the last of the unit's warps to arrive merges them and writes
-//     the unit's output (pa_decode) or its partition statistics
-//     (pa_decode_partitioned), while the other warps stream on.
+//  2. numbers the units in that order; cluster c of the NC clusters takes
+//     ranks c, 2NC-1-c, 2NC+c, ... ("snake" order), which deals the longest
+//     units out first and evens the per-cluster totals;
+//  3. concatenates the 16-token blocks of its cluster's units into one
+//     stream of F blocks and gives warp g of the cluster's C*NW warps the
+//     contiguous range [g*F/(C*NW), (g+1)*F/(C*NW)): every warp gets the same
+//     number of blocks (to one), and a long unit spreads over several warps
+//     and SMs.  Each warp keeps a ring of S stages filled with bulk copies
+//     (tensor-map copies of whole swizzled tiles for 16-bit caches, 1-D
+//     copies of the valid rows for fp32) of its next blocks' K and V, running
+//     ahead across unit boundaries;
+//  4. a unit that lies inside one warp's range is finished by that warp
+//     alone.  A unit that crosses range boundaries leaves one partial
+//     (m, l, acc) per warp that touched it -- each warp has one slot for the
+//     unit it starts in and one for the unit it ends in, so slots are never
+//     reused -- and the last of those warps to arrive (an atomic counter of
+//     the unit's first warp, in distributed shared memory when the warps
+//     span several blocks) merges the partials in warp order and writes the
+//     unit's output (pa_decode) or partition statistics
+//     (pa_decode_partitioned).  No warp ever waits for another.
 //
-// Everything a unit's result depends on -- the unit order, the warp that
-// handles each block, the merge order -- is a function of seq_lens and the
-// logical block index only, never of where the blocks sit in the pool, so
-// outputs are bit-identical under any permutation of physical blocks and
-// under prefix aliasing.
+// Everything a unit's result depends on -- the unit order, the block ranges,
+// the merge order -- is a function of seq_lens and logical block indices
+// only, never of where the blocks sit in the pool, so outputs are
+// bit-identical under any permutation of physical blocks and under prefix
+// aliasing.
 #pragma once
 
 #include <type_traits>
@@ -42,20 +49,24 @@ struct UnitRec {
     int s, j, lb0, nb, L, part;
 };
 
-template <typename T, int D, int G, int NW, int S>
+template <typename T, int D, int G, int NW, int S, bool PARTIAL>
 struct PersistentLayout {
     using Sh = Shape<T, D>;
-    static constexpr int R = 2;                           // merge slots in flight
-    static constexpr int NU_MAX = 160;                    // units per block
+    static constexpr int NU_MAX = 160;                    // units per cluster
     static constexpr size_t STAGES = (size_t)NW * S * 2 * Sh::TILE_BYTES;
-    static constexpr size_t SLOT_FLOATS = (size_t)NW * (G * D + 2 * G);
+    // one partial: O[G][D], M[G], L[G], padded to 16 bytes
+    static constexpr size_t PART_FLOATS = ((size_t)G * D + 2 * G + 3) / 4 * 4;
     static constexpr size_t OFF_BARS = STAGES;
     static constexpr size_t OFF_SCR = OFF_BARS + (size_t)NW * S * 8;
-    static constexpr size_t OFF_SLOTS = OFF_SCR + (size_t)NW * warp_scratch_floats<G>() * 4;
-    static constexpr size_t OFF_UNITS = OFF_SLOTS + (size_t)R * SLOT_FLOATS * 4;
+    static constexpr size_t OFF_PARTS = OFF_SCR + (size_t)NW * warp_scratch_floats<G>() * 4;
+    static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * 2 * PART_FLOATS * 4;
     static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
-    static constexpr size_t OFF_CTL = OFF_CUM + (size_t)(NU_MAX + 1) * 4;
+    static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
     static constexpr size_t BYTES = OFF_CTL + 64 + 1024;   // + alignment of the base
+    static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
+    static_assert(OFF_SCR % 16 == 0 && OFF_PARTS % 16 == 0 && OFF_UNITS % 16 == 0 &&
+                      OFF_CTL % 16 == 0 && PART_FLOATS % 4 == 0,
+                  "shared-memory regions must stay 16-byte aligned");
     // the sort scratch (keys, padded to a power of two, + scan) lives in the
     // stage region before streaming: at most 12 bytes per sequence
     static constexpr int MAX_SEQS = (int)(STAGES / 12) > 65535 ? 65535 : (int)(STAGES / 12);
@@ -97,13 +108,14 @@ __global__ void __launch_bounds__(NW * 32)
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr bool TC = use_tc<T>();
     using W = std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>;
-    using Lay = PersistentLayout<T, D, G, NW, S>;
+    using Lay = PersistentLayout<T, D, G, NW, S, PARTIAL>;
     using Sh = Shape<T, D>;
-    constexpr int E = Sh::E, NCH = Sh::NCH;
+    constexpr int E = Sh::E;
     constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
     constexpr int NT = NW * 32;
-    constexpr int R = Lay::R, NU_MAX = Lay::NU_MAX;
+    constexpr int NU_MAX = Lay::NU_MAX;
     constexpr int WS = warp_scratch_floats<G>();
+    constexpr int PF = (int)Lay::PART_FLOATS;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzle pattern is tied to 1024-byte aligned addresses
@@ -111,19 +123,21 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     unsigned char *stages = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);
     float *scr = reinterpret_cast<float *>(smem + Lay::OFF_SCR);
-    float *slots = reinterpret_cast<float *>(smem + Lay::OFF_SLOTS);
+    float *parts = reinterpret_cast<float *>(smem + Lay::OFF_PARTS);   // [NW][2][PF]
     UnitRec *units = reinterpret_cast<UnitRec *>(smem + Lay::OFF_UNITS);
     int *cum = reinterpret_cast<int *>(smem + Lay::OFF_CUM);
     int *ctl = reinterpret_cast<int *>(smem + Lay::OFF_CTL);
-    volatile int *slot_cnt = ctl;          // [R] warps that parked in the slot
-    volatile int *slot_done = ctl + R;     // [R] last unit merged from the slot
-    int *nu_sh = ctl + 2 * R;              // units of this block
-    int *wtot = ctl + 2 * R + 1;           // [NW] scan scratch
+    int *arrive = ctl;                       // [NW] warps done with the unit that
+                                             //      starts in this warp's range
+    int *wtot = ctl + NW;                    // [NW] scan scratch
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
     const int cap = PARTIAL ? min(p.max_seq_len, p.max_blocks * 16) : p.max_blocks * 16;
     const int PB = PARTIAL ? p.partition_blocks : 1;
+    const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+    const int NWC = C * NW;                  // warps of the cluster
+    const int gw = rank * NW + warp;         // this warp's index in the cluster
 
     auto seq_len = [&](int s) -> int {
         int L = p.seq_lens[s];
@@ -179,14 +193,14 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     }
     __syncthreads();
 
-    // ---- 3. this block's units (snake over the ranks) -------------------------
-    const int P = gridDim.x, me = blockIdx.x;
+    // ---- 3. this cluster's units (snake over the ranks) -----------------------
+    const int NC = gridDim.x / C, me = blockIdx.x / C;
     auto rank_of = [&](int q) -> long long {
-        return (long long)q * P + ((q & 1) ? (P - 1 - me) : me);
+        return (long long)q * NC + ((q & 1) ? (NC - 1 - me) : me);
     };
     int nu = 0;
     while (rank_of(nu) < U) ++nu;
-    if (nu > NU_MAX) {
+    if (nu > NU_MAX) {                             // the host sizes the grid to avoid this
         if (tid == 0) set_error(p.err, ERR_SEQ_LEN);
         nu = NU_MAX;
     }
@@ -232,25 +246,20 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             if (q < nu) cum[q] = run + x - v;
             run += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) {
-            cum[nu] = run;
-            *nu_sh = nu;
-        }
+        if (lane == 0) cum[nu] = run;
     }
+    if (tid < NW) arrive[tid] = 0;
     if (tid == 0) {
         for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
-        for (int i = 0; i < R; ++i) {
-            slot_cnt[i] = 0;
-            slot_done[i] = i - R;
-        }
     }
     // the sort scratch in the stage region is overwritten by bulk copies next
     fence_proxy_async_smem();
     __syncthreads();
+    if (C > 1) cluster_sync();                     // peers' counters are initialised
 
     // units with no tokens (pa_decode only): their output is zero
-    if (!PARTIAL && warp == NW - 1) {
+    if (!PARTIAL && rank == 0 && warp == NW - 1) {
         for (int q = 0; q < nu; ++q) {
             const UnitRec u = units[q];
             if (u.nb != 0) continue;
@@ -264,9 +273,14 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         }
     }
 
-    // ---- 4. stream this warp's blocks: positions warp, warp+NW, ... ---------
+    // ---- 4. stream this warp's range of the cluster's blocks ------------------
     const int F = cum[nu];
-    const int n_mine = F > warp ? (F - warp + NW - 1) / NW : 0;
+    auto range_lo = [&](int g) -> int { return (int)((long long)g * F / NWC); };
+    auto owner = [&](int f) -> int {               // warp whose range holds position f
+        return (int)(((long long)(f + 1) * NWC - 1) / F);
+    };
+    const int my_lo = range_lo(gw), my_hi = range_lo(gw + 1);
+    const int n_mine = my_hi - my_lo;
     auto locate = [&](int f) -> int {              // unit holding stream position f
         int lo = 0, hi = nu - 1;
         while (lo < hi) {
@@ -280,7 +294,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         ui = -1;
         pb = 0;
         if (k < n_mine) {
-            const int f = warp + k * NW;
+            const int f = my_lo + k;
             ui = locate(f);
             const UnitRec &u = units[ui];
             const int lb = u.lb0 + (f - cum[ui]);
@@ -301,7 +315,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     };
     auto rows_of = [&](int k, int ui) -> int {
         const UnitRec &u = units[ui];
-        const int lb = u.lb0 + (warp + k * NW - cum[ui]);
+        const int lb = u.lb0 + (my_lo + k - cum[ui]);
         return min(16, u.L - lb * 16);
     };
 
@@ -349,87 +363,98 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     float *Pb = Sc + 16 * G;
     float *Al = Pb + 16 * G;
 
-    // Leave unit `ui`: park this warp's partial in the unit's slot; the last
-    // of the unit's warps merges the slot and writes the result.
-    auto leave_unit = [&](int ui) -> bool {
-        wa.finish();
-        const int slot = ui % R;
-        float *base = slots + (size_t)slot * Lay::SLOT_FLOATS;
-        float *Mw = base, *Lw = base + NW * G, *Aw = base + 2 * NW * G;
-        // wait (bounded) until the slot's previous unit has been merged
-        bool ok = true;
-        if (slot_done[slot] != ui - R) {
-            const unsigned long long t0 = globaltimer();
-            while (slot_done[slot] != ui - R) {
-                if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-                    if (lane == 0) set_error(p.err, ERR_TIMEOUT);
-                    ok = false;
-                    break;
-                }
+    // Partial slots of warp g (in block g / NW): slot 0 holds the unit the
+    // warp's range starts inside of (shared with earlier warps, ending in this
+    // range); slot 1 holds the unit that runs past the end of the range, and
+    // before that, one at a time, the units lying wholly inside the range
+    // (the warp merges those itself at once).
+    auto part_of = [&](int g, int which) -> float * {
+        return parts + ((size_t)(g % NW) * 2 + which) * PF;
+    };
+
+    // Write the result of unit u from a merged (M, L, O) of chunk (g, d0).
+    auto emit = [&](const UnitRec &u, int g, int d0, float M, float Ls, float *O) {
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        if constexpr (PARTIAL) {
+            const long long row = ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
+            float *po = p.part_o + row * D + d0;
+#pragma unroll
+            for (int e = 0; e < E; e += 4)
+                *reinterpret_cast<float4 *>(po + e) =
+                    make_float4(O[e] * inv, O[e + 1] * inv, O[e + 2] * inv, O[e + 3] * inv);
+            if (d0 == 0) {
+                p.part_m[row] = M * LN2;          // natural units
+                p.part_l[row] = Ls;
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) O[e] *= inv;
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d0;
+            store_chunk<T>(o, O);
         }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return false;
-        wa.store_partial(Mw + warp * G, Lw + warp * G, Aw + warp * G * D);
-        __threadfence_block();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd((int *)&slot_cnt[slot], 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
+    };
+
+    // Leave unit `ui`: park this warp's partial; the last warp of the unit
+    // merges every partial of the unit (in warp order) and writes the result.
+    auto leave_unit = [&](int ui) {
+        wa.finish();
         const UnitRec u = units[ui];
-        const int contributors = min(u.nb, NW);
-        if (old == contributors - 1) {
-            __threadfence_block();
-            const int first = cum[ui] % NW;        // warp of the unit's first block
+        const int u_lo = cum[ui], u_hi = cum[ui] + u.nb;
+        const bool from_before = u_lo < my_lo, to_after = u_hi > my_hi;
+        float *mine = part_of(gw, (from_before && !to_after) ? 0 : 1);
+        // partial layout: O[G][D], M[G], L[G]
+        wa.store_partial(mine + G * D, mine + G * D + G, mine);
+        __syncwarp();
+        bool last = true;
+        const int g_first = owner(u_lo), g_last = owner(u_hi - 1);
+        if (from_before || to_after) {
+            // count this warp in at the unit's first warp
+            int n_part = 0;                        // warps whose range is not empty
+            for (int g = g_first; g <= g_last; ++g) n_part += range_lo(g) < range_lo(g + 1);
+            int old = 0;
+            if (lane == 0) {
+                fence_acq_rel_cluster();
+                old = atom_add_acq_rel_dsmem(map_to_rank(&arrive[g_first % NW], g_first / NW), 1);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            last = old == n_part - 1;
+            if (last) fence_acq_rel_cluster();
+        }
+        if (last) {
             for (int ch = lane; ch < G * (D / E); ch += 32) {
                 const int g = ch / (D / E), d0 = (ch % (D / E)) * E;
                 float M = -INFINITY;
-                for (int i = 0; i < contributors; ++i) {
-                    const int w = (first + i) % NW;
-                    M = fmaxf(M, Mw[w * G + g]);
+                for (int w = g_first; w <= g_last; ++w) {
+                    if (range_lo(w) == range_lo(w + 1)) continue;
+                    const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
+                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(pw + G * D + g, w / NW)));
                 }
                 float O[E], Ls = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) O[e] = 0.f;
                 if (M != -INFINITY) {
-                    for (int i = 0; i < contributors; ++i) {
-                        const int w = (first + i) % NW;
-                        const float mw = Mw[w * G + g];
+                    for (int w = g_first; w <= g_last; ++w) {
+                        if (range_lo(w) == range_lo(w + 1)) continue;
+                        const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
+                        const uint32_t rw = (uint32_t)(w / NW);
+                        const float mw = ld_dsmem_f32(map_to_rank(pw + G * D + g, rw));
                         const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-                        Ls = fmaf(f, Lw[w * G + g], Ls);
-                        const float *a = Aw + (w * G + g) * D + d0;
+                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(pw + G * D + G + g, rw)), Ls);
 #pragma unroll
-                        for (int e = 0; e < E; ++e) O[e] = fmaf(f, a[e], O[e]);
+                        for (int e = 0; e < E; e += 4) {
+                            const float4 a = ld_dsmem_f32x4(map_to_rank(pw + g * D + d0 + e, rw));
+                            O[e] = fmaf(f, a.x, O[e]);
+                            O[e + 1] = fmaf(f, a.y, O[e + 1]);
+                            O[e + 2] = fmaf(f, a.z, O[e + 2]);
+                            O[e + 3] = fmaf(f, a.w, O[e + 3]);
+                        }
                     }
                 }
-                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                if constexpr (PARTIAL) {
-                    const long long row = ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
-                    float *po = p.part_o + row * D + d0;
-#pragma unroll
-                    for (int e = 0; e < E; e += 4)
-                        *reinterpret_cast<float4 *>(po + e) =
-                            make_float4(O[e] * inv, O[e + 1] * inv, O[e + 2] * inv, O[e + 3] * inv);
-                    if (d0 == 0) {
-                        p.part_m[row] = M * LN2;      // natural units
-                        p.part_l[row] = Ls;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) O[e] *= inv;
-                    T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d0;
-                    store_chunk<T>(o, O);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                slot_cnt[slot] = 0;
-                __threadfence_block();
-                slot_done[slot] = ui;
+                emit(u, g, d0, M, Ls, O);
             }
         }
+        __syncwarp();
         wa.reset();
-        return true;
     };
 
     int cur = -1;
@@ -445,7 +470,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         int ui, pbk;
         of(k, ui, pbk);
         if (ui != cur) {
-            if (cur >= 0 && !leave_unit(cur)) { ok = false; break; }
+            if (cur >= 0) leave_unit(cur);
             cur = ui;
             const UnitRec &u = units[ui];
             const T *qp = reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
@@ -479,7 +504,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             if (lane == 0) issue(kn, uin, pbn);
         }
     }
-    if (ok && cur >= 0) ok = leave_unit(cur);
+    // a timeout leaves the unit unmerged (its output is not written; the
+    // error word says so); otherwise finish the last unit
+    if (ok && cur >= 0) leave_unit(cur);
 
     // after a timeout: wait (bounded) for this warp's copies still in flight
     if (!ok) {
@@ -487,6 +514,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         for (int k = k_done; k < issued; ++k)
             mbar_wait_bounded(&my_bars[k % S], (uint32_t)((k / S) & 1), p.err);
     }
+    // keep this block's shared memory alive while peers may still read it
+    __syncthreads();
+    if (C > 1) cluster_sync();
 }
 
 // Stages per warp: about 16 KiB of K+V in flight per warp, at least 2.
@@ -500,7 +530,7 @@ template <typename T, int D, int G, bool PARTIAL>
 struct PersistentConfig {
     static constexpr int NW = 4;
     static constexpr int S = persistent_stages<T, D>();
-    using Lay = PersistentLayout<T, D, G, NW, S>;
+    using Lay = PersistentLayout<T, D, G, NW, S, PARTIAL>;
 };
 
 // Largest num_seqs the persistent kernel sorts in shared memory.
@@ -509,38 +539,63 @@ constexpr int persistent_max_seqs() {
     return PersistentConfig<T, D, G, PARTIAL>::Lay::MAX_SEQS;
 }
 
+// Clusters of `cluster` blocks, as many as fit on the GPU at once (looked up
+// once per device and cluster size), but at least enough that no cluster
+// gets more than NU_MAX units.
 template <typename T, int D, int G, bool PARTIAL>
-cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, cudaStream_t st) {
+cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int cluster,
+                              cudaStream_t st) {
     using C = PersistentConfig<T, D, G, PARTIAL>;
     constexpr size_t smem = C::Lay::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory");
     auto kern = decode_persistent_kernel<T, D, G, C::NW, C::S, PARTIAL>;
     if (p.num_seqs > C::Lay::MAX_SEQS) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
+    static int fitted[64][4];                      // clusters resident per device, per size
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NW * 32, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    int sms = sm_count_of_current_device();
-    if (sms <= 0) sms = 152;
-    long long P = (long long)sms * per_sm;
+    const int ci = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : 3;
+    int nc = (dev >= 0 && dev < 64) ? fitted[dev][ci] : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::NW * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (nc <= 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(cluster * 64), 1, 1);
+        e = cudaOccupancyMaxActiveClusters(&nc, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (nc < 1) nc = 1;
+        if (dev >= 0 && dev < 64) fitted[dev][ci] = nc;
+    }
+    long long NC = nc;
     const long long need = (unit_bound + C::Lay::NU_MAX - 1) / C::Lay::NU_MAX;
-    if (need > P) P = need;
-    if (P > unit_bound) P = unit_bound > 0 ? unit_bound : 1;
-    if (P > 0x7fffffff) return cudaErrorNotSupported;
-    kern<<<(unsigned)P, C::NW * 32, smem, st>>>(p);
+    if (need > NC) NC = need;
+    if (NC > unit_bound) NC = unit_bound > 0 ? unit_bound : 1;
+    if (NC * cluster > 0x7fffffffLL) return cudaErrorNotSupported;
+    cfg.gridDim = dim3((unsigned)(NC * cluster), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t dispatch_persistent(const DecodeParams &p, int D, int G, bool partial,
-                                long long unit_bound, cudaStream_t st) {
-#define PA_CASE(DD, GG)                                                              \
-    if (D == DD && G == GG)                                                          \
-        return partial ? launch_persistent<T, DD, GG, true>(p, unit_bound, st)      \
-                       : launch_persistent<T, DD, GG, false>(p, unit_bound, st);
+                                long long unit_bound, int cluster, cudaStream_t st) {
+#define PA_CASE(DD, GG)                                                                   \
+    if (D == DD && G == GG)                                                               \
+        return partial ? launch_persistent<T, DD, GG, true>(p, unit_bound, cluster, st)  \
+                       : launch_persistent<T, DD, GG, false>(p, unit_bound, cluster, st);
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
 #undef PA_CASE
