@@ -177,6 +177,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// Bring a tensor-map descriptor (kernel parameter) into the TMA unit's cache.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
+}
+
 // L2 policy for data read once per call (the streamed K/V tiles).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

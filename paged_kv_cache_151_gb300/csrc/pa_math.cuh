@@ -95,6 +95,7 @@ struct WarpAttn {
 
     int lane, r, c, g_sm, row0;
     float qreg[G][E];
+    uint4 qraw[G];                  // the next unit's query chunks, loaded ahead
     float acc[G][E];
     float m_run, l_run;
 
@@ -128,13 +129,42 @@ struct WarpAttn {
     // query slice of this lane straight from global memory: q points at the
     // first of the G heads ([G][D], 16-byte aligned rows)
     __device__ __forceinline__ void load_q_global(const T *q, float scale_log2) {
+        prefetch_q(q);
+        take_q(scale_log2);
+    }
+
+    __device__ __forceinline__ void prefetch_q(const T *q) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            qraw[g] = __ldg(reinterpret_cast<const uint4 *>(q + g * D + c * E));
+    }
+
+    __device__ __forceinline__ void take_q(float scale_log2) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(q + g * D + c * E));
             float f[E];
-            Elem<T>::to_f32(raw, f);
+            Elem<T>::to_f32(qraw[g], f);
 #pragma unroll
             for (int e = 0; e < E; ++e) qreg[g][e] = f[e] * scale_log2;
+        }
+    }
+
+    // After finish(): this warp's own result for its G heads (a unit no other
+    // warp touched).  f(g, d, v0, v1, first, m, l) gets the normalised outputs
+    // of head g at d, d+1; `first` marks one call per head, which also carries
+    // the head's running maximum m (log2 units) and sum l.
+    template <typename Fn>
+    __device__ __forceinline__ void for_each_result(Fn &&f) const {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float l = __shfl_sync(0xffffffffu, l_run, g * LPH);
+            const float m = __shfl_sync(0xffffffffu, m_run, g * LPH);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            if (r == 0) {
+#pragma unroll
+                for (int e = 0; e < E; e += 2)
+                    f(g, c * E + e, acc[g][e] * inv, acc[g][e + 1] * inv, c == 0 && e == 0, m, l);
+            }
         }
     }
 
@@ -288,6 +318,25 @@ __device__ __forceinline__ void store_chunk<__half>(__half *dst, const float *v)
     h = __floats2half2_rn(v[4], v[5]); o.z = *reinterpret_cast<uint32_t *>(&h);
     h = __floats2half2_rn(v[6], v[7]); o.w = *reinterpret_cast<uint32_t *>(&h);
     *reinterpret_cast<uint4 *>(dst) = o;
+}
+
+// Store two fp32 values as two consecutive elements of T.
+template <typename T>
+__device__ __forceinline__ void store_pair(T *dst, float a, float b);
+
+template <>
+__device__ __forceinline__ void store_pair<float>(float *dst, float a, float b) {
+    *reinterpret_cast<float2 *>(dst) = make_float2(a, b);
+}
+
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16 *dst, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(a, b);
+}
+
+template <>
+__device__ __forceinline__ void store_pair<__half>(__half *dst, float a, float b) {
+    *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(a, b);
 }
 
 }  // namespace pa

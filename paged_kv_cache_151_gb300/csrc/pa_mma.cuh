@@ -102,6 +102,7 @@ struct WarpAttnTC {
     int lane, g, t;
     bool head_ok;                          // this lane's row g is a real head
     uint32_t qa0[KS], qa2[KS];             // A fragments of Q (rows 0..7)
+    uint32_t qn0[KS], qn2[KS];             // the next unit's, loaded ahead
     float acc[NT][4];                      // O fragments ([2],[3]: rows 8..15, unused)
     float m_run, l_run;
 
@@ -124,12 +125,39 @@ struct WarpAttnTC {
 
     // q points at the first of the G heads ([G][D] of T); rows >= G are zero
     __device__ __forceinline__ void load_q_global(const T *q) {
+        prefetch_q(q);
+        take_q();
+    }
+
+    // start loading the next unit's query fragments (used by take_q)
+    __device__ __forceinline__ void prefetch_q(const T *q) {
         const uint32_t *qw = reinterpret_cast<const uint32_t *>(q + (head_ok ? g : 0) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qa0[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t) / 2) : 0u;
-            qa2[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t + 8) / 2) : 0u;
+            qn0[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t) / 2) : 0u;
+            qn2[ks] = head_ok ? __ldg(qw + (16 * ks + 2 * t + 8) / 2) : 0u;
         }
+    }
+
+    __device__ __forceinline__ void take_q() {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qa0[ks] = qn0[ks];
+            qa2[ks] = qn2[ks];
+        }
+    }
+
+    // After finish(): this warp's own result for its G heads (a unit no other
+    // warp touched).  f(g, d, v0, v1, first, m, l) gets the normalised outputs
+    // of head g at d, d+1; `first` marks one call per head, which also carries
+    // the head's running maximum m (log2 units) and sum l.
+    template <typename Fn>
+    __device__ __forceinline__ void for_each_result(Fn &&f) const {
+        if (!head_ok) return;
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+            f(g, 8 * j + 2 * t, acc[j][0] * inv, acc[j][1] * inv, t == 0 && j == 0, m_run, l_run);
     }
 
     // One block: kt, vt are shared-memory addresses of the swizzled tiles.

@@ -62,15 +62,100 @@ struct PersistentLayout {
     static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * 2 * PART_FLOATS * 4;
     static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
     static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
-    static constexpr size_t BYTES = OFF_CTL + 64 + 1024;   // + alignment of the base
+    static constexpr size_t BYTES = OFF_CTL + 256 + 1024;   // + alignment of the base
     static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
     static_assert(OFF_SCR % 16 == 0 && OFF_PARTS % 16 == 0 && OFF_UNITS % 16 == 0 &&
                       OFF_CTL % 16 == 0 && PART_FLOATS % 4 == 0,
                   "shared-memory regions must stay 16-byte aligned");
-    // the sort scratch (keys, padded to a power of two, + scan) lives in the
-    // stage region before streaming: at most 12 bytes per sequence
-    static constexpr int MAX_SEQS = (int)(STAGES / 12) > 65535 ? 65535 : (int)(STAGES / 12);
+    // the sort scratch (keys padded to a power of two >= the thread count,
+    // scan, lengths) lives in the stage region before streaming: at most 16
+    // bytes per sequence
+    static constexpr int MAX_SEQS = (int)(STAGES / 16) > 65535 ? 65535 : (int)(STAGES / 16);
 };
+
+// In-thread compare-exchange of a bitonic network stage with stride J < EPT
+// (elements t*EPT .. t*EPT+EPT-1 in registers).
+template <int EPT, int J>
+__device__ __forceinline__ void bitonic_local(uint32_t (&v)[EPT], int t, int k) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        const int e2 = e ^ J;
+        if (e2 > e) {
+            const bool up = ((t * EPT + e) & k) == 0;
+            const uint32_t a = v[e], b = v[e2];
+            if ((a > b) == up) { v[e] = b; v[e2] = a; }
+        }
+    }
+}
+
+// Ascending bitonic sort of keys[0 .. EPT*NT) (distinct values), EPT per
+// thread in registers: strides inside a thread are register swaps, strides
+// inside a warp are shuffles, and only strides that cross warps go through
+// shared memory.
+template <int EPT, int NT>
+__device__ __forceinline__ void bitonic_sort_regs(uint32_t *keys) {
+    constexpr int N = EPT * NT;
+    const int t = threadIdx.x;
+    uint32_t v[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) v[e] = keys[t * EPT + e];
+    for (int k = 2; k <= N; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            if (jj < EPT) {
+                if constexpr (EPT > 1) { if (jj == 1) bitonic_local<EPT, 1>(v, t, k); }
+                if constexpr (EPT > 2) { if (jj == 2) bitonic_local<EPT, 2>(v, t, k); }
+                if constexpr (EPT > 4) { if (jj == 4) bitonic_local<EPT, 4>(v, t, k); }
+            } else if (jj < 32 * EPT) {
+                const int m = jj / EPT;
+                const bool lower = (t & m) == 0;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const bool up = ((t * EPT + e) & k) == 0;
+                    const uint32_t b = __shfl_xor_sync(0xffffffffu, v[e], m);
+                    v[e] = (lower == up) ? min(v[e], b) : max(v[e], b);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) keys[t * EPT + e] = v[e];
+                __syncthreads();
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const int i = t * EPT + e, ixj = i ^ jj;
+                    const uint32_t b = keys[ixj];
+                    const bool up = (i & k) == 0;
+                    v[e] = ((i < ixj) == up) ? min(v[e], b) : max(v[e], b);
+                }
+                __syncthreads();
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) keys[t * EPT + e] = v[e];
+    __syncthreads();
+}
+
+// Ascending sort of keys[0 .. Np) (Np a power of two >= NT, distinct values).
+template <int NT>
+__device__ void sort_keys(uint32_t *keys, int Np) {
+    if (Np == NT) { bitonic_sort_regs<1, NT>(keys); return; }
+    if (Np == 2 * NT) { bitonic_sort_regs<2, NT>(keys); return; }
+    if (Np == 4 * NT) { bitonic_sort_regs<4, NT>(keys); return; }
+    if (Np == 8 * NT) { bitonic_sort_regs<8, NT>(keys); return; }
+    const int tid = threadIdx.x;                   // larger batches: shared memory only
+    for (int k = 2; k <= Np; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int i = tid; i < Np; i += NT) {
+                const int ixj = i ^ jj;
+                if (ixj > i) {
+                    const uint32_t a = keys[i], b = keys[ixj];
+                    const bool up = (i & k) == 0;
+                    if ((a > b) == up) { keys[i] = b; keys[ixj] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
 
 // Exclusive scan of one int per thread across the block; returns this
 // thread's exclusive prefix and writes the total to *total.
@@ -103,6 +188,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
 template <typename T>
 __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
+// What a warp pays to enter a unit (load its query, park or write its
+// result), in quarters of one 16-token block; used to split the stream.
+#ifndef PA_UNIT_COST_Q4
+#define PA_UNIT_COST_Q4 4
+#endif
+
 template <typename T, int D, int G, int NW, int S, bool PARTIAL>
 __global__ void __launch_bounds__(NW * 32)
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
@@ -116,6 +207,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr int NU_MAX = Lay::NU_MAX;
     constexpr int WS = warp_scratch_floats<G>();
     constexpr int PF = (int)Lay::PART_FLOATS;
+    constexpr int UNIT_COST = PA_UNIT_COST_Q4;     // quarter blocks charged per unit
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzle pattern is tied to 1024-byte aligned addresses
@@ -130,6 +222,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     int *arrive = ctl;                       // [NW] warps done with the unit that
                                              //      starts in this warp's range
     int *wtot = ctl + NW;                    // [NW] scan scratch
+    int *bound = ctl + 2 * NW;               // [C*NW + 1] warp ranges of the stream
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
@@ -139,40 +232,32 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     const int NWC = C * NW;                  // warps of the cluster
     const int gw = rank * NW + warp;         // this warp's index in the cluster
 
-    auto seq_len = [&](int s) -> int {
-        int L = p.seq_lens[s];
-        return L < 0 ? 0 : (L > cap ? cap : L);
-    };
-
     // ---- 1. sort the sequences by block count (longest first) ----------------
-    int Bp = 1;
+    if constexpr (TC) {
+        if (tid == 0) {                            // fetch the descriptors early
+            prefetch_tensormap(&p.tmap_k);
+            prefetch_tensormap(&p.tmap_v);
+        }
+    }
+    int Bp = NT;
     while (Bp < B) Bp <<= 1;
-    uint32_t *keys = reinterpret_cast<uint32_t *>(stages);
-    int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(stages);           // [Bp]
+    int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);   // [B]
+    int *lens = start + B;                                           // [B], clamped
     for (int i = tid; i < Bp; i += NT) {
         uint32_t key = 0xffffffffu;
         if (i < B) {
             const int L0 = p.seq_lens[i];
             if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
-            const int nb = (seq_len(i) + 15) >> 4;
+            const int L = L0 < 0 ? 0 : (L0 > cap ? cap : L0);
+            lens[i] = L;
+            const int nb = (L + 15) >> 4;
             key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
         }
         keys[i] = key;
     }
     __syncthreads();
-    for (int k = 2; k <= Bp; k <<= 1) {
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int i = tid; i < Bp; i += NT) {
-                const int ixj = i ^ jj;
-                if (ixj > i) {
-                    const uint32_t a = keys[i], b = keys[ixj];
-                    const bool up = (i & k) == 0;
-                    if ((a > b) == up) { keys[i] = b; keys[ixj] = a; }
-                }
-            }
-            __syncthreads();
-        }
-    }
+    sort_keys<NT>(keys, Bp);
 
     // ---- 2. number the units: exclusive scan of units per sorted sequence -----
     auto units_of = [&](int pos) -> int {          // pos < B
@@ -216,7 +301,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         const int local = r - start[lo];
         UnitRec u;
         u.s = s;
-        u.L = seq_len(s);
+        u.L = lens[s];
         if (PARTIAL) {
             const int ps = (nb + PB - 1) / PB;
             u.j = local / ps;
@@ -247,6 +332,36 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             run += __shfl_sync(0xffffffffu, x, 31);
         }
         if (lane == 0) cum[nu] = run;
+        __syncwarp();
+        // Split the stream into C*NW ranges of equal cost, a block costing 4
+        // and each unit a warp enters a further UNIT_COST (quarter blocks):
+        // in a virtual stream where every unit starts with UNIT_COST/4 header
+        // blocks, cut at equal steps and move each cut to a real block.
+        int nz = 0;                                // units with blocks (they come first)
+        for (int base = 0; base < nu; base += 32) {
+            const int q = base + lane;
+            nz += __popc(__ballot_sync(0xffffffffu, q < nu && units[q].nb > 0));
+        }
+        const long long vtot = 4LL * run + (long long)nz * UNIT_COST;
+        auto vstart = [&](int q) -> long long {
+            return 4LL * cum[q] + (long long)min(q, nz) * UNIT_COST;
+        };
+        for (int g = lane; g <= NWC; g += 32) {
+            int real = run;
+            if (g < NWC && nz > 0) {
+                const long long v = (long long)g * vtot / NWC;
+                int lo = 0, hi = nz - 1;           // last unit starting at or before v
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (vstart(mid) <= v) lo = mid; else hi = mid - 1;
+                }
+                const long long o = v - vstart(lo);
+                real = o < UNIT_COST ? cum[lo]
+                                     : min(cum[lo + 1], cum[lo] + (int)((o - UNIT_COST) / 4));
+            }
+            if (g == 0) real = 0;
+            bound[g] = real;
+        }
     }
     if (tid < NW) arrive[tid] = 0;
     if (tid == 0) {
@@ -275,9 +390,14 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
 
     // ---- 4. stream this warp's range of the cluster's blocks ------------------
     const int F = cum[nu];
-    auto range_lo = [&](int g) -> int { return (int)((long long)g * F / NWC); };
+    auto range_lo = [&](int g) -> int { return bound[g]; };
     auto owner = [&](int f) -> int {               // warp whose range holds position f
-        return (int)(((long long)(f + 1) * NWC - 1) / F);
+        int lo = 0, hi = NWC - 1;                  // last warp starting at or before f
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (bound[mid] <= f) lo = mid; else hi = mid - 1;
+        }
+        return lo;
     };
     const int my_lo = range_lo(gw), my_hi = range_lo(gw + 1);
     const int n_mine = my_hi - my_lo;
@@ -401,6 +521,27 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         const UnitRec u = units[ui];
         const int u_lo = cum[ui], u_hi = cum[ui] + u.nb;
         const bool from_before = u_lo < my_lo, to_after = u_hi > my_hi;
+        if (!from_before && !to_after) {
+            // a unit only this warp touched: write its result from registers
+            wa.for_each_result([&](int g, int d, float v0, float v1, bool first, float m,
+                                   float l) {
+                if constexpr (PARTIAL) {
+                    const long long row =
+                        ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
+                    *reinterpret_cast<float2 *>(p.part_o + row * D + d) = make_float2(v0, v1);
+                    if (first) {
+                        p.part_m[row] = m * LN2;      // natural units
+                        p.part_l[row] = l;
+                    }
+                } else {
+                    T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d;
+                    store_pair<T>(o, v0, v1);
+                }
+            });
+            __syncwarp();
+            wa.reset();
+            return;
+        }
         float *mine = part_of(gw, (from_before && !to_after) ? 0 : 1);
         // partial layout: O[G][D], M[G], L[G]
         wa.store_partial(mine + G * D, mine + G * D + G, mine);
@@ -457,7 +598,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         wa.reset();
     };
 
-    int cur = -1;
+    int cur = -1, qnext = -1;                      // unit whose query is loaded ahead
     int k_done = 0;
     bool ok = true;
     for (int k = 0; k < n_mine; ++k) {
@@ -472,11 +613,20 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         if (ui != cur) {
             if (cur >= 0) leave_unit(cur);
             cur = ui;
-            const UnitRec &u = units[ui];
-            const T *qp = reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
-                          (long long)u.j * G * D;
-            if constexpr (TC) wa.load_q_global(qp);
-            else wa.load_q_global(qp, p.scale_log2);
+            auto qptr = [&](int q) {
+                const UnitRec &u = units[q];
+                return reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
+                       (long long)u.j * G * D;
+            };
+            if (qnext != ui) wa.prefetch_q(qptr(ui));
+            if constexpr (TC) wa.take_q();
+            else wa.take_q(p.scale_log2);
+            // load the next unit's query while this one streams
+            qnext = -1;
+            if (ui + 1 < nu && cum[ui + 1] < my_hi && units[ui + 1].nb > 0) {
+                qnext = ui + 1;
+                wa.prefetch_q(qptr(qnext));
+            }
         }
         const int st = k % S;
         const bool waited = mbar_wait_bounded(&my_bars[st], (uint32_t)((k / S) & 1), p.err);
@@ -488,6 +638,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             if constexpr (TC) {
                 if (rows < 16) {                   // tail rows hold other tokens' data
                     W::zero_rows(Kt + TILE, rows, lane);
+                    // these generic writes must be ordered before the next
+                    // bulk copy into the stage
+                    fence_proxy_async_smem();
                     __syncwarp();
                 }
                 wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, p.scale_log2);
@@ -495,8 +648,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                 wa.block(Kt, Kt + TILE, rows, Sc, Pb, Al);
             }
         }
-        fence_proxy_async_smem();                  // generic accesses before the next copy
-        __syncwarp();
+        __syncwarp();                              // every lane is done with the stage
         const int kn = k + S;
         if (kn < n_mine) {
             int uin, pbn;
