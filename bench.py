@@ -100,6 +100,25 @@ def recorded_traffic(name: str):
 
 
 # ---------------------------------------------------------------------------
+# ranks: every rank runs its own replica; time = max over ranks
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job units per second: all ranks' units over the slowest rank's time."""
+    return world * units_per_rank * steps / (max_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
 
@@ -158,12 +177,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def make_flush(device):
+    """L2 flush between timed calls: write a buffer of twice the L2 size,
+    then read a second one, so that the lines left behind are clean and the
+    next timed kernel does not pay for write-backs of the flush itself."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     n = max(2 * l2, 256 << 20)
-    buf = torch.empty(n // 4, dtype=torch.int32, device=device)
+    wbuf = torch.empty(n // 4, dtype=torch.int32, device=device)
+    rbuf = torch.ones(n // 4, dtype=torch.int32, device=device)
+    sink = torch.empty((), dtype=torch.int64, device=device)
 
     def flush():
-        buf.fill_(1)
+        wbuf.fill_(1)
+        torch.sum(rbuf, dtype=torch.int64, out=sink)
     return flush, n
 
 
@@ -230,11 +255,7 @@ def gpu_arm(args, rank, world, device):
     step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
     write_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
     dec_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), world, device)
     flags = pa.pa_device_error(clear=True)
 
     dec_mean = statistics.mean(dec_ms)
@@ -246,7 +267,7 @@ def gpu_arm(args, rank, world, device):
 
     result = {
         "metric": METRIC,
-        "value": world * b.num_seqs * args.steps / (total_ms * 1e-3),
+        "value": aggregate_rate(world, b.num_seqs, args.steps, total_ms),
         "unit": "seqs/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -262,7 +283,8 @@ def gpu_arm(args, rank, world, device):
             "global_batch": world * b.num_seqs,
             "tokens_attended": int(b.seq_lens.sum()),
             "num_blocks": b.num_blocks,
-            "l2": f"flushed between steps ({flush_bytes >> 20} MiB write, outside the events)",
+            "l2": f"flushed between steps ({flush_bytes >> 20} MiB write, then "
+                  f"{flush_bytes >> 20} MiB read, outside the events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "decode_kernel": "persistent (LPT-sorted units, per-warp bulk-copy rings)",
         },

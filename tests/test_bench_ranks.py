@@ -1,0 +1,48 @@
+"""Multi-rank arithmetic of bench.py on CPU (gloo, world size 2): each rank
+runs its own replica; the reported time is the slowest rank's and the rate
+counts every rank's sequences.  No GPU is involved."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, times, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    try:
+        dist.barrier()
+        m = bench.max_over_ranks(times[rank], world)
+        v = bench.aggregate_rate(world, 256, 10, m)
+        out[rank] = (m, v)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_rate_gloo():
+    world = 2
+    times = [12.5, 20.0]
+    mgr = mp.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    mp.spawn(_worker, args=(world, port, times, out), nprocs=world, join=True)
+    for r in range(world):
+        m, v = out[r]
+        assert m == pytest.approx(20.0)
+        assert v == pytest.approx(2 * 256 * 10 / 20e-3)
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.aggregate_rate(1, 256, 4, 2.0) == pytest.approx(256 * 4 / 2e-3)
