@@ -188,7 +188,7 @@ def make_flush(device):
 
     def flush():
         wbuf.fill_(1)
-        torch.sum(rbuf, dtype=torch.int64, out=sink)
+        torch.sum(rbuf, dim=0, dtype=torch.int64, out=sink)
     return flush, n
 
 

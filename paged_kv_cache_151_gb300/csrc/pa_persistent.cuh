@@ -134,9 +134,36 @@ __device__ __forceinline__ void bitonic_sort_regs(uint32_t *keys) {
     __syncthreads();
 }
 
-// Ascending sort of keys[0 .. Np) (Np a power of two >= NT, distinct values).
+// Ascending sort of keys[0 .. N) (distinct values) by counting: each key's
+// position is the number of smaller keys.  EPT keys per thread compared
+// against all N (broadcast reads); out receives the sorted keys.
+template <int EPT, int NT>
+__device__ __forceinline__ void rank_sort(const uint32_t *keys, uint32_t *out) {
+    constexpr int N = EPT * NT;
+    const int t = threadIdx.x;
+    uint32_t v[EPT];
+    int rk[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        v[e] = keys[t * EPT + e];
+        rk[e] = 0;
+    }
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+#pragma unroll 4
+    for (int i = 0; i < N / 4; ++i) {
+        const uint4 w = k4[i];
+#pragma unroll
+        for (int e = 0; e < EPT; ++e)
+            rk[e] += (w.x < v[e]) + (w.y < v[e]) + (w.z < v[e]) + (w.w < v[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) out[rk[e]] = v[e];
+    __syncthreads();
+}
+
+// Ascending bitonic sort of keys[0 .. Np) (Np a power of two >= NT).
 template <int NT>
-__device__ void sort_keys(uint32_t *keys, int Np) {
+__device__ void sort_keys_bitonic(uint32_t *keys, int Np) {
     if (Np == NT) { bitonic_sort_regs<1, NT>(keys); return; }
     if (Np == 2 * NT) { bitonic_sort_regs<2, NT>(keys); return; }
     if (Np == 4 * NT) { bitonic_sort_regs<4, NT>(keys); return; }
@@ -155,6 +182,16 @@ __device__ void sort_keys(uint32_t *keys, int Np) {
             __syncthreads();
         }
     }
+}
+
+// Ascending sort of keys[0 .. Np) (Np a power of two >= NT, distinct values);
+// `tmp` has room for Np keys.  Returns the array holding the result.
+template <int NT>
+__device__ uint32_t *sort_keys(uint32_t *keys, uint32_t *tmp, int Np) {
+    if (Np == NT) { rank_sort<1, NT>(keys, tmp); return tmp; }
+    if (Np == 2 * NT) { rank_sort<2, NT>(keys, tmp); return tmp; }
+    sort_keys_bitonic<NT>(keys, Np);
+    return keys;
 }
 
 // Exclusive scan of one int per thread across the block; returns this
@@ -244,6 +281,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     uint32_t *keys = reinterpret_cast<uint32_t *>(stages);           // [Bp]
     int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);   // [B]
     int *lens = start + B;                                           // [B], clamped
+    uint32_t *sort_tmp = reinterpret_cast<uint32_t *>(lens + ((B + 3) & ~3));  // [Bp] if Bp <= 2*NT
     for (int i = tid; i < Bp; i += NT) {
         uint32_t key = 0xffffffffu;
         if (i < B) {
@@ -257,7 +295,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         keys[i] = key;
     }
     __syncthreads();
-    sort_keys<NT>(keys, Bp);
+    keys = sort_keys<NT>(keys, sort_tmp, Bp);
 
     // ---- 2. number the units: exclusive scan of units per sorted sequence -----
     auto units_of = [&](int pos) -> int {          // pos < B
@@ -283,8 +321,10 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     auto rank_of = [&](int q) -> long long {
         return (long long)q * NC + ((q & 1) ? (NC - 1 - me) : me);
     };
-    int nu = 0;
-    while (rank_of(nu) < U) ++nu;
+    // ranks q*NC + (q even ? me : NC-1-me) below U: every full round, and the
+    // partial last round if this cluster's offset falls inside it
+    int nu = U / NC;
+    if (rank_of(nu) < U) ++nu;
     if (nu > NU_MAX) {                             // the host sizes the grid to avoid this
         if (tid == 0) set_error(p.err, ERR_SEQ_LEN);
         nu = NU_MAX;
