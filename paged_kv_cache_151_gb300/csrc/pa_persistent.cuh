@@ -52,18 +52,22 @@ struct UnitRec {
 template <typename T, int D, int G, int NW, int S, bool PARTIAL>
 struct PersistentLayout {
     using Sh = Shape<T, D>;
-    static constexpr int NU_MAX = 160;                    // units per cluster
+    static constexpr int NU_MAX = 128;                    // units per cluster
     static constexpr size_t STAGES = (size_t)NW * S * 2 * Sh::TILE_BYTES;
     // one partial: O[G][D], M[G], L[G], padded to 16 bytes
     static constexpr size_t PART_FLOATS = ((size_t)G * D + 2 * G + 3) / 4 * 4;
     static constexpr size_t OFF_BARS = STAGES;
     static constexpr size_t OFF_SCR = OFF_BARS + (size_t)NW * S * 8;
-    static constexpr size_t OFF_PARTS = OFF_SCR + (size_t)NW * warp_scratch_floats<G>() * 4;
-    static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * 2 * PART_FLOATS * 4;
+    // per-warp score scratch of the CUDA-core path (16-bit caches use none)
+    static constexpr size_t SCR_BYTES = sizeof(T) == 2 ? 0 : (size_t)NW * warp_scratch_floats<G>() * 4;
+    static constexpr size_t OFF_PARTS = OFF_SCR + SCR_BYTES;
+    static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * PART_FLOATS * 4;
     static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
     static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
     static constexpr size_t BYTES = OFF_CTL + 256 + 1024;   // + alignment of the base
     static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
+    static_assert(S == 0 || (size_t)S * 2 * Sh::TILE_BYTES >= PART_FLOATS * 4,
+                  "a warp's stages must hold one partial");
     static_assert(OFF_SCR % 16 == 0 && OFF_PARTS % 16 == 0 && OFF_UNITS % 16 == 0 &&
                       OFF_CTL % 16 == 0 && PART_FLOATS % 4 == 0,
                   "shared-memory regions must stay 16-byte aligned");
@@ -252,7 +256,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     unsigned char *stages = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);
     float *scr = reinterpret_cast<float *>(smem + Lay::OFF_SCR);
-    float *parts = reinterpret_cast<float *>(smem + Lay::OFF_PARTS);   // [NW][2][PF]
+    float *parts = reinterpret_cast<float *>(smem + Lay::OFF_PARTS);   // [NW][PF]
     UnitRec *units = reinterpret_cast<UnitRec *>(smem + Lay::OFF_UNITS);
     int *cum = reinterpret_cast<int *>(smem + Lay::OFF_CUM);
     int *ctl = reinterpret_cast<int *>(smem + Lay::OFF_CTL);
@@ -523,13 +527,16 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     float *Pb = Sc + 16 * G;
     float *Al = Pb + 16 * G;
 
-    // Partial slots of warp g (in block g / NW): slot 0 holds the unit the
-    // warp's range starts inside of (shared with earlier warps, ending in this
-    // range); slot 1 holds the unit that runs past the end of the range, and
-    // before that, one at a time, the units lying wholly inside the range
-    // (the warp merges those itself at once).
+    // Partial slots of warp g (in block g / NW).  Slot 0 holds the unit the
+    // warp's range starts inside of (shared with earlier warps and ending in
+    // this range), written while the warp streams on, so it has its own
+    // space.  Slot 1 holds the unit that runs past the end of the range: the
+    // warp's last unit, written when its ring is idle, so it lives in the
+    // warp's stage buffers.  (Units wholly inside the range are written from
+    // registers.)
     auto part_of = [&](int g, int which) -> float * {
-        return parts + ((size_t)(g % NW) * 2 + which) * PF;
+        return which == 0 ? parts + (size_t)(g % NW) * PF
+                          : reinterpret_cast<float *>(stages + (size_t)(g % NW) * S * 2 * TILE);
     };
 
     // Write the result of unit u from a merged (M, L, O) of chunk (g, d0).
@@ -711,17 +718,25 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     if (C > 1) cluster_sync();
 }
 
-// Stages per warp: about 16 KiB of K+V in flight per warp, at least 2.
-template <typename T, int D>
+// Stages per warp: as many as keep two blocks per SM (<= 113 KiB of shared
+// memory each), up to about PA_STAGE_KB KiB of K+V in flight per warp.
+#ifndef PA_STAGE_KB
+#define PA_STAGE_KB 16
+#endif
+template <typename T, int D, int G, bool PARTIAL>
 __host__ __device__ constexpr int persistent_stages() {
-    constexpr int s = 16384 / (2 * Shape<T, D>::TILE_BYTES);
-    return s < 2 ? 2 : (s > 6 ? 6 : s);
+    int s = PA_STAGE_KB * 1024 / (2 * Shape<T, D>::TILE_BYTES);
+    s = s < 2 ? 2 : (s > 6 ? 6 : s);
+    while (s > 2 && PersistentLayout<T, D, G, 4, 0, PARTIAL>::BYTES +
+                            (size_t)4 * s * (2 * Shape<T, D>::TILE_BYTES + 8) > 113 * 1024)
+        --s;
+    return s;
 }
 
 template <typename T, int D, int G, bool PARTIAL>
 struct PersistentConfig {
     static constexpr int NW = 4;
-    static constexpr int S = persistent_stages<T, D>();
+    static constexpr int S = persistent_stages<T, D, G, PARTIAL>();
     using Lay = PersistentLayout<T, D, G, NW, S, PARTIAL>;
 };
 
