@@ -14,6 +14,9 @@ fp64 numpy arrays.  The arithmetic is documented in ``pa_ref.c``:
 * ``decode`` / ``decode_one`` -- gather through the block table, then
   textbook softmax attention in fp64 (same page, *PagedAttention in one
   paragraph*).
+* ``decode_multi`` -- several new query tokens per sequence, each attending
+  causally to the cache up to its own position (chunked prefill and
+  speculative verification over the paged cache).
 * ``partition_stats`` / ``lse_merge`` -- split-KV partition statistics and
   their log-sum-exp merge.
 * ``kv_bytes_per_token`` / ``bytes_per_block`` / ``blocks_for_tokens`` --
@@ -72,6 +75,9 @@ def bind(path: str):
     lib.pa_ref_decode_one.argtypes = [P, P, i64, i32] + common
     lib.pa_ref_partition_stats.restype = i64
     lib.pa_ref_partition_stats.argtypes = [P, P, P, i64, i32, i32] + common
+    lib.pa_ref_decode_multi.restype = ctypes.c_int
+    lib.pa_ref_decode_multi.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i64,
+                                        i64, i64, f32, i32]
     lib.pa_ref_lse_merge.restype = None
     lib.pa_ref_lse_merge.argtypes = [P, P, P, P, i64, i32]
     return lib
@@ -233,6 +239,28 @@ def decode_one(s, h, q, k_cache, v_cache, block_tables, seq_lens, scale,
     if rc:
         raise ValueError("oracle decode_one: invalid input")
     return out, w[:L]
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale,
+                 num_kv_heads, dtype: str) -> np.ndarray:
+    """fp64 multi-token-query attention: q [T, H_q, D] packed by query_start
+    [B+1]; returns [T, H_q, D]."""
+    qh = _host(q)
+    kc, vc = _host(k_cache), _host(v_cache)
+    bt = _host(block_tables, np.int32)
+    sl = _host(seq_lens, np.int32)
+    qs = _host(query_start, np.int32)
+    T, H, D = qh.shape
+    N, kvh, bs, _ = kc.shape
+    if kvh != num_kv_heads:
+        raise ValueError("num_kv_heads does not match the cache")
+    out = np.zeros((T, H, D), dtype=np.float64)
+    rc = _active().pa_ref_decode_multi(_p(out), _p(qh), _p(kc), _p(vc), _p(bt), _p(sl),
+                                       _p(qs), sl.shape[0], H, kvh, D, bs, N, bt.shape[1],
+                                       H * D, float(scale), REF_DTYPE[dtype])
+    if rc:
+        raise ValueError("oracle decode_multi: invalid input")
+    return out
 
 
 def problem(q, k_cache, v_cache, block_tables, seq_lens, scale, num_kv_heads,

@@ -27,6 +27,14 @@
  *    "vLLM: Architecture, PagedAttention & Internals", *Custom model
  *    registration*).  L_s == 0 gives out = 0.
  *
+ *  - Multi-token queries (the prefill chunk or the k+1 positions a
+ *    speculative step verifies, "vLLM: Architecture, PagedAttention &
+ *    Internals", *Chunked prefill* and *Speculative decoding*, over the same
+ *    paged cache): sequence s has n_s new query tokens, already written to
+ *    the cache, at positions L_s - n_s .. L_s - 1; query token i attends to
+ *    positions 0 .. L_s - n_s + i (causal among the new tokens) with the same
+ *    textbook softmax.
+ *
  *  - Split-KV partition statistics and their log-sum-exp merge: the token
  *    range is cut into fixed partitions; partition p reports
  *        m_p = max z_t,  l_p = sum exp(z_t - m_p),
@@ -316,6 +324,70 @@ int pa_ref_decode_one(double *out, double *weights, int64_t s, int32_t h,
         return -1;
     if (s < 0 || s >= num_seqs || h < 0 || h >= num_heads) return -1;
     return decode_one(&a, s, h, out, weights);
+}
+
+/* ---- multi-token queries ------------------------------------------------- */
+
+/* out[T][H_q][D] (fp64) for q[T][H_q][D] (token stride q_tok_stride, head
+ * stride D); query_start[B+1] gives each sequence's tokens.  Query token i of
+ * sequence s sees the first L_s - n_s + i + 1 tokens of the sequence.
+ * Returns 0, or -1 on bad input. */
+int pa_ref_decode_multi(double *out, const void *q, const void *k_cache,
+                        const void *v_cache, const int32_t *block_tables,
+                        const int32_t *seq_lens, const int32_t *query_start,
+                        int64_t num_seqs, int32_t num_heads,
+                        int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t num_blocks,
+                        int64_t max_blocks, int64_t q_tok_stride, float scale,
+                        int32_t dtype) {
+    ref_args a;
+    if (make_args(&a, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks, q_tok_stride, head_dim, scale, dtype))
+        return -1;
+    const int64_t D = head_dim;
+    const int32_t G = num_heads / num_kv_heads;
+    int rc = 0;
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        int64_t L;
+        if (check_len(&a, s, &L)) return -1;
+        const int64_t t0 = query_start[s], n = query_start[s + 1] - query_start[s];
+        if (n < 0 || n > L) return -1;
+        double *K = malloc(sizeof(double) * (L > 0 ? L : 1) * D);
+        double *V = malloc(sizeof(double) * (L > 0 ? L : 1) * D);
+        double *z = malloc(sizeof(double) * (L > 0 ? L : 1));
+        if (!K || !V || !z) { free(K); free(V); free(z); return -1; }
+        for (int32_t j = 0; j < num_kv_heads && rc == 0; ++j) {
+            if (L > 0 && gather_kv(&a, s, j, L, K, V)) { rc = -1; break; }
+            for (int32_t g = 0; g < G; ++g) {
+                const int32_t h = j * G + g;
+                for (int64_t i = 0; i < n; ++i) {
+                    const int64_t tok = t0 + i;
+                    const int64_t seen = L - n + i + 1;     /* causal prefix */
+                    double *o = out + (tok * num_heads + h) * D;
+                    const int64_t qoff = tok * q_tok_stride + (int64_t)h * D;
+                    for (int64_t t = 0; t < seen; ++t) {
+                        double acc = 0.0;
+                        for (int64_t d = 0; d < D; ++d)
+                            acc += load_elem(q, qoff + d, dtype) * K[t * D + d];
+                        z[t] = a.scale * acc;
+                    }
+                    double M = -INFINITY;
+                    for (int64_t t = 0; t < seen; ++t) M = z[t] > M ? z[t] : M;
+                    double S = 0.0;
+                    for (int64_t t = 0; t < seen; ++t) { z[t] = exp(z[t] - M); S += z[t]; }
+                    for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+                    for (int64_t t = 0; t < seen; ++t) {
+                        const double w = z[t] / S;
+                        for (int64_t d = 0; d < D; ++d) o[d] += w * V[t * D + d];
+                    }
+                }
+            }
+        }
+        free(K); free(V); free(z);
+        if (rc) return rc;
+    }
+    return 0;
 }
 
 /* ---- split-KV partitions ------------------------------------------------- */

@@ -408,6 +408,48 @@ def random_batch(seed: int, *, num_seqs: int, max_len: int, num_heads: int,
                        new_in_pool=new_in_pool)
 
 
+def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
+                      n_new, num_heads: int, num_kv_heads: int, head_dim: int,
+                      dtype: str, device="cpu", canary=True, keep_seq=True,
+                      kv_std: float = 1.0, lens=None) -> PagedBatch:
+    """Several new query tokens per sequence (a prefill chunk, or the k+1
+    positions of a speculative step), already written to the cache.
+
+    Sequence s holds ``seq_lens[s] = ctx + n_s`` tokens in the pool; its n_s
+    query tokens (positions seq_len - n_s .. seq_len - 1) are rows
+    ``query_start[s] .. query_start[s+1]`` of ``q`` ([T, H, D]), kept in
+    ``meta["query_start"]``.  ``n_new`` is an int or an inclusive (lo, hi)
+    range; ``lens`` optionally fixes the context lengths."""
+    rng = np.random.default_rng(seed)
+    if lens is None:
+        ctx = rng.integers(min_ctx, max_ctx, size=num_seqs, endpoint=True)
+    else:
+        ctx = np.asarray(lens, dtype=np.int64)
+    if isinstance(n_new, int):
+        n = np.full(num_seqs, n_new, dtype=np.int64)
+    else:
+        n = rng.integers(n_new[0], n_new[1], size=num_seqs, endpoint=True)
+    total = ctx + n
+    need = sum(math.ceil(int(L) / BLOCK_SIZE) for L in total)
+    fl = FreeList(need + 8, rng)
+    tables = [fl.allocate(int(L)) for L in total]
+    b = build_batch(f"multi{seed}", ctx_lens=np.maximum(total - 1, 0), num_heads=num_heads,
+                    num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype,
+                    num_blocks=need + 8, tables=tables, seed=seed, device=device,
+                    canary=canary, keep_seq=keep_seq, kv_std=kv_std, new_in_pool=True)
+    qs = np.zeros(num_seqs + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(n)
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(int(seed) + 7919)
+    T = int(qs[-1])
+    q = torch.randn((T, num_heads, head_dim), generator=gen,
+                    device=torch.device(device)).to(DTYPES[dtype])
+    b = replace(b, q=q, seq_lens=total.astype(np.int32), name=f"multi{seed}")
+    b.meta["query_start"] = qs
+    b.meta["n_new"] = n.astype(np.int32)
+    return b
+
+
 # ---------------------------------------------------------------------------
 # Layout transforms used by the invariance tests
 # ---------------------------------------------------------------------------

@@ -275,6 +275,81 @@ def test_table_padding_is_never_read():
 
 
 # ---------------------------------------------------------------------------
+# multi-token queries
+# ---------------------------------------------------------------------------
+
+def oracle_multi(b):
+    return oracle.decode_multi(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens,
+                               b.meta["query_start"], b.scale, b.num_kv_heads, b.dtype)
+
+
+def test_multi_with_one_token_is_decode():
+    b = wl.multi_query_batch(41, num_seqs=5, min_ctx=0, max_ctx=80, n_new=1, num_heads=8,
+                             num_kv_heads=2, head_dim=64, dtype="bf16")
+    out = oracle_multi(b)
+    ref = oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
+                        b.num_kv_heads, "bf16")
+    assert np.array_equal(out, ref)
+
+
+def test_multi_token_i_is_decode_of_its_causal_prefix():
+    b = wl.multi_query_batch(42, num_seqs=4, min_ctx=0, max_ctx=60, n_new=(1, 6),
+                             num_heads=8, num_kv_heads=2, head_dim=64, dtype="f32")
+    out = oracle_multi(b)
+    qs, n = b.meta["query_start"], b.meta["n_new"]
+    for s in range(b.num_seqs):
+        for i in range(int(n[s])):
+            tok = int(qs[s]) + i
+            sl = b.seq_lens.copy()
+            sl[s] = b.seq_lens[s] - n[s] + i + 1
+            qb = torch.zeros((b.num_seqs, b.num_heads, b.head_dim))
+            qb[s] = b.q[tok]
+            ref = oracle.decode(qb, b.k_cache, b.v_cache, b.block_tables, sl, b.scale,
+                                b.num_kv_heads, "f32")
+            assert np.array_equal(out[tok], ref[s])
+
+
+@pytest.mark.parametrize("dtype,H,Hkv,D", [("bf16", 32, 8, 128), ("f32", 8, 8, 64),
+                                            ("f16", 16, 2, 64)])
+def test_multi_matches_masked_sdpa(dtype, H, Hkv, D):
+    b = wl.multi_query_batch(43, num_seqs=4, min_ctx=0, max_ctx=70, n_new=(1, 9),
+                             num_heads=H, num_kv_heads=Hkv, head_dim=D, dtype=dtype)
+    out = oracle_multi(b)
+    qs, n = b.meta["query_start"], b.meta["n_new"]
+    for s in range(b.num_seqs):
+        L, ns = int(b.seq_lens[s]), int(n[s])
+        q = b.q[int(qs[s]):int(qs[s]) + ns].double().permute(1, 0, 2)[None]  # [1,H,n,D]
+        k = b.seq_k[s].double().permute(1, 0, 2)[None]                        # [1,Hkv,L,D]
+        v = b.seq_v[s].double().permute(1, 0, 2)[None]
+        pos_q = torch.arange(L - ns, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos_q                              # [n, L]
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask,
+                                             scale=float(np.float32(b.scale)),
+                                             enable_gqa=True)[0].permute(1, 0, 2)
+        np.testing.assert_allclose(out[int(qs[s]):int(qs[s]) + ns], ref.numpy(),
+                                   rtol=0, atol=1e-12)
+
+
+def test_multi_whole_sequence_new_is_causal_prefill():
+    """All tokens new (a first prefill chunk): plain causal attention."""
+    b = wl.multi_query_batch(44, num_seqs=2, min_ctx=0, max_ctx=0, n_new=(5, 20),
+                             num_heads=4, num_kv_heads=2, head_dim=64, dtype="f32",
+                             lens=[0, 0])
+    out = oracle_multi(b)
+    qs = b.meta["query_start"]
+    for s in range(2):
+        L = int(b.seq_lens[s])
+        q = b.q[int(qs[s]):int(qs[s]) + L].double().permute(1, 0, 2)[None]
+        k = b.seq_k[s].double().permute(1, 0, 2)[None]
+        v = b.seq_v[s].double().permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(q, k, v, is_causal=True,
+                                             scale=float(np.float32(b.scale)),
+                                             enable_gqa=True)[0].permute(1, 0, 2)
+        np.testing.assert_allclose(out[int(qs[s]):int(qs[s]) + L], ref.numpy(), rtol=0,
+                                   atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # split-KV partitions
 # ---------------------------------------------------------------------------
 
@@ -363,6 +438,8 @@ MUTATIONS = {
     "merge_sign": ("double c = l[p] * exp(m[p] - M);", "double c = l[p] * exp(M - m[p]);"),
     "table_row_stride": ("int64_t pb = a->block_tables[s * a->max_blocks + lb];",
                          "int64_t pb = a->block_tables[s + lb * a->num_seqs];"),
+    "multi_causal_offset": ("const int64_t seen = L - n + i + 1;     /* causal prefix */",
+                            "const int64_t seen = L - n + i;     /* causal prefix */"),
 }
 
 
@@ -385,6 +462,24 @@ def _pins_hold() -> bool:
                                          b.num_kv_heads, "f32")
         if not np.allclose(oracle.lse_merge(m, l, o), out[1, 3], rtol=0, atol=1e-9):
             return False
+        mb = wl.multi_query_batch(32, num_seqs=3, min_ctx=0, max_ctx=40, n_new=(2, 5),
+                                  num_heads=4, num_kv_heads=2, head_dim=64, dtype="f32")
+        mo = oracle.decode_multi(mb.q, mb.k_cache, mb.v_cache, mb.block_tables,
+                                 mb.seq_lens, mb.meta["query_start"], mb.scale,
+                                 mb.num_kv_heads, "f32")
+        qs, n = mb.meta["query_start"], mb.meta["n_new"]
+        for s in range(mb.num_seqs):
+            L, ns = int(mb.seq_lens[s]), int(n[s])
+            q = mb.q[int(qs[s]):int(qs[s]) + ns].double().permute(1, 0, 2)[None]
+            k = mb.seq_k[s].double().permute(1, 0, 2)[None]
+            v = mb.seq_v[s].double().permute(1, 0, 2)[None]
+            mask = torch.arange(L)[None, :] <= torch.arange(L - ns, L)[:, None]
+            ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask,
+                                                 scale=float(np.float32(mb.scale)),
+                                                 enable_gqa=True)[0].permute(1, 0, 2)
+            if not np.allclose(mo[int(qs[s]):int(qs[s]) + ns], ref.numpy(), rtol=0,
+                               atol=1e-9):
+                return False
     except ValueError:
         return False
     return True
