@@ -58,6 +58,22 @@ def decode_bytes(b) -> dict:
     return {"kv": kv, "kv_full_blocks": kv_full, "total": kv + qo + tab}
 
 
+def multi_bytes(b) -> dict:
+    """Multi-token queries: every cached token's K and V read at least once,
+    q and out once; flops of QK^T and PV over the causal positions."""
+    es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
+    L = b.seq_lens.astype(np.int64)
+    n = np.diff(b.meta["query_start"]).astype(np.int64)
+    kv = int(L.sum()) * 2 * b.num_kv_heads * b.head_dim * es
+    T = int(n.sum())
+    qo = 2 * T * b.num_heads * b.head_dim * es
+    # row i of a sequence with n rows sees L - n + i + 1 positions
+    seen = int(sum(int(n_s) * (int(L_s) - int(n_s)) + int(n_s) * (int(n_s) + 1) // 2
+                   for L_s, n_s in zip(L, n)))
+    flops = 4 * seen * b.num_heads * b.head_dim
+    return {"kv": kv, "total": kv + qo, "rows": T, "flops": flops}
+
+
 def cache_write_bytes(b) -> int:
     es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
     rows = b.num_seqs * b.num_kv_heads * b.head_dim * es
@@ -314,6 +330,7 @@ def gpu_arm(args, rank, world, device):
     if not args.no_extras and world == 1:
         result["long_context"] = long_context_arm(args, device, flush, pa)
         result["paging_overhead"] = paging_overhead_arm(args, device, flush, pa)
+        result["multi_query"] = multi_query_arm(args, device, flush, pa)
     return result, b
 
 
@@ -380,6 +397,38 @@ def long_context_arm(args, device, flush, pa):
             "seqs_per_s": 8 / t, "us_per_call": t * 1e6, "kv_gbs": nb["kv"] / t / 1e9,
             "achieved_gbs": nb["total"] / t / 1e9, "frac_of_peak": nb["total"] / t / 1e9 / peak,
             "peak_kind": kind, "bytes": nb}
+
+
+def multi_query_arm(args, device, flush, pa):
+    """pa_decode_multi on a speculative-verification step (256 seqs x 4 query
+    rows, serving-mix lengths) and a chunked-prefill step (4 x 512-token
+    chunks beside 124 one-token decodes)."""
+    peak, kind = measured_peak()
+    res = {}
+    for name, make in (("spec_verify", wl.spec_verify), ("chunked_prefill", wl.chunked_prefill_mix)):
+        b = make(device=device, canary=False)
+        bt, sl, _ = b.torch_tables(device)
+        qs = torch.from_numpy(b.meta["query_start"]).to(device)
+        mq = int(np.diff(b.meta["query_start"]).max())
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode_multi(out, b.q, b.k_cache, b.v_cache, bt, sl, qs, mq, b.scale,
+                               b.num_kv_heads)
+        for _ in range(3):
+            call()
+        ms = time_calls(call, 20, flush, torch.cuda.current_stream())
+        t = statistics.mean(ms) * 1e-3
+        nb = multi_bytes(b)
+        res[name] = {"workload": make.__doc__.split("\n\n")[0].replace("\n", " "),
+                     "us_per_call": t * 1e6, "rows_per_s": nb["rows"] / t,
+                     "kv_gbs": nb["kv"] / t / 1e9,
+                     "achieved_gbs": nb["total"] / t / 1e9,
+                     "frac_of_peak": nb["total"] / t / 1e9 / peak, "peak_kind": kind,
+                     "attn_tflops": nb["flops"] / t / 1e12, "bytes": nb}
+        del b, out
+        torch.cuda.empty_cache()
+    return res
 
 
 def paging_overhead_arm(args, device, flush, pa):
@@ -536,6 +585,17 @@ def single_kernel(args, device):
         def call():
             pa.pa_decode_partitioned(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale,
                                      b.num_kv_heads, 512, msl, ws)
+    elif args.only in ("multi_spec", "multi_prefill"):
+        b = (wl.spec_verify if args.only == "multi_spec" else wl.chunked_prefill_mix)(
+            device=device, canary=False)
+        bt, sl, _ = b.torch_tables(device)
+        qs = torch.from_numpy(b.meta["query_start"]).to(device)
+        mq = int(np.diff(b.meta["query_start"]).max())
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode_multi(out, b.q, b.k_cache, b.v_cache, bt, sl, qs, mq, b.scale,
+                               b.num_kv_heads)
     else:
         b = wl.serving_mix(device=device, canary=False)
         bt, sl, sm = b.torch_tables(device)
@@ -551,7 +611,7 @@ def single_kernel(args, device):
         call()
     torch.cuda.synchronize()
     ms = time_calls(call, args.steps, flush, torch.cuda.current_stream())
-    nb = decode_bytes(b)
+    nb = multi_bytes(b) if args.only.startswith("multi") else decode_bytes(b)
     print(json.dumps({"only": args.only, "workload": b.name, "us": [m * 1e3 for m in ms],
                       "bytes": nb, "device_error_flags": pa.pa_device_error(clear=True)}))
 
@@ -570,9 +630,10 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="approximate seconds of oracle work for the reference arm")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the long-context and paging-overhead measurements")
+                    help="skip the long-context, paging-overhead and multi-query measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["decode", "partitioned", "cache_write"],
+    ap.add_argument("--only", choices=["decode", "partitioned", "cache_write", "multi_spec",
+                                       "multi_prefill"],
                     help="launch one kernel alone (for profiling); prints timings only")
     args = ap.parse_args()
     if args.warmup < 3:

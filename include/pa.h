@@ -11,6 +11,9 @@
  *   pa_decode_partitioned  the same attention split into fixed token
  *                          partitions whose results are merged by
  *                          log-sum-exp (for long contexts)
+ *   pa_decode_multi        several new query tokens per sequence (a
+ *                          prompt chunk or speculative positions), causal
+ *                          among themselves, over the same paged cache
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -86,7 +89,8 @@ typedef enum {
 /* bits of the device error word */
 #define PA_DEVERR_BLOCK_ID   0x1u  /* a block-table entry outside [0, num_blocks) was skipped */
 #define PA_DEVERR_SEQ_LEN    0x2u  /* a seq_len < 0 or > max_blocks_per_seq*block_size (or past
-                                      max_seq_len in the partitioned call) was clamped */
+                                      max_seq_len in the partitioned call) was clamped, or
+                                      a query row range of pa_decode_multi was invalid */
 #define PA_DEVERR_SLOT       0x4u  /* a slot >= num_blocks*block_size was skipped */
 #define PA_DEVERR_TIMEOUT    0x8u  /* a wait on an asynchronous copy exceeded its limit */
 
@@ -204,6 +208,49 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
                           void *stream);
 
 /*
+ * pa_decode_multi -- paged attention for several new query tokens per
+ * sequence: a chunk of a long prompt (chunked prefill) or the k+1 positions
+ * a target model verifies in one pass of speculative decoding.
+ *
+ * Defined in "vLLM: Architecture, PagedAttention & Internals", *Prefill,
+ * decode, and chunked prefill* (one forward pass mixes a slice of a prompt's
+ * tokens with one-token decodes, each attending over its sequence's cache)
+ * and *Speculative decoding* (the target model scores the k drafted tokens
+ * and the one after them in a single pass).  The new tokens' keys and values
+ * are in the cache already (pa_reshape_and_cache of the same step), and new
+ * token i of a sequence sees the cache up to and including itself.
+ *
+ * Sequence s owns query rows r = query_start[s] .. query_start[s+1]-1
+ * (n_s = query_start[s+1] - query_start[s] of them, 0 <= n_s <= seq_lens[s]);
+ * row r = query_start[s] + i is the token at position seq_lens[s] - n_s + i.
+ * For every such row and query head h:
+ *     out[r][h] = sum_t softmax_t(scale * q[r][h] . K_s[t]) * V_s[t],
+ *     t = 0 .. seq_lens[s] - n_s + i,
+ * with K_s, V_s and the GQA mapping as in pa_decode.  A sequence with n_s = 0
+ * (a request that runs no token this step) has no rows.
+ *
+ * Layouts: q is [num_q_rows][num_heads][head_dim] with row stride
+ * q_row_stride (>= num_heads*head_dim, a multiple of 8 elements); out is
+ * [num_q_rows][num_heads][head_dim], contiguous; query_start is int32
+ * [num_seqs + 1], non-decreasing, query_start[num_seqs] <= num_q_rows.
+ *
+ * Requirements: as pa_decode, and dtype PA_BF16 or PA_F16 (PA_F32 gives
+ * PA_ERR_UNSUPPORTED); max_query_len >= every n_s (it sizes the launch);
+ * q, out 16-byte aligned.  A sequence whose row range is out of bounds,
+ * decreasing, longer than max_query_len or longer than seq_lens[s] sets
+ * PA_DEVERR_SEQ_LEN and its rows are not written.  num_seqs == 0 or
+ * num_q_rows == 0 launches nothing.
+ */
+int pa_decode_multi(void *out, const void *q, const void *k_cache,
+                    const void *v_cache, const int32_t *block_tables,
+                    const int32_t *seq_lens, const int32_t *query_start,
+                    int32_t num_seqs, int32_t num_q_rows, int32_t max_query_len,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int64_t num_blocks, int32_t block_size,
+                    int32_t max_blocks_per_seq, int64_t q_row_stride,
+                    float scale, int32_t dtype, void *stream);
+
+/*
  * pa_decode_partitioned_noalloc -- pa_decode_partitioned without a caller
  * workspace, for callers that cannot allocate device memory where they
  * decode (for example while another stream is being captured into a CUDA
@@ -249,7 +296,7 @@ const char *pa_status_string(int status);
  */
 int pa_device_error(uint32_t *flags, int clear);
 
-/* ABI version of this header (increments on any signature change). */
+/* ABI version of this header (increments on any signature change or addition). */
 int pa_abi_version(void);
 
 #ifdef __cplusplus

@@ -227,7 +227,7 @@ bool workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
 
 extern "C" {
 
-int pa_abi_version(void) { return 1; }
+int pa_abi_version(void) { return 2; }
 
 const char *pa_status_string(int status) {
     switch (status) {
@@ -356,6 +356,49 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
     const int64_t cap = (int64_t)max_blocks_per_seq * 16;
     mp.seq_cap = (int)(max_seq_len < cap ? max_seq_len : cap);
     e = run_merge(mp, dtype, num_seqs, st);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *seq_lens,
+                    const int32_t *query_start, int32_t num_seqs, int32_t num_q_rows,
+                    int32_t max_query_len, int32_t num_heads, int32_t num_kv_heads,
+                    int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                    int32_t max_blocks_per_seq, int64_t q_row_stride, float scale,
+                    int32_t dtype, void *stream) {
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_row_stride, scale, dtype);
+    if (rc != PA_OK) return rc;
+    if (num_q_rows < 0 || max_query_len < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_q_rows == 0) return PA_OK;
+    if (!query_start) return PA_ERR_INVALID_ARG;
+    if (dtype == PA_F32) return PA_ERR_UNSUPPORTED;
+    if (!q_rows_aligned(q, q_row_stride, dtype) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    // work units: (sequence, KV head, 16-row tile of the sequence's rows x G heads)
+    const int64_t rows = (int64_t)(max_query_len < num_q_rows ? max_query_len : num_q_rows) * G;
+    const int64_t tiles = (rows + 15) / 16;
+    if (tiles == 0) return PA_OK;
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.block_tables = block_tables; p.seq_lens = seq_lens;
+    p.query_start = query_start;
+    p.max_query_len = max_query_len;
+    p.num_q_rows = num_q_rows;
+    p.num_blocks = num_blocks; p.q_seq_stride = q_row_stride;
+    p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_log2 = scale * pa::LOG2E;
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    if (!prepare_maps(p, dtype, head_dim)) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long unit_bound = (long long)num_seqs * num_kv_heads * tiles;
+    cudaError_t e = dtype == PA_BF16
+                        ? pa::decode_multi_bf16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st)
+                        : pa::decode_multi_f16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st);
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -66,6 +66,9 @@ struct DecodeParams {
     int partition_blocks;     // PARTIAL: 16-token blocks per partition
     int max_parts;            // PARTIAL: partitions the workspace holds
     int max_seq_len;          // PARTIAL: bound on seq_len
+    const int32_t *query_start;  // multi-token queries: [num_seqs + 1] row offsets
+    int max_query_len;        // multi-token queries: bound on a sequence's rows
+    int num_q_rows;           // multi-token queries: rows of q and out
     float scale_log2;         // scale * log2(e)
     unsigned int *err;        // device error word
     // 16-bit caches, persistent kernel: the caches as 3-D tensors

@@ -26,6 +26,11 @@ cudaError_t decode_persistent_bf16(const DecodeParams &p, int D, int G, bool par
                                    long long unit_bound, int cluster, cudaStream_t st);
 cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
                                   long long unit_bound, int cluster, cudaStream_t st);
+// multi-token queries (16-bit storage only)
+cudaError_t decode_multi_bf16(const DecodeParams &p, int D, int G, long long unit_bound,
+                              int cluster, cudaStream_t st);
+cudaError_t decode_multi_f16(const DecodeParams &p, int D, int G, long long unit_bound,
+                             int cluster, cudaStream_t st);
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

@@ -51,6 +51,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 template <typename T> struct Mma;
 
 template <> struct Mma<__nv_bfloat16> {
+    // d = a . b + d with all 16 rows of a
+    __device__ __forceinline__ static void run4(float *d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
     // d = a . b + d, a: rows 0-7 only (a1 = a3 = 0)
     __device__ __forceinline__ static void run(float *d, uint32_t a0, uint32_t a2, uint32_t b0,
                                                uint32_t b1) {
@@ -71,6 +80,14 @@ template <> struct Mma<__nv_bfloat16> {
 };
 
 template <> struct Mma<__half> {
+    __device__ __forceinline__ static void run4(float *d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
     __device__ __forceinline__ static void run(float *d, uint32_t a0, uint32_t a2, uint32_t b0,
                                                uint32_t b1) {
         asm volatile(
@@ -240,6 +257,153 @@ struct WarpAttnTC {
 #pragma unroll
         for (int j = 0; j < NT; ++j)
             *reinterpret_cast<float2 *>(Aw + g * D + 8 * j + 2 * t) = make_float2(acc[j][0], acc[j][1]);
+    }
+};
+
+// Sixteen query rows at once: the (query token, head) pairs of a multi-token
+// query (a prefill chunk or the k+1 positions of a speculative step) that
+// share one KV head.  Lane (g, t) holds rows g ("lo") and g + 8 ("hi"); each
+// row has its own causal limit, the last position it may see.  The layout
+// of scores, probabilities and accumulators is that of WarpAttnTC with the
+// upper eight rows in use.
+template <typename T, int D>
+struct WarpAttnTC16 {
+    static_assert(sizeof(T) == 2, "tensor-core path is for 16-bit caches");
+    static constexpr int KS = D / 16;
+    static constexpr int NT = D / 8;
+
+    int lane, g, t;
+    int lim_lo, lim_hi;                    // last visible position per row (-1: no row)
+    uint32_t qa[KS][4];                    // A fragments (lo k-lo, hi k-lo, lo k-hi, hi k-hi)
+    float acc[NT][4];                      // [0],[1]: row lo; [2],[3]: row hi
+    float m_lo, m_hi, l_lo, l_hi;
+
+    __device__ __forceinline__ void init(int lane_) {
+        lane = lane_;
+        g = lane >> 2;
+        t = lane & 3;
+        lim_lo = lim_hi = -1;
+        reset();
+    }
+
+    __device__ __forceinline__ void reset() {
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    }
+
+    // query rows (nullptr: no such row) and their causal limits
+    __device__ __forceinline__ void load_q(const T *q_lo, const T *q_hi, int lo_lim, int hi_lim) {
+        lim_lo = q_lo ? lo_lim : -1;
+        lim_hi = q_hi ? hi_lim : -1;
+        const uint32_t *wl = reinterpret_cast<const uint32_t *>(q_lo);
+        const uint32_t *wh = reinterpret_cast<const uint32_t *>(q_hi);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qa[ks][0] = q_lo ? __ldg(wl + 8 * ks + t) : 0u;
+            qa[ks][1] = q_hi ? __ldg(wh + 8 * ks + t) : 0u;
+            qa[ks][2] = q_lo ? __ldg(wl + 8 * ks + t + 4) : 0u;
+            qa[ks][3] = q_hi ? __ldg(wh + 8 * ks + t + 4) : 0u;
+        }
+    }
+
+    // One block whose row 0 is at sequence position pos0.
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int pos0, float scale_log2) {
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int rr = lane & 7, mi = lane >> 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int tok = (mi >> 1) * 8 + rr, chunk = 2 * ks + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            Mma<T>::run4(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            Mma<T>::run4(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+        // s0: (lo, 2t) (lo, 2t+1) (hi, 2t) (hi, 2t+1); s1: the same at 8 + 2t
+        const int p0 = pos0 + 2 * t, p1 = p0 + 1, p2 = p0 + 8, p3 = p0 + 9;
+        float lo[4] = {p0 <= lim_lo ? s0[0] * scale_log2 : -INFINITY,
+                       p1 <= lim_lo ? s0[1] * scale_log2 : -INFINITY,
+                       p2 <= lim_lo ? s1[0] * scale_log2 : -INFINITY,
+                       p3 <= lim_lo ? s1[1] * scale_log2 : -INFINITY};
+        float hi[4] = {p0 <= lim_hi ? s0[2] * scale_log2 : -INFINITY,
+                       p1 <= lim_hi ? s0[3] * scale_log2 : -INFINITY,
+                       p2 <= lim_hi ? s1[2] * scale_log2 : -INFINITY,
+                       p3 <= lim_hi ? s1[3] * scale_log2 : -INFINITY};
+        float mxl = fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3]));
+        float mxh = fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3]));
+        mxl = fmaxf(mxl, __shfl_xor_sync(0xffffffffu, mxl, 1));
+        mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 1));
+        mxl = fmaxf(mxl, __shfl_xor_sync(0xffffffffu, mxl, 2));
+        mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 2));
+        // a row may see nothing yet (all -inf): keep its state at zero weight
+        const float nl = fmaxf(m_lo, mxl), nh = fmaxf(m_hi, mxh);
+        const float sl = nl == -INFINITY ? 0.f : nl, sh = nh == -INFINITY ? 0.f : nh;
+        const float al = ex2(m_lo - sl), ah = ex2(m_hi - sh);
+        const uint32_t pa0 = Mma<T>::pack(ex2(lo[0] - sl), ex2(lo[1] - sl));
+        const uint32_t pa2 = Mma<T>::pack(ex2(lo[2] - sl), ex2(lo[3] - sl));
+        const uint32_t pa1 = Mma<T>::pack(ex2(hi[0] - sh), ex2(hi[1] - sh));
+        const uint32_t pa3 = Mma<T>::pack(ex2(hi[2] - sh), ex2(hi[3] - sh));
+        float x0, x1, x2, x3;
+        Mma<T>::unpack(pa0, x0, x1);
+        Mma<T>::unpack(pa2, x2, x3);
+        l_lo = l_lo * al + ((x0 + x1) + (x2 + x3));
+        Mma<T>::unpack(pa1, x0, x1);
+        Mma<T>::unpack(pa3, x2, x3);
+        l_hi = l_hi * ah + ((x0 + x1) + (x2 + x3));
+        m_lo = nl;
+        m_hi = nh;
+        if (__any_sync(0xffffffffu, al != 1.f || ah != 1.f)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                acc[j][0] *= al;
+                acc[j][1] *= al;
+                acc[j][2] *= ah;
+                acc[j][3] *= ah;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+            const int tok = (mi & 1) * 8 + rr, chunk = j + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            Mma<T>::run4(acc[j], pa0, pa1, pa2, pa3, b0, b1);
+            Mma<T>::run4(acc[j + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+    }
+
+    __device__ __forceinline__ void finish() {
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    }
+
+    // merge slot: Mw[16], Lw[16], Aw[16][D]
+    __device__ __forceinline__ void store_partial(float *Mw, float *Lw, float *Aw) const {
+        if (t == 0) {
+            Mw[g] = m_lo; Lw[g] = l_lo;
+            Mw[g + 8] = m_hi; Lw[g + 8] = l_hi;
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            *reinterpret_cast<float2 *>(Aw + g * D + 8 * j + 2 * t) = make_float2(acc[j][0], acc[j][1]);
+            *reinterpret_cast<float2 *>(Aw + (g + 8) * D + 8 * j + 2 * t) =
+                make_float2(acc[j][2], acc[j][3]);
+        }
+    }
+
+    // f(row, d, v0, v1, first, m, l) for the rows that exist
+    template <typename Fn>
+    __device__ __forceinline__ void for_each_result(Fn &&f) const {
+        const float il = l_lo > 0.f ? 1.f / l_lo : 0.f, ih = l_hi > 0.f ? 1.f / l_hi : 0.f;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            if (lim_lo >= 0) f(g, 8 * j + 2 * t, acc[j][0] * il, acc[j][1] * il, t == 0 && j == 0, m_lo, l_lo);
+            if (lim_hi >= 0) f(g + 8, 8 * j + 2 * t, acc[j][2] * ih, acc[j][3] * ih, t == 0 && j == 0, m_hi, l_hi);
+        }
     }
 };
 

@@ -7,7 +7,8 @@ namespace pa {
 
 cudaError_t decode_persistent_f16(const DecodeParams &p, int D, int G, bool partial,
                                 long long unit_bound, int cluster, cudaStream_t st) {
-    return dispatch_persistent<__half>(p, D, G, partial, unit_bound, cluster, st);
+    return partial ? dispatch_persistent<__half, MODE_PARTITIONED>(p, D, G, unit_bound, cluster, st)
+                   : dispatch_persistent<__half, MODE_DECODE>(p, D, G, unit_bound, cluster, st);
 }
 
 }  // namespace pa

@@ -7,7 +7,8 @@ namespace pa {
 
 cudaError_t decode_persistent_f32(const DecodeParams &p, int D, int G, bool partial,
                                 long long unit_bound, int cluster, cudaStream_t st) {
-    return dispatch_persistent<float>(p, D, G, partial, unit_bound, cluster, st);
+    return partial ? dispatch_persistent<float, MODE_PARTITIONED>(p, D, G, unit_bound, cluster, st)
+                   : dispatch_persistent<float, MODE_DECODE>(p, D, G, unit_bound, cluster, st);
 }
 
 }  // namespace pa

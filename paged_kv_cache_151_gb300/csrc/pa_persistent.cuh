@@ -45,17 +45,28 @@
 
 namespace pa {
 
+// What a launch computes: whole-sequence decode (one query token per
+// sequence), split-KV partitions, or several query tokens per sequence.
+enum Mode : int { MODE_DECODE = 0, MODE_PARTITIONED = 1, MODE_MULTI = 2 };
+
+// Rows of one unit's query tile: the G heads of one token, or for multi-token
+// queries 16 (token, head) pairs.
+__host__ __device__ constexpr int rows_of_mode(int mode, int G) { return mode == MODE_MULTI ? 16 : G; }
+
 struct UnitRec {
-    int s, j, lb0, nb, L, part;
+    int s, j, lb0, nb, L, part;   // part: partition (partitioned) or row tile (multi)
+    int q0, nq;                   // multi: first query row of the sequence, its count
 };
 
-template <typename T, int D, int G, int NW, int S, bool PARTIAL>
+template <typename T, int D, int G, int NW, int S, int MODE>
 struct PersistentLayout {
+    static constexpr bool PARTIAL = MODE == MODE_PARTITIONED;
+    static constexpr int ROWS = rows_of_mode(MODE, G);
     using Sh = Shape<T, D>;
     static constexpr int NU_MAX = 128;                    // units per cluster
     static constexpr size_t STAGES = (size_t)NW * S * 2 * Sh::TILE_BYTES;
-    // one partial: O[G][D], M[G], L[G], padded to 16 bytes
-    static constexpr size_t PART_FLOATS = ((size_t)G * D + 2 * G + 3) / 4 * 4;
+    // one partial: O[ROWS][D], M[ROWS], L[ROWS], padded to 16 bytes
+    static constexpr size_t PART_FLOATS = ((size_t)ROWS * D + 2 * ROWS + 3) / 4 * 4;
     static constexpr size_t OFF_BARS = STAGES;
     static constexpr size_t OFF_SCR = OFF_BARS + (size_t)NW * S * 8;
     // per-warp score scratch of the CUDA-core path (16-bit caches use none)
@@ -235,12 +246,17 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 #define PA_UNIT_COST_Q4 4
 #endif
 
-template <typename T, int D, int G, int NW, int S, bool PARTIAL>
+template <typename T, int D, int G, int NW, int S, int MODE>
 __global__ void __launch_bounds__(NW * 32)
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr bool TC = use_tc<T>();
-    using W = std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>;
-    using Lay = PersistentLayout<T, D, G, NW, S, PARTIAL>;
+    constexpr bool PARTIAL = MODE == MODE_PARTITIONED;
+    constexpr bool MQ = MODE == MODE_MULTI;
+    constexpr int ROWS = rows_of_mode(MODE, G);
+    static_assert(!MQ || TC, "multi-token queries use the tensor-core path");
+    using W = std::conditional_t<MQ, WarpAttnTC16<T, D>,
+                                 std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>>;
+    using Lay = PersistentLayout<T, D, G, NW, S, MODE>;
     using Sh = Shape<T, D>;
     constexpr int E = Sh::E;
     constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
@@ -280,6 +296,12 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             prefetch_tensormap(&p.tmap_v);
         }
     }
+    // multi-token queries: rows query_start[s] .. query_start[s+1]-1 belong to
+    // sequence s; a range outside its bounds is flagged and gets no rows
+    auto mq_valid = [&](int s, int L) -> bool {
+        const int a = p.query_start[s], b = p.query_start[s + 1];
+        return a >= 0 && b >= a && b <= p.num_q_rows && b - a <= p.max_query_len && b - a <= L;
+    };
     int Bp = NT;
     while (Bp < B) Bp <<= 1;
     uint32_t *keys = reinterpret_cast<uint32_t *>(stages);           // [Bp]
@@ -293,6 +315,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             if ((L0 < 0 || L0 > cap) && blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
             const int L = L0 < 0 ? 0 : (L0 > cap ? cap : L0);
             lens[i] = L;
+            if constexpr (MQ) {
+                if (blockIdx.x == 0 && !mq_valid(i, L)) set_error(p.err, ERR_SEQ_LEN);
+            }
             const int nb = (L + 15) >> 4;
             key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
         }
@@ -304,6 +329,11 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     // ---- 2. number the units: exclusive scan of units per sorted sequence -----
     auto units_of = [&](int pos) -> int {          // pos < B
         const int nb = 0xffff - (int)(keys[pos] >> 16);
+        if constexpr (MQ) {
+            const int s = (int)(keys[pos] & 0xffffu);
+            const int nq = mq_valid(s, lens[s]) ? p.query_start[s + 1] - p.query_start[s] : 0;
+            return Hkv * ((nq * G + 15) / 16);
+        }
         return PARTIAL ? Hkv * ((nb + PB - 1) / PB) : Hkv;
     };
     int U = 0;
@@ -346,7 +376,21 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         UnitRec u;
         u.s = s;
         u.L = lens[s];
-        if (PARTIAL) {
+        u.q0 = 0;
+        u.nq = 1;
+        if constexpr (MQ) {
+            const int q0 = p.query_start[s], nq = p.query_start[s + 1] - q0;   // valid: it has units
+            const int tiles = (nq * G + 15) / 16;
+            u.j = local / tiles;
+            u.part = local % tiles;
+            u.q0 = q0;
+            u.nq = nq;
+            u.lb0 = 0;
+            // the tile's last row sees positions up to L - nq + its token
+            const int last_tok = min(16 * u.part + 15, nq * G - 1) / G;
+            const int lim = u.L - nq + last_tok;             // >= 0: nq <= L
+            u.nb = lim >= 0 ? lim / 16 + 1 : 0;
+        } else if (PARTIAL) {
             const int ps = (nb + PB - 1) / PB;
             u.j = local / ps;
             u.part = local % ps;
@@ -418,7 +462,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     if (C > 1) cluster_sync();                     // peers' counters are initialised
 
     // units with no tokens (pa_decode only): their output is zero
-    if (!PARTIAL && rank == 0 && warp == NW - 1) {
+    if (!PARTIAL && !MQ && rank == 0 && warp == NW - 1) {
         for (int q = 0; q < nu; ++q) {
             const UnitRec u = units[q];
             if (u.nb != 0) continue;
@@ -433,7 +477,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     }
 
     // ---- 4. stream this warp's range of the cluster's blocks ------------------
-    const int F = cum[nu];
     auto range_lo = [&](int g) -> int { return bound[g]; };
     auto owner = [&](int f) -> int {               // warp whose range holds position f
         int lo = 0, hi = NWC - 1;                  // last warp starting at or before f
@@ -477,11 +520,11 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         ui = kk < 32 ? a : b;
         pb = kk < 32 ? x : y;
     };
-    auto rows_of = [&](int k, int ui) -> int {
+    auto pos_of = [&](int k, int ui) -> int {     // sequence position of block k's row 0
         const UnitRec &u = units[ui];
-        const int lb = u.lb0 + (my_lo + k - cum[ui]);
-        return min(16, u.L - lb * 16);
+        return (u.lb0 + (my_lo + k - cum[ui])) * 16;
     };
+    auto rows_of = [&](int k, int ui) -> int { return min(16, units[ui].L - pos_of(k, ui)); };
 
     unsigned char *my_stages = stages + (size_t)warp * S * 2 * TILE;
     uint64_t *my_bars = bars + warp * S;
@@ -539,6 +582,18 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                           : reinterpret_cast<float *>(stages + (size_t)(g % NW) * S * 2 * TILE);
     };
 
+    // Output row (in units of D) of row r of unit u's query tile; -1 if the
+    // tile's row is past the sequence's query rows.
+    auto out_row = [&](const UnitRec &u, int r) -> long long {
+        if constexpr (MQ) {
+            const int rr = 16 * u.part + r;
+            if (rr >= u.nq * G) return -1;
+            return (long long)(u.q0 + rr / G) * H + u.j * G + rr % G;
+        } else {
+            return (long long)u.s * H + u.j * G + r;
+        }
+    };
+
     // Write the result of unit u from a merged (M, L, O) of chunk (g, d0).
     auto emit = [&](const UnitRec &u, int g, int d0, float M, float Ls, float *O) {
         const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
@@ -556,7 +611,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         } else {
 #pragma unroll
             for (int e = 0; e < E; ++e) O[e] *= inv;
-            T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d0;
+            T *o = reinterpret_cast<T *>(p.out) + out_row(u, g) * D + d0;
             store_chunk<T>(o, O);
         }
     };
@@ -581,7 +636,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                         p.part_l[row] = l;
                     }
                 } else {
-                    T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G + g) * D + d;
+                    T *o = reinterpret_cast<T *>(p.out) + out_row(u, g) * D + d;
                     store_pair<T>(o, v0, v1);
                 }
             });
@@ -590,8 +645,8 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             return;
         }
         float *mine = part_of(gw, (from_before && !to_after) ? 0 : 1);
-        // partial layout: O[G][D], M[G], L[G]
-        wa.store_partial(mine + G * D, mine + G * D + G, mine);
+        // partial layout: O[ROWS][D], M[ROWS], L[ROWS]
+        wa.store_partial(mine + ROWS * D, mine + ROWS * D + ROWS, mine);
         __syncwarp();
         bool last = true;
         const int g_first = owner(u_lo), g_last = owner(u_hi - 1);
@@ -609,13 +664,14 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             if (last) fence_acq_rel_cluster();
         }
         if (last) {
-            for (int ch = lane; ch < G * (D / E); ch += 32) {
+            for (int ch = lane; ch < ROWS * (D / E); ch += 32) {
                 const int g = ch / (D / E), d0 = (ch % (D / E)) * E;
+                if (MQ && out_row(u, g) < 0) continue;
                 float M = -INFINITY;
                 for (int w = g_first; w <= g_last; ++w) {
                     if (range_lo(w) == range_lo(w + 1)) continue;
                     const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
-                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(pw + G * D + g, w / NW)));
+                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(pw + ROWS * D + g, w / NW)));
                 }
                 float O[E], Ls = 0.f;
 #pragma unroll
@@ -625,9 +681,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                         if (range_lo(w) == range_lo(w + 1)) continue;
                         const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
                         const uint32_t rw = (uint32_t)(w / NW);
-                        const float mw = ld_dsmem_f32(map_to_rank(pw + G * D + g, rw));
+                        const float mw = ld_dsmem_f32(map_to_rank(pw + ROWS * D + g, rw));
                         const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(pw + G * D + G + g, rw)), Ls);
+                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(pw + ROWS * D + ROWS + g, rw)), Ls);
 #pragma unroll
                         for (int e = 0; e < E; e += 4) {
                             const float4 a = ld_dsmem_f32x4(map_to_rank(pw + g * D + d0 + e, rw));
@@ -660,19 +716,33 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         if (ui != cur) {
             if (cur >= 0) leave_unit(cur);
             cur = ui;
-            auto qptr = [&](int q) {
-                const UnitRec &u = units[q];
-                return reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
-                       (long long)u.j * G * D;
-            };
-            if (qnext != ui) wa.prefetch_q(qptr(ui));
-            if constexpr (TC) wa.take_q();
-            else wa.take_q(p.scale_log2);
-            // load the next unit's query while this one streams
-            qnext = -1;
-            if (ui + 1 < nu && cum[ui + 1] < my_hi && units[ui + 1].nb > 0) {
-                qnext = ui + 1;
-                wa.prefetch_q(qptr(qnext));
+            if constexpr (MQ) {
+                // this lane's rows g and g + 8 of the unit's 16-row tile:
+                // (token i, head) pairs, token i seeing positions up to L - nq + i
+                const UnitRec &u = units[ui];
+                const int r_lo = 16 * u.part + (lane >> 2), r_hi = r_lo + 8;
+                auto qrow = [&](int r) -> const T * {
+                    if (r >= u.nq * G) return nullptr;
+                    return reinterpret_cast<const T *>(p.q) +
+                           (long long)(u.q0 + r / G) * p.q_seq_stride +
+                           (long long)(u.j * G + r % G) * D;
+                };
+                wa.load_q(qrow(r_lo), qrow(r_hi), u.L - u.nq + r_lo / G, u.L - u.nq + r_hi / G);
+            } else {
+                auto qptr = [&](int q) {
+                    const UnitRec &u = units[q];
+                    return reinterpret_cast<const T *>(p.q) + (long long)u.s * p.q_seq_stride +
+                           (long long)u.j * G * D;
+                };
+                if (qnext != ui) wa.prefetch_q(qptr(ui));
+                if constexpr (TC) wa.take_q();
+                else wa.take_q(p.scale_log2);
+                // load the next unit's query while this one streams
+                qnext = -1;
+                if (ui + 1 < nu && cum[ui + 1] < my_hi && units[ui + 1].nb > 0) {
+                    qnext = ui + 1;
+                    wa.prefetch_q(qptr(qnext));
+                }
             }
         }
         const int st = k % S;
@@ -684,13 +754,14 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             const int rows = rows_of(k, ui);
             if constexpr (TC) {
                 if (rows < 16) {                   // tail rows hold other tokens' data
-                    W::zero_rows(Kt + TILE, rows, lane);
+                    WarpAttnTC<T, D, G>::zero_rows(Kt + TILE, rows, lane);
                     // these generic writes must be ordered before the next
                     // bulk copy into the stage
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, p.scale_log2);
+                if constexpr (MQ) wa.block(smem_u32(Kt), smem_u32(Kt + TILE), pos_of(k, ui), p.scale_log2);
+                else wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, p.scale_log2);
             } else {
                 wa.block(Kt, Kt + TILE, rows, Sc, Pb, Al);
             }
@@ -723,39 +794,39 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
 #ifndef PA_STAGE_KB
 #define PA_STAGE_KB 16
 #endif
-template <typename T, int D, int G, bool PARTIAL>
+template <typename T, int D, int G, int MODE>
 __host__ __device__ constexpr int persistent_stages() {
     int s = PA_STAGE_KB * 1024 / (2 * Shape<T, D>::TILE_BYTES);
     s = s < 2 ? 2 : (s > 6 ? 6 : s);
-    while (s > 2 && PersistentLayout<T, D, G, 4, 0, PARTIAL>::BYTES +
+    while (s > 2 && PersistentLayout<T, D, G, 4, 0, MODE>::BYTES +
                             (size_t)4 * s * (2 * Shape<T, D>::TILE_BYTES + 8) > 113 * 1024)
         --s;
     return s;
 }
 
-template <typename T, int D, int G, bool PARTIAL>
+template <typename T, int D, int G, int MODE>
 struct PersistentConfig {
     static constexpr int NW = 4;
-    static constexpr int S = persistent_stages<T, D, G, PARTIAL>();
-    using Lay = PersistentLayout<T, D, G, NW, S, PARTIAL>;
+    static constexpr int S = persistent_stages<T, D, G, MODE>();
+    using Lay = PersistentLayout<T, D, G, NW, S, MODE>;
 };
 
 // Largest num_seqs the persistent kernel sorts in shared memory.
-template <typename T, int D, int G, bool PARTIAL>
+template <typename T, int D, int G, int MODE>
 constexpr int persistent_max_seqs() {
-    return PersistentConfig<T, D, G, PARTIAL>::Lay::MAX_SEQS;
+    return PersistentConfig<T, D, G, MODE>::Lay::MAX_SEQS;
 }
 
 // Clusters of `cluster` blocks, as many as fit on the GPU at once (looked up
 // once per device and cluster size), but at least enough that no cluster
 // gets more than NU_MAX units.
-template <typename T, int D, int G, bool PARTIAL>
+template <typename T, int D, int G, int MODE>
 cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int cluster,
                               cudaStream_t st) {
-    using C = PersistentConfig<T, D, G, PARTIAL>;
+    using C = PersistentConfig<T, D, G, MODE>;
     constexpr size_t smem = C::Lay::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory");
-    auto kern = decode_persistent_kernel<T, D, G, C::NW, C::S, PARTIAL>;
+    auto kern = decode_persistent_kernel<T, D, G, C::NW, C::S, MODE>;
     if (p.num_seqs > C::Lay::MAX_SEQS) return cudaErrorNotSupported;
     if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
     static int fitted[64][4];                      // clusters resident per device, per size
@@ -796,13 +867,12 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t dispatch_persistent(const DecodeParams &p, int D, int G, bool partial,
-                                long long unit_bound, int cluster, cudaStream_t st) {
-#define PA_CASE(DD, GG)                                                                   \
-    if (D == DD && G == GG)                                                               \
-        return partial ? launch_persistent<T, DD, GG, true>(p, unit_bound, cluster, st)  \
-                       : launch_persistent<T, DD, GG, false>(p, unit_bound, cluster, st);
+// Launch mode MODE for the built shapes: D in {64, 128}, G in {1, 2, 4, 8}.
+template <typename T, int MODE>
+cudaError_t dispatch_persistent(const DecodeParams &p, int D, int G, long long unit_bound,
+                                int cluster, cudaStream_t st) {
+#define PA_CASE(DD, GG) \
+    if (D == DD && G == GG) return launch_persistent<T, DD, GG, MODE>(p, unit_bound, cluster, st);
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
 #undef PA_CASE

@@ -69,6 +69,9 @@ def load():
         lib.pa_decode_partitioned.argtypes = dec + [i32, i32, P, sz, P]
         lib.pa_decode_partitioned_noalloc.restype = ctypes.c_int
         lib.pa_decode_partitioned_noalloc.argtypes = dec + [i32, i32, P]
+        lib.pa_decode_multi.restype = ctypes.c_int
+        lib.pa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                        i64, i32, i32, i64, f32, i32, P]
         lib.pa_device_error.restype = ctypes.c_int
         lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         _lib = lib
@@ -220,6 +223,42 @@ def pa_decode_partitioned_noalloc(out, q, k_cache, v_cache, block_tables, seq_le
     _check("pa_decode_partitioned_noalloc", rc)
 
 
+def pa_decode_multi(out, q, k_cache, v_cache, block_tables, seq_lens, query_start,
+                    max_query_len, scale, num_kv_heads, stream=None):
+    """Paged attention of several new tokens per sequence: q and out are
+    [T, H_q, D] with the rows of sequence s at query_start[s] ..
+    query_start[s+1]-1 (int32 [B+1]); row i of a sequence with n rows sees
+    positions 0 .. seq_lens[s] - n + i of its cache."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("seq_lens", seq_lens),
+                 ("query_start", query_start)):
+        _dev(t, n)
+    N, Hkv, bs, D = _cache_dims(k_cache, v_cache)
+    if num_kv_heads != Hkv:
+        raise ValueError("num_kv_heads does not match the cache")
+    if q.dim() != 3 or q.shape[2] != D or q.stride(2) != 1 or q.stride(1) != D:
+        raise ValueError("q must be [num_rows, num_heads, head_dim] with contiguous heads")
+    if out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if q.dtype != k_cache.dtype or out.dtype != k_cache.dtype:
+        raise ValueError("q, out and the caches must share a dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.dim() != 1 or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 [num_seqs]")
+    B = seq_lens.shape[0]
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != B or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks]")
+    if query_start.dtype != torch.int32 or query_start.shape != (B + 1,) or \
+            not query_start.is_contiguous():
+        raise ValueError("query_start must be a contiguous int32 [num_seqs + 1]")
+    rc = load().pa_decode_multi(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), seq_lens.data_ptr(), query_start.data_ptr(), B,
+        q.shape[0], int(max_query_len), q.shape[1], Hkv, D, N, bs, block_tables.shape[1],
+        q.stride(0), float(scale), _DTYPE[q.dtype], _stream(stream))
+    _check("pa_decode_multi", rc)
+
+
 def workspace_views(workspace, num_seqs, num_heads, head_dim, max_seq_len, partition_size):
     """(o_part, m_part, l_part) fp32 views of a partitioned-decode workspace,
     following the layout documented in include/pa.h."""
@@ -247,7 +286,7 @@ def pa_device_error(clear: bool = True) -> int:
 __all__ = [
     "PAError", "load", "library_path", "pa_status_string", "pa_abi_version",
     "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
-    "pa_decode_partitioned_workspace_size", "pa_decode_partitioned",
+    "pa_decode_partitioned_workspace_size", "pa_decode_partitioned", "pa_decode_multi",
     "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",
     "pa_device_error", "workspace_views",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SEQ_LEN", "PA_DEVERR_SLOT", "PA_DEVERR_TIMEOUT",

@@ -411,7 +411,7 @@ def random_batch(seed: int, *, num_seqs: int, max_len: int, num_heads: int,
 def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
                       n_new, num_heads: int, num_kv_heads: int, head_dim: int,
                       dtype: str, device="cpu", canary=True, keep_seq=True,
-                      kv_std: float = 1.0, lens=None) -> PagedBatch:
+                      kv_std: float = 1.0, lens=None, table_width=None) -> PagedBatch:
     """Several new query tokens per sequence (a prefill chunk, or the k+1
     positions of a speculative step), already written to the cache.
 
@@ -419,7 +419,8 @@ def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
     query tokens (positions seq_len - n_s .. seq_len - 1) are rows
     ``query_start[s] .. query_start[s+1]`` of ``q`` ([T, H, D]), kept in
     ``meta["query_start"]``.  ``n_new`` is an int or an inclusive (lo, hi)
-    range; ``lens`` optionally fixes the context lengths."""
+    range or one count per sequence; ``lens`` optionally fixes the context
+    lengths."""
     rng = np.random.default_rng(seed)
     if lens is None:
         ctx = rng.integers(min_ctx, max_ctx, size=num_seqs, endpoint=True)
@@ -427,8 +428,10 @@ def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
         ctx = np.asarray(lens, dtype=np.int64)
     if isinstance(n_new, int):
         n = np.full(num_seqs, n_new, dtype=np.int64)
-    else:
+    elif isinstance(n_new, tuple):
         n = rng.integers(n_new[0], n_new[1], size=num_seqs, endpoint=True)
+    else:
+        n = np.asarray(n_new, dtype=np.int64)
     total = ctx + n
     need = sum(math.ceil(int(L) / BLOCK_SIZE) for L in total)
     fl = FreeList(need + 8, rng)
@@ -436,7 +439,8 @@ def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
     b = build_batch(f"multi{seed}", ctx_lens=np.maximum(total - 1, 0), num_heads=num_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype,
                     num_blocks=need + 8, tables=tables, seed=seed, device=device,
-                    canary=canary, keep_seq=keep_seq, kv_std=kv_std, new_in_pool=True)
+                    canary=canary, keep_seq=keep_seq, kv_std=kv_std, new_in_pool=True,
+                    table_width=table_width)
     qs = np.zeros(num_seqs + 1, dtype=np.int32)
     qs[1:] = np.cumsum(n)
     gen = torch.Generator(device=torch.device(device))
@@ -448,6 +452,39 @@ def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
     b.meta["query_start"] = qs
     b.meta["n_new"] = n.astype(np.int32)
     return b
+
+
+def spec_verify(device="cpu", canary=True, batch=256, k=3, seed=11,
+                max_len=4096) -> PagedBatch:
+    """Speculative-decoding verification step: 256 sequences with the
+    serving-mix context lengths (lognormal, median 350, sigma 1.0, clipped to
+    [1, 4096]), each scoring k = 3 drafted tokens plus the next one (k + 1 = 4
+    query rows), 32/8 heads x 128, bf16, K/V ~ N(0,1)*0.5."""
+    rng = np.random.default_rng(seed)
+    ctx = lognormal_lengths(rng, batch, hi=max_len)
+    b = multi_query_batch(seed, num_seqs=batch, min_ctx=0, max_ctx=0, n_new=k + 1,
+                          num_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+                          device=device, canary=canary, keep_seq=False, kv_std=0.5,
+                          lens=ctx, table_width=math.ceil((max_len + k + 1) / BLOCK_SIZE))
+    return replace(b, name="spec_verify")
+
+
+def chunked_prefill_mix(device="cpu", canary=True, batch=128, chunks=4, chunk=512,
+                        seed=12, max_len=4096) -> PagedBatch:
+    """One mixed step of chunked prefill: ``chunks`` sequences each run a
+    ``chunk``-token slice of their prompt on top of 0..3072 earlier prompt
+    tokens, next to batch - chunks one-token decodes with serving-mix
+    lengths; 32/8 heads x 128, bf16, K/V ~ N(0,1)*0.5."""
+    rng = np.random.default_rng(seed)
+    ctx = lognormal_lengths(rng, batch, hi=max_len - 1)
+    ctx[:chunks] = rng.integers(0, 3072, size=chunks, endpoint=True)
+    n = np.ones(batch, dtype=np.int64)
+    n[:chunks] = chunk
+    b = multi_query_batch(seed, num_seqs=batch, min_ctx=0, max_ctx=0, n_new=n,
+                          num_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+                          device=device, canary=canary, keep_seq=False, kv_std=0.5,
+                          lens=ctx, table_width=math.ceil((max_len + chunk) / BLOCK_SIZE))
+    return replace(b, name="chunked_prefill_mix")
 
 
 # ---------------------------------------------------------------------------

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert pa.pa_abi_version() == 1
+    assert pa.pa_abi_version() == 2
     assert pa.pa_status_string(0) == "ok"
     assert "invalid" in pa.pa_status_string(-1)
     assert "unsupported" in pa.pa_status_string(-2)
@@ -102,3 +102,30 @@ def test_host_side_argument_checks(lib):
     rc = lib.pa_decode_partitioned(1, 1, 16, 16, 1, 1, 4, 8, 2, 64, 10, 16, 4, 512,
                                    0.125, 0, 100, 64, ws, 1 << 20, None)
     assert rc == -1                                             # partition not x16
+
+
+def _multi_status(lib, **kw):
+    a = dict(out=16, q=16, k_cache=16, v_cache=16, block_tables=16, seq_lens=16,
+             query_start=16, num_seqs=4, num_q_rows=12, max_query_len=3, num_heads=8,
+             num_kv_heads=2, head_dim=64, num_blocks=10, block_size=16, max_blocks=4,
+             q_row_stride=512, scale=0.125, dtype=1)
+    a.update(kw)
+    return lib.pa_decode_multi(a["out"], a["q"], a["k_cache"], a["v_cache"],
+                               a["block_tables"], a["seq_lens"], a["query_start"],
+                               a["num_seqs"], a["num_q_rows"], a["max_query_len"],
+                               a["num_heads"], a["num_kv_heads"], a["head_dim"],
+                               a["num_blocks"], a["block_size"], a["max_blocks"],
+                               a["q_row_stride"], a["scale"], a["dtype"], None)
+
+
+def test_multi_query_host_checks(lib):
+    assert _multi_status(lib, dtype=0) == -2                   # fp32: not built
+    assert _multi_status(lib, query_start=None) == -1
+    assert _multi_status(lib, num_q_rows=-1) == -1
+    assert _multi_status(lib, max_query_len=-1) == -1
+    assert _multi_status(lib, q=8) == -1                       # q not 16-byte aligned
+    assert _multi_status(lib, q_row_stride=516) == -1          # rows not 16-byte aligned
+    assert _multi_status(lib, head_dim=96) == -2
+    assert _multi_status(lib, num_seqs=0) == 0                 # nothing to do
+    assert _multi_status(lib, num_q_rows=0) == 0
+    assert _multi_status(lib, max_query_len=0) == 0            # no rows can exist
