@@ -21,6 +21,9 @@ fp64 numpy arrays.  The arithmetic is documented in ``pa_ref.c``:
   their log-sum-exp merge.
 * ``kv_bytes_per_token`` / ``bytes_per_block`` / ``blocks_for_tokens`` --
   the pages' KV sizing arithmetic.
+* ``e4m3_encode`` / ``e4m3_decode`` / ``reshape_and_cache_fp8`` and the
+  ``kv_scales=`` form of ``decode`` / ``decode_one`` -- the FP8 (E4M3) KV
+  cache with one scale per KV head for K and for V.
 """
 from __future__ import annotations
 
@@ -78,6 +81,17 @@ def bind(path: str):
     lib.pa_ref_decode_multi.restype = ctypes.c_int
     lib.pa_ref_decode_multi.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i64,
                                         i64, i64, f32, i32]
+    lib.pa_ref_e4m3_to_double.restype = ctypes.c_double
+    lib.pa_ref_e4m3_to_double.argtypes = [i32]
+    lib.pa_ref_e4m3_from_float.restype = i32
+    lib.pa_ref_e4m3_from_float.argtypes = [f32]
+    lib.pa_ref_reshape_and_cache_fp8.restype = i64
+    lib.pa_ref_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, i64, i32, i32, i64, i64,
+                                                 i32, i64, i32, P, P]
+    lib.pa_ref_decode_fp8.restype = ctypes.c_int
+    lib.pa_ref_decode_fp8.argtypes = [P] + common + [P, P, i32]
+    lib.pa_ref_decode_one_fp8.restype = ctypes.c_int
+    lib.pa_ref_decode_one_fp8.argtypes = [P, P, i64, i32] + common + [P, P]
     lib.pa_ref_lse_merge.restype = None
     lib.pa_ref_lse_merge.argtypes = [P, P, P, P, i64, i32]
     return lib
@@ -147,6 +161,8 @@ def _host(x, np_dtype=None) -> np.ndarray:
                 raise ValueError("oracle takes host tensors")
             if x.dtype in (torch.bfloat16, torch.float16):
                 x = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+            elif x.dtype in (getattr(torch, "float8_e4m3fn", None), torch.uint8):
+                x = x.contiguous().view(torch.uint8).numpy()
             else:
                 x = x.contiguous().numpy()
     except ImportError:  # pragma: no cover
@@ -190,11 +206,48 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, dtype: str):
     return kc, vc, int(bad)
 
 
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (uint8) of binary32 values: nearest, ties to even,
+    saturating at +-448; NaN -> 0x7F."""
+    x = np.asarray(x, dtype=np.float32)
+    f = _active().pa_ref_e4m3_from_float
+    return np.array([f(float(v)) for v in x.reshape(-1)], dtype=np.uint8).reshape(x.shape)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (fp64) of E4M3 codes."""
+    c = np.asarray(codes, dtype=np.uint8)
+    f = _active().pa_ref_e4m3_to_double
+    return np.array([f(int(v)) for v in c.reshape(-1)], dtype=np.float64).reshape(c.shape)
+
+
+def reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, dtype: str, k_scale,
+                          v_scale):
+    """FP8 cache write: return (k_cache', v_cache', n_bad) with the new rows
+    stored as E4M3(x / scale[j]).  ``k``/``v``: [T, H_kv, D] in ``dtype``;
+    caches: E4M3 codes [N, H_kv, bs, D] (copied, not modified); scales [H_kv]."""
+    lib = _active()
+    k = _host(k); v = _host(v)
+    kc = _host(k_cache).copy(); vc = _host(v_cache).copy()
+    sm = _host(slot_mapping, np.int64)
+    ks = _host(k_scale, np.float32); vs = _host(v_scale, np.float32)
+    T, Hkv, D = k.shape
+    N, _, bs, _ = kc.shape
+    if ks.shape != (Hkv,) or vs.shape != (Hkv,):
+        raise ValueError("one K and one V scale per KV head")
+    bad = lib.pa_ref_reshape_and_cache_fp8(_p(k), _p(v), _p(kc), _p(vc), _p(sm), T, Hkv,
+                                           D, Hkv * D, Hkv * D, bs, N, REF_DTYPE[dtype],
+                                           _p(ks), _p(vs))
+    return kc, vc, int(bad)
+
+
 class _Problem:
-    """Marshalled arguments shared by the decode entry points."""
+    """Marshalled arguments shared by the decode entry points.  With
+    ``kv_scales=(k_scale, v_scale)`` the caches hold E4M3 codes and ``dtype``
+    is the type of q."""
 
     def __init__(self, q, k_cache, v_cache, block_tables, seq_lens, scale,
-                 num_kv_heads, dtype):
+                 num_kv_heads, dtype, kv_scales=None):
         self.q = _host(q)
         self.kc = _host(k_cache)
         self.vc = _host(v_cache)
@@ -208,6 +261,17 @@ class _Problem:
         self.max_blocks = self.bt.shape[1]
         self.scale = float(scale)
         self.dtype = REF_DTYPE[dtype]
+        self.fp8 = kv_scales is not None
+        if self.fp8:
+            self.ks = _host(kv_scales[0], np.float32)
+            self.vs = _host(kv_scales[1], np.float32)
+            if self.ks.shape != (kvh,) or self.vs.shape != (kvh,):
+                raise ValueError("one K and one V scale per KV head")
+            if self.kc.dtype != np.uint8:
+                raise ValueError("FP8 caches hold uint8 E4M3 codes")
+
+    def scales(self):
+        return [_p(self.ks), _p(self.vs)]
 
     def common(self):
         return [_p(self.q), _p(self.kc), _p(self.vc), _p(self.bt), _p(self.sl),
@@ -216,12 +280,16 @@ class _Problem:
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, num_kv_heads,
-           dtype: str, nthreads: int = 1) -> np.ndarray:
-    """fp64 decode attention for every (sequence, query head): [B, H_q, D]."""
+           dtype: str, nthreads: int = 1, kv_scales=None) -> np.ndarray:
+    """fp64 decode attention for every (sequence, query head): [B, H_q, D].
+    ``kv_scales=(k_scale, v_scale)``: E4M3 caches with per-KV-head scales."""
     pr = _Problem(q, k_cache, v_cache, block_tables, seq_lens, scale,
-                  num_kv_heads, dtype)
+                  num_kv_heads, dtype, kv_scales)
     out = np.zeros((pr.B, pr.H, pr.D), dtype=np.float64)
-    rc = _active().pa_ref_decode(_p(out), *pr.common(), int(nthreads))
+    if pr.fp8:
+        rc = _active().pa_ref_decode_fp8(_p(out), *pr.common(), *pr.scales(), int(nthreads))
+    else:
+        rc = _active().pa_ref_decode(_p(out), *pr.common(), int(nthreads))
     if rc:
         raise ValueError("oracle decode: invalid input (block id or seq_len out of range)")
     return out
@@ -235,7 +303,11 @@ def decode_one(s, h, q, k_cache, v_cache, block_tables, seq_lens, scale,
     L = int(pr.sl[s])
     out = np.zeros(pr.D, dtype=np.float64)
     w = np.zeros(max(L, 1), dtype=np.float64)
-    rc = _active().pa_ref_decode_one(_p(out), _p(w), int(s), int(h), *pr.common())
+    if pr.fp8:
+        rc = _active().pa_ref_decode_one_fp8(_p(out), _p(w), int(s), int(h), *pr.common(),
+                                             *pr.scales())
+    else:
+        rc = _active().pa_ref_decode_one(_p(out), _p(w), int(s), int(h), *pr.common())
     if rc:
         raise ValueError("oracle decode_one: invalid input")
     return out, w[:L]
@@ -264,11 +336,11 @@ def decode_multi(q, k_cache, v_cache, block_tables, seq_lens, query_start, scale
 
 
 def problem(q, k_cache, v_cache, block_tables, seq_lens, scale, num_kv_heads,
-            dtype: str) -> _Problem:
+            dtype: str, kv_scales=None) -> _Problem:
     """Marshal once, then pass as ``problem=`` to ``decode_one`` /
     ``partition_stats`` for many samples of one large batch."""
     return _Problem(q, k_cache, v_cache, block_tables, seq_lens, scale,
-                    num_kv_heads, dtype)
+                    num_kv_heads, dtype, kv_scales)
 
 
 def partition_stats(s, h, partition_size, q, k_cache, v_cache, block_tables,

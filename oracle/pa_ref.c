@@ -43,8 +43,20 @@
  *        out = sum_p c_p o_p / sum_p c_p,
  *    which equals the unpartitioned softmax exactly in real arithmetic.
  *
+ *  - FP8 KV cache (named, without a format, as the way to enlarge the pool in
+ *    "vLLM: Architecture, PagedAttention & Internals", *The knobs that
+ *    actually matter*, item 5, and "vLLM: High-Throughput Serving with
+ *    PagedAttention", *The benefits of vLLM*).  Reading taken here: the OCP
+ *    FP8 E4M3 format with one float scale per KV head for K and one for V.
+ *    The cache write stores code = E4M3(x / scale_j), the quotient rounded
+ *    once to binary32 and then to E4M3 (round to nearest, ties to even;
+ *    finite values beyond the largest code, and infinities, saturate to
+ *    +-448; NaN becomes the NaN code 0x7F).  Attention reads
+ *    value(code) * scale_j and is otherwise unchanged.
+ *
  * Storage formats read here: f32, bf16 (the upper 16 bits of an IEEE binary32)
- * and f16 (IEEE binary16), each widened exactly to double.
+ * and f16 (IEEE binary16), each widened exactly to double, and E4M3 codes in
+ * FP8 caches.
  */
 #include <math.h>
 #include <pthread.h>
@@ -52,7 +64,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { REF_F32 = 0, REF_BF16 = 1, REF_F16 = 2 };
+enum { REF_F32 = 0, REF_BF16 = 1, REF_F16 = 2, REF_E4M3 = 3 };
 
 /* ---- element access ---------------------------------------------------- */
 
@@ -72,8 +84,54 @@ static double f16_bits_to_double(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* OCP FP8 E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ * infinities; exponent 15 with fraction 7 is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448; exponent 0 holds the subnormals f * 2^-9. */
+double pa_ref_e4m3_to_double(int32_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xf;
+    int f = code & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) v = ldexp((double)f, -9);
+    else v = ldexp((double)(8 + f), e - 10);    /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Round a binary32 value to E4M3: to nearest, ties to even; magnitudes above
+ * 448 (after rounding) and infinities saturate to 448; NaN gives 0x7F. */
+int32_t pa_ref_e4m3_from_float(float x) {
+    if (isnan(x)) return 0x7f;
+    const int sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    if (a > 448.0) return sign | 0x7e;
+    /* the spacing of E4M3 values around a: 2^(E-3) for a in [2^E, 2^(E+1)),
+     * E >= -6; the subnormal range [0, 2^-6) has spacing 2^-9 */
+    int E = -6;
+    if (a >= ldexp(1.0, -6)) {
+        int e2;
+        frexp(a, &e2);                 /* a = f * 2^e2, f in [0.5, 1) */
+        E = e2 - 1;
+    }
+    const double step = ldexp(1.0, E - 3);
+    const double n = a / step;         /* exact: a power-of-two divisor */
+    double r = floor(n);
+    const double rem = n - r;
+    if (rem > 0.5 || (rem == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    const double v = r * step;         /* the rounded magnitude */
+    if (v > 448.0) return sign | 0x7e;
+    if (v < ldexp(1.0, -6)) return sign | (int)(v / ldexp(1.0, -9));
+    int ev;
+    frexp(v, &ev);
+    const int Ev = ev - 1;             /* v in [2^Ev, 2^(Ev+1)) */
+    const int f = (int)(v / ldexp(1.0, Ev - 3)) - 8;
+    return sign | ((Ev + 7) << 3) | f;
+}
+
 static double load_elem(const void *base, int64_t idx, int dtype) {
-    if (dtype == REF_F32) {
+    if (dtype == REF_E4M3) {
+        return pa_ref_e4m3_to_double(((const uint8_t *)base)[idx]);
+    } else if (dtype == REF_F32) {
         return (double)((const float *)base)[idx];
     } else if (dtype == REF_BF16) {
         uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
@@ -85,7 +143,7 @@ static double load_elem(const void *base, int64_t idx, int dtype) {
     }
 }
 
-static int elem_bytes(int dtype) { return dtype == REF_F32 ? 4 : 2; }
+static int elem_bytes(int dtype) { return dtype == REF_F32 ? 4 : (dtype == REF_E4M3 ? 1 : 2); }
 
 /* ---- sizes ("vLLM: High-Throughput Serving with PagedAttention" (lesson 13.15), *The problem: the KV cache eats GPU
  * memory*; "vLLM: Architecture, PagedAttention & Internals", *How many blocks
@@ -144,6 +202,36 @@ int64_t pa_ref_reshape_and_cache(const void *k, const void *v, void *k_cache,
     return bad;
 }
 
+/* FP8 cache write: k, v as above in `src_dtype` (f32, bf16 or f16); caches
+ * hold E4M3 codes; element d of KV head j becomes E4M3(x / scale_j) with the
+ * quotient taken in binary32.  Returns the number of out-of-range slots. */
+int64_t pa_ref_reshape_and_cache_fp8(const void *k, const void *v, uint8_t *k_cache,
+                                     uint8_t *v_cache, const int64_t *slot_mapping,
+                                     int64_t num_tokens, int32_t num_kv_heads,
+                                     int32_t head_dim, int64_t k_tok_stride,
+                                     int64_t v_tok_stride, int32_t block_size,
+                                     int64_t num_blocks, int32_t src_dtype,
+                                     const float *k_scale, const float *v_scale) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * (int64_t)block_size) { ++bad; continue; }
+        int64_t blk = slot / block_size;
+        int64_t row = slot % block_size;
+        for (int32_t j = 0; j < num_kv_heads; ++j) {
+            int64_t dst = ((blk * num_kv_heads + j) * block_size + row) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                float xk = (float)load_elem(k, t * k_tok_stride + (int64_t)j * head_dim + d, src_dtype);
+                float xv = (float)load_elem(v, t * v_tok_stride + (int64_t)j * head_dim + d, src_dtype);
+                k_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xk / k_scale[j]);
+                v_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xv / v_scale[j]);
+            }
+        }
+    }
+    return bad;
+}
+
 /* ---- decode attention ---------------------------------------------------- */
 
 typedef struct {
@@ -157,7 +245,10 @@ typedef struct {
     int64_t num_blocks, max_blocks;
     int64_t q_seq_stride, q_head_stride;
     double scale;
-    int32_t dtype;
+    int32_t dtype;            /* q (and, unless kv_dtype says otherwise, the caches) */
+    int32_t kv_dtype;         /* storage of k_cache / v_cache */
+    const float *k_scale;     /* E4M3 caches: [H_kv] dequantisation scales */
+    const float *v_scale;
 } ref_args;
 
 /* Gather the L tokens of (sequence s, KV head j) through the block table into
@@ -170,9 +261,11 @@ static int gather_kv(const ref_args *a, int64_t s, int32_t j, int64_t L,
         int64_t pb = a->block_tables[s * a->max_blocks + lb];
         if (pb < 0 || pb >= a->num_blocks) return -1;
         int64_t base = ((pb * a->num_kv_heads + j) * bs + t % bs) * D;
+        const double ks = a->k_scale ? (double)a->k_scale[j] : 1.0;
+        const double vs = a->v_scale ? (double)a->v_scale[j] : 1.0;
         for (int64_t d = 0; d < D; ++d) {
-            K[t * D + d] = load_elem(a->k_cache, base + d, a->dtype);
-            V[t * D + d] = load_elem(a->v_cache, base + d, a->dtype);
+            K[t * D + d] = load_elem(a->k_cache, base + d, a->kv_dtype) * ks;
+            V[t * D + d] = load_elem(a->v_cache, base + d, a->kv_dtype) * vs;
         }
     }
     return 0;
@@ -264,32 +357,24 @@ static int make_args(ref_args *a, const void *q, const void *k_cache,
     a->max_blocks = max_blocks; a->q_seq_stride = q_seq_stride;
     a->q_head_stride = q_head_stride; a->scale = (double)scale;
     a->dtype = dtype;
+    a->kv_dtype = dtype;
+    a->k_scale = NULL;
+    a->v_scale = NULL;
     return 0;
 }
 
 /* Full decode: out[B][H_q][D] (fp64).  The (s, h) pairs are split over
  * `nthreads` threads; each pair is computed independently, so the result does
  * not depend on the thread count. */
-int pa_ref_decode(double *out, const void *q, const void *k_cache,
-                  const void *v_cache, const int32_t *block_tables,
-                  const int32_t *seq_lens, int64_t num_seqs, int32_t num_heads,
-                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                  int64_t num_blocks, int64_t max_blocks, int64_t q_seq_stride,
-                  int64_t q_head_stride, float scale, int32_t dtype,
-                  int32_t nthreads) {
-    ref_args a;
-    if (make_args(&a, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
-                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                  max_blocks, q_seq_stride, q_head_stride, scale, dtype))
-        return -1;
-    int64_t n = num_seqs * num_heads;
+static int run_decode(const ref_args *a, double *out, int32_t nthreads) {
+    int64_t n = a->num_seqs * a->num_heads;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if (n < nthreads) nthreads = (int32_t)(n > 0 ? n : 1);
     pthread_t th[256];
     ref_job jobs[256];
     for (int i = 0; i < nthreads; ++i) {
-        jobs[i].a = &a; jobs[i].out = out;
+        jobs[i].a = a; jobs[i].out = out;
         jobs[i].begin = n * i / nthreads; jobs[i].end = n * (i + 1) / nthreads;
         jobs[i].rc = 0;
     }
@@ -306,6 +391,64 @@ int pa_ref_decode(double *out, const void *q, const void *k_cache,
         }
     }
     return rc;
+}
+
+int pa_ref_decode(double *out, const void *q, const void *k_cache,
+                  const void *v_cache, const int32_t *block_tables,
+                  const int32_t *seq_lens, int64_t num_seqs, int32_t num_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                  int64_t num_blocks, int64_t max_blocks, int64_t q_seq_stride,
+                  int64_t q_head_stride, float scale, int32_t dtype,
+                  int32_t nthreads) {
+    ref_args a;
+    if (make_args(&a, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks, q_seq_stride, q_head_stride, scale, dtype))
+        return -1;
+    return run_decode(&a, out, nthreads);
+}
+
+/* Decode over E4M3 caches: `dtype` is the type of q; K and V of KV head j
+ * read value(code) * k_scale[j] and value(code) * v_scale[j]. */
+int pa_ref_decode_fp8(double *out, const void *q, const void *k_cache,
+                      const void *v_cache, const int32_t *block_tables,
+                      const int32_t *seq_lens, int64_t num_seqs, int32_t num_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int64_t num_blocks, int64_t max_blocks, int64_t q_seq_stride,
+                      int64_t q_head_stride, float scale, int32_t dtype,
+                      const float *k_scale, const float *v_scale, int32_t nthreads) {
+    ref_args a;
+    if (make_args(&a, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks, q_seq_stride, q_head_stride, scale, dtype))
+        return -1;
+    if (!k_scale || !v_scale) return -1;
+    a.kv_dtype = REF_E4M3;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return run_decode(&a, out, nthreads);
+}
+
+/* One (sequence, query head) over E4M3 caches (see pa_ref_decode_fp8). */
+int pa_ref_decode_one_fp8(double *out, double *weights, int64_t s, int32_t h,
+                          const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, const int32_t *seq_lens,
+                          int64_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                          int64_t max_blocks, int64_t q_seq_stride,
+                          int64_t q_head_stride, float scale, int32_t dtype,
+                          const float *k_scale, const float *v_scale) {
+    ref_args a;
+    if (make_args(&a, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                  num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  max_blocks, q_seq_stride, q_head_stride, scale, dtype))
+        return -1;
+    if (!k_scale || !v_scale) return -1;
+    if (s < 0 || s >= num_seqs || h < 0 || h >= num_heads) return -1;
+    a.kv_dtype = REF_E4M3;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return decode_one(&a, s, h, out, weights);
 }
 
 /* One (sequence, query head): out[D], and the normalised softmax weights

@@ -488,6 +488,61 @@ def chunked_prefill_mix(device="cpu", canary=True, batch=128, chunks=4, chunk=51
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) pools
+# ---------------------------------------------------------------------------
+
+FP8_NAN = 0x7F            # an E4M3 NaN code: the canary of unreferenced FP8 slots
+
+
+def with_fp8_pool(batch: PagedBatch, seed: int, kv_std: float = 0.5) -> PagedBatch:
+    """The same tables, queries and new rows over a pool of E4M3 codes.
+
+    Per KV head j a K scale and a V scale are drawn as ``4 * kv_std / 448``
+    times U[0.75, 1.25]; every pool element that holds a token gets the code
+    of a N(0, (kv_std / scale_j)^2) draw clamped to [-448, 448] (so real
+    values are about N(0, kv_std^2) and the largest ones saturate), and slots
+    left as canaries in ``batch`` hold the NaN code.  Codes are uint8 tensors
+    [N, H_kv, bs, D]; the scales are float32 [H_kv] in ``meta["k_scale"]`` and
+    ``meta["v_scale"]``.  ``q``, ``k_new`` and ``v_new`` keep their 16-bit (or
+    f32) values: the step's cache write quantises them."""
+    device = batch.device
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) + 104729)
+    Hkv = batch.num_kv_heads
+    base = 4.0 * kv_std / 448.0
+    scales = []
+    for _ in range(2):
+        u = torch.rand((Hkv,), generator=gen, device=device) * 0.5 + 0.75
+        scales.append((u * base).float())
+    pools = []
+    for cache, sc in ((batch.k_cache, scales[0]), (batch.v_cache, scales[1])):
+        z = torch.randn(cache.shape, generator=gen, device=device)
+        z = (z * (kv_std / sc).view(1, Hkv, 1, 1)).clamp_(-448.0, 448.0)
+        codes = z.to(torch.float8_e4m3fn).view(torch.uint8)
+        codes = torch.where(torch.isnan(cache), torch.full_like(codes, FP8_NAN), codes)
+        pools.append(codes.contiguous())
+    meta = dict(batch.meta)
+    meta["kv"] = "e4m3"
+    meta["k_scale"] = scales[0].contiguous()
+    meta["v_scale"] = scales[1].contiguous()
+    return replace(batch, k_cache=pools[0], v_cache=pools[1], seq_k=None, seq_v=None,
+                   name=batch.name + "_fp8", meta=meta)
+
+
+def serving_mix_fp8(device="cpu", canary=True, new_in_pool=False) -> PagedBatch:
+    """The serving mix (batch 256, lognormal lengths, 32/8 x 128, bf16 q and
+    new rows) over an E4M3 pool with per-KV-head scales."""
+    return with_fp8_pool(serving_mix(device=device, canary=canary, new_in_pool=new_in_pool),
+                         seed=13)
+
+
+def long_context_fp8(device="cpu", canary=True) -> PagedBatch:
+    """The long-context batch (8 seqs x 32k..128k tokens, 64/8 x 128, bf16 q)
+    over an E4M3 pool with per-KV-head scales."""
+    return with_fp8_pool(long_context(device=device, canary=canary), seed=15)
+
+
+# ---------------------------------------------------------------------------
 # Layout transforms used by the invariance tests
 # ---------------------------------------------------------------------------
 

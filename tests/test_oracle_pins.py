@@ -423,6 +423,148 @@ def test_reshape_and_cache_rejects_out_of_range_slots():
 
 
 # ---------------------------------------------------------------------------
+# FP8 (E4M3) cache: the format against torch's float8_e4m3fn, the write
+# against element-wise library conversion, the read against SDPA on the
+# dequantised values
+# ---------------------------------------------------------------------------
+
+ALL_CODES = np.arange(256, dtype=np.uint8)
+
+
+def torch_e4m3_values(codes) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(
+        torch.float8_e4m3fn).double().numpy()
+
+
+def torch_e4m3_codes(x) -> np.ndarray:
+    """torch's round-to-nearest-even conversion (it does not saturate: only
+    for magnitudes below 464)."""
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def test_e4m3_decoding_of_every_code():
+    got = oracle.e4m3_decode(ALL_CODES)
+    ref = torch_e4m3_values(ALL_CODES)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    # the format's landmarks: largest finite, smallest normal and subnormal,
+    # one, the two NaN codes
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0
+    assert got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+    assert got[0x38] == 1.0 and got[0xC0] == -2.0
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+    assert np.isnan(got).sum() == 2
+
+
+def test_e4m3_encoding_round_to_nearest_even():
+    vals = oracle.e4m3_decode(ALL_CODES)
+    finite = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = (finite[:-1] + finite[1:]) / 2            # every tie between neighbours
+    rng = np.random.default_rng(0)
+    rand = rng.standard_normal(6000) * np.exp2(rng.integers(-14, 10, 6000))
+    x = np.concatenate([finite, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9),
+                        rand, -rand]).astype(np.float32)
+    x = x[np.abs(x) < 464]
+    assert np.array_equal(oracle.e4m3_encode(x), torch_e4m3_codes(x))
+    # encode(decode(c)) == c for every finite code except -0 / +0 aliasing none
+    fin = np.isfinite(vals)
+    assert np.array_equal(oracle.e4m3_encode(vals[fin].astype(np.float32)), ALL_CODES[fin])
+
+
+def test_e4m3_encoding_saturates_and_keeps_nan():
+    big = np.array([448.5, 463.9, 464.0, 1e6, 3.4e38, np.inf], dtype=np.float32)
+    assert (oracle.e4m3_encode(big) == 0x7E).all()
+    assert (oracle.e4m3_encode(-big) == 0xFE).all()
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+    assert oracle.e4m3_encode(np.array([-0.0, -1e-30, 1e-30], np.float32)).tolist() == \
+        [0x80, 0x80, 0x00]
+
+
+def fp8_scales(Hkv, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.uniform(0.003, 0.02, Hkv).astype(np.float32),
+            rng.uniform(0.003, 0.02, Hkv).astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_reshape_and_cache_fp8_matches_elementwise_conversion(dtype):
+    b = wl.random_batch(22, num_seqs=9, max_len=40, num_heads=8, num_kv_heads=4,
+                        head_dim=64, dtype=dtype, kv_std=1.0)
+    b = wl.with_fp8_pool(b, seed=1)
+    ks, vs = fp8_scales(4, 2)
+    sm = b.slot_mapping.copy()
+    sm[2] = -1
+    kc, vc, bad = oracle.reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache, b.v_cache, sm,
+                                               dtype, ks, vs)
+    assert bad == 0
+    for pool, new, sc, got in ((b.k_cache, b.k_new, ks, kc), (b.v_cache, b.v_new, vs, vc)):
+        q = new.float().numpy() / sc[None, :, None]          # binary32 quotients
+        assert np.abs(q).max() > 448                          # some saturate
+        q = np.clip(q, -448.0, 448.0)                         # saturation, then RNE
+        ref = pool.numpy().copy()
+        N, Hkv, bs, D = ref.shape
+        tok = ref.transpose(0, 2, 1, 3).reshape(N * bs, Hkv, D).copy()
+        keep = sm >= 0
+        tok[sm[keep]] = torch_e4m3_codes(q[keep])
+        ref = tok.reshape(N, bs, Hkv, D).transpose(0, 2, 1, 3)
+        assert np.array_equal(got, ref)
+
+
+def dequantised_sdpa(b, s, ks, vs):
+    """SDPA of sequence s on K/V gathered by plain indexing and dequantised
+    with torch's float8 conversion."""
+    L = int(b.seq_lens[s])
+    nb = -(-L // 16)
+    blocks = torch.from_numpy(b.block_tables[s, :nb].astype(np.int64))
+    def gather(pool, sc):
+        c = pool[blocks].permute(0, 2, 1, 3).reshape(nb * 16, b.num_kv_heads, b.head_dim)[:L]
+        v = c.contiguous().view(torch.float8_e4m3fn).double()
+        return v * torch.from_numpy(sc).double().view(1, -1, 1)
+    k, v = gather(b.k_cache, ks), gather(b.v_cache, vs)
+    q = b.q[s].double()[None, :, None, :]
+    out = F.scaled_dot_product_attention(q, k.permute(1, 0, 2)[None], v.permute(1, 0, 2)[None],
+                                         scale=float(np.float32(b.scale)), enable_gqa=True)
+    return out[0, :, 0, :].numpy()
+
+
+@pytest.mark.parametrize("H,Hkv,D", [(32, 8, 128), (8, 8, 64), (16, 2, 64)])
+def test_decode_fp8_matches_sdpa_on_dequantised_cache(H, Hkv, D):
+    b = wl.random_batch(23 + H, num_seqs=5, max_len=90, num_heads=H, num_kv_heads=Hkv,
+                        head_dim=D, dtype="bf16", new_in_pool=True)
+    b = wl.with_fp8_pool(b, seed=3)
+    ks, vs = b.meta["k_scale"].numpy(), b.meta["v_scale"].numpy()
+    assert len(set(ks.tolist())) == Hkv                  # distinct per-head scales
+    out = oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
+                        Hkv, "bf16", kv_scales=(ks, vs))
+    for s in range(b.num_seqs):
+        np.testing.assert_allclose(out[s], dequantised_sdpa(b, s, ks, vs), rtol=0, atol=1e-9)
+
+
+def test_decode_fp8_with_power_of_two_scales_is_decode_of_the_values():
+    """With scales 2^k the dequantised values are exact in f32: the FP8 read
+    must give bit for bit what the f32 read of those values gives."""
+    b = wl.random_batch(24, num_seqs=4, max_len=70, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype="f32", new_in_pool=True)
+    b = wl.with_fp8_pool(b, seed=4)
+    ks = np.array([2.0 ** -7, 2.0 ** -5], np.float32)
+    vs = np.array([2.0 ** -6, 2.0 ** -8], np.float32)
+    kf = (torch_e4m3_values(b.k_cache.numpy()) * ks[None, :, None, None]).astype(np.float32)
+    vf = (torch_e4m3_values(b.v_cache.numpy()) * vs[None, :, None, None]).astype(np.float32)
+    ref = oracle.decode(b.q, kf, vf, b.block_tables, b.seq_lens, b.scale, 2, "f32")
+    got = oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale, 2,
+                        "f32", kv_scales=(ks, vs))
+    assert np.array_equal(np.isnan(ref), np.isnan(got)) and not np.isnan(got).any()
+    assert np.array_equal(ref, got)
+    for s, h in ((0, 0), (3, 7)):
+        one, _ = oracle.decode_one(s, h, b.q, b.k_cache, b.v_cache, b.block_tables,
+                                   b.seq_lens, b.scale, 2, "f32", problem=oracle.problem(
+                                       b.q, b.k_cache, b.v_cache, b.block_tables,
+                                       b.seq_lens, b.scale, 2, "f32", kv_scales=(ks, vs)))
+        assert np.array_equal(one, got[s, h])
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: each must make at least one pin fail
 # ---------------------------------------------------------------------------
 
@@ -440,6 +582,13 @@ MUTATIONS = {
                          "int64_t pb = a->block_tables[s + lb * a->num_seqs];"),
     "multi_causal_offset": ("const int64_t seen = L - n + i + 1;     /* causal prefix */",
                             "const int64_t seen = L - n + i;     /* causal prefix */"),
+    "e4m3_bias": ("else v = ldexp((double)(8 + f), e - 10);", "else v = ldexp((double)(8 + f), e - 9);"),
+    "e4m3_ties_away": ("if (rem > 0.5 || (rem == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;",
+                       "if (rem >= 0.5) r += 1.0;"),
+    "fp8_write_multiplies": ("k_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xk / k_scale[j]);",
+                             "k_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xk * k_scale[j]);"),
+    "fp8_read_head_scale": ("const double vs = a->v_scale ? (double)a->v_scale[j] : 1.0;",
+                            "const double vs = a->v_scale ? (double)a->v_scale[0] : 1.0;"),
 }
 
 
@@ -479,6 +628,33 @@ def _pins_hold() -> bool:
                                                  enable_gqa=True)[0].permute(1, 0, 2)
             if not np.allclose(mo[int(qs[s]):int(qs[s]) + ns], ref.numpy(), rtol=0,
                                atol=1e-9):
+                return False
+        # FP8: every code's value, the ties of the encoder, the write and the read
+        vals = oracle.e4m3_decode(ALL_CODES)
+        ref = torch_e4m3_values(ALL_CODES)
+        if not np.array_equal(vals[~np.isnan(ref)], ref[~np.isnan(ref)]):
+            return False
+        fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+        mids = ((fin[:-1] + fin[1:]) / 2).astype(np.float32)
+        mids = mids[np.abs(mids) < 464]
+        if not np.array_equal(oracle.e4m3_encode(mids), torch_e4m3_codes(mids)):
+            return False
+        fb = wl.with_fp8_pool(wl.random_batch(33, num_seqs=3, max_len=40, num_heads=4,
+                                              num_kv_heads=2, head_dim=64, dtype="bf16",
+                                              new_in_pool=True), seed=5)
+        ks, vs = fb.meta["k_scale"].numpy(), fb.meta["v_scale"].numpy()
+        kc, _, _ = oracle.reshape_and_cache_fp8(fb.k_new, fb.v_new, fb.k_cache, fb.v_cache,
+                                                fb.slot_mapping, "bf16", ks, vs)
+        sm = fb.slot_mapping
+        want = torch_e4m3_codes(np.clip(fb.k_new.float().numpy() / ks[None, :, None],
+                                        -448.0, 448.0))
+        got = kc.transpose(0, 2, 1, 3).reshape(-1, 2, 64)[sm]
+        if not np.array_equal(got, want):
+            return False
+        fo = oracle.decode(fb.q, fb.k_cache, fb.v_cache, fb.block_tables, fb.seq_lens,
+                           fb.scale, 2, "bf16", kv_scales=(ks, vs))
+        for s in range(fb.num_seqs):
+            if not np.allclose(fo[s], dequantised_sdpa(fb, s, ks, vs), rtol=0, atol=1e-9):
                 return False
     except ValueError:
         return False
