@@ -50,9 +50,10 @@ FALLBACK_HBM_GBS = 6800.0
 
 def decode_bytes(b) -> dict:
     es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
+    kv_es = 1 if b.meta.get("kv") == "e4m3" else es      # E4M3 caches: one byte
     L = b.seq_lens.astype(np.int64)
-    kv = int(L.sum()) * 2 * b.num_kv_heads * b.head_dim * es
-    kv_full = int(np.ceil(L / 16).sum()) * 16 * 2 * b.num_kv_heads * b.head_dim * es
+    kv = int(L.sum()) * 2 * b.num_kv_heads * b.head_dim * kv_es
+    kv_full = int(np.ceil(L / 16).sum()) * 16 * 2 * b.num_kv_heads * b.head_dim * kv_es
     qo = 2 * b.num_seqs * b.num_heads * b.head_dim * es
     tab = int(np.ceil(L / 16).sum()) * 4 + 4 * b.num_seqs
     return {"kv": kv, "kv_full_blocks": kv_full, "total": kv + qo + tab}
@@ -331,6 +332,7 @@ def gpu_arm(args, rank, world, device):
         result["long_context"] = long_context_arm(args, device, flush, pa)
         result["paging_overhead"] = paging_overhead_arm(args, device, flush, pa)
         result["multi_query"] = multi_query_arm(args, device, flush, pa)
+        result["fp8"] = fp8_arm(args, device, flush, pa)
     return result, b
 
 
@@ -428,6 +430,69 @@ def multi_query_arm(args, device, flush, pa):
                      "attn_tflops": nb["flops"] / t / 1e12, "bytes": nb}
         del b, out
         torch.cuda.empty_cache()
+    return res
+
+
+def fp8_arm(args, device, flush, pa):
+    """E4M3 caches: the serving-mix step (FP8 cache write of 256 tokens +
+    pa_decode_fp8) and the long-context split-KV decode over E4M3."""
+    peak, kind = measured_peak()
+    res = {}
+    b = wl.serving_mix_fp8(device=device, canary=False)
+    bt, sl, sm = b.torch_tables(device)
+    ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+    out = torch.empty_like(b.q)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(30)]
+    for _ in range(3):
+        pa.pa_reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache, b.v_cache, ks, vs, sm)
+        pa.pa_decode_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl, b.scale, b.num_kv_heads)
+    stream = torch.cuda.current_stream()
+    for e0, e1, e2 in ev:
+        flush()
+        e0.record(stream)
+        pa.pa_reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache, b.v_cache, ks, vs, sm)
+        e1.record(stream)
+        pa.pa_decode_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl, b.scale, b.num_kv_heads)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    dec = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev) * 1e-3
+    wr = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev) * 1e-3
+    step = statistics.mean(e0.elapsed_time(e2) for e0, _, e2 in ev) * 1e-3
+    nb = decode_bytes(b)
+    res["serving_mix_fp8"] = {
+        "workload": "serving_mix over an E4M3 cache (per-KV-head scales): step = "
+                    "pa_reshape_and_cache_fp8 of 256 tokens + pa_decode_fp8",
+        "seqs_per_s": b.num_seqs / step, "step_us": step * 1e6, "decode_us": dec * 1e6,
+        "cache_write_us": wr * 1e6, "kv_gbs": nb["kv"] / dec / 1e9,
+        "achieved_gbs": nb["total"] / dec / 1e9, "frac_of_peak": nb["total"] / dec / 1e9 / peak,
+        "peak_kind": kind, "bytes": nb}
+    del b, out
+    torch.cuda.empty_cache()
+
+    b = wl.long_context_fp8(device=device, canary=False)
+    bt, sl, _ = b.torch_tables(device)
+    ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+    msl = 131072
+    ws = torch.empty(pa.pa_decode_partitioned_workspace_size(b.num_seqs, b.num_heads,
+                                                             b.head_dim, msl, 512),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(b.q)
+
+    def call():
+        pa.pa_decode_partitioned_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl, b.scale,
+                                     b.num_kv_heads, 512, msl, ws)
+    for _ in range(3):
+        call()
+    t = statistics.mean(time_calls(call, 20, flush, stream)) * 1e-3
+    nb = decode_bytes(b)
+    res["long_context_fp8"] = {
+        "workload": "long_context over an E4M3 cache: batch 8, 64/8 x 128, seq_lens "
+                    "U[32768,131072], 512-token partitions (pa_decode_partitioned_fp8 + merge)",
+        "seqs_per_s": b.num_seqs / t, "us_per_call": t * 1e6, "kv_gbs": nb["kv"] / t / 1e9,
+        "achieved_gbs": nb["total"] / t / 1e9, "frac_of_peak": nb["total"] / t / 1e9 / peak,
+        "peak_kind": kind, "bytes": nb}
+    del b, ws, out
+    torch.cuda.empty_cache()
     return res
 
 
@@ -585,6 +650,30 @@ def single_kernel(args, device):
         def call():
             pa.pa_decode_partitioned(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale,
                                      b.num_kv_heads, 512, msl, ws)
+    elif args.only in ("decode_fp8", "cache_write_fp8"):
+        b = wl.serving_mix_fp8(device=device, canary=False)
+        bt, sl, sm = b.torch_tables(device)
+        ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+        out = torch.empty_like(b.q)
+        if args.only == "decode_fp8":
+            def call():
+                pa.pa_decode_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl, b.scale,
+                                 b.num_kv_heads)
+        else:
+            def call():
+                pa.pa_reshape_and_cache_fp8(b.k_new, b.v_new, b.k_cache, b.v_cache, ks, vs, sm)
+    elif args.only == "partitioned_fp8":
+        b = wl.long_context_fp8(device=device, canary=False)
+        bt, sl, _ = b.torch_tables(device)
+        ks, vs = b.meta["k_scale"], b.meta["v_scale"]
+        msl = 131072
+        ws = torch.empty(pa.pa_decode_partitioned_workspace_size(
+            b.num_seqs, b.num_heads, b.head_dim, msl, 512), dtype=torch.uint8, device=device)
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode_partitioned_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl,
+                                         b.scale, b.num_kv_heads, 512, msl, ws)
     elif args.only in ("multi_spec", "multi_prefill"):
         b = (wl.spec_verify if args.only == "multi_spec" else wl.chunked_prefill_mix)(
             device=device, canary=False)
@@ -630,10 +719,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="approximate seconds of oracle work for the reference arm")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the long-context, paging-overhead and multi-query measurements")
+                    help="skip the long-context, paging-overhead, multi-query and FP8 "
+                         "measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["decode", "partitioned", "cache_write", "multi_spec",
-                                       "multi_prefill"],
+                                       "multi_prefill", "decode_fp8", "cache_write_fp8",
+                                       "partitioned_fp8"],
                     help="launch one kernel alone (for profiling); prints timings only")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -14,6 +14,8 @@
  *   pa_decode_multi        several new query tokens per sequence (a
  *                          prompt chunk or speculative positions), causal
  *                          among themselves, over the same paged cache
+ *   *_fp8                  the cache write, decode and split-KV decode
+ *                          over an FP8 (E4M3) cache with per-KV-head scales
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -75,7 +77,8 @@ extern "C" {
 typedef enum {
     PA_F32 = 0,
     PA_BF16 = 1,
-    PA_F16 = 2
+    PA_F16 = 2,
+    PA_E4M3 = 3      /* FP8 E4M3 cache storage (the *_fp8 entry points only) */
 } pa_dtype;
 
 typedef enum {
@@ -249,6 +252,69 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache,
                     int64_t num_blocks, int32_t block_size,
                     int32_t max_blocks_per_seq, int64_t q_row_stride,
                     float scale, int32_t dtype, void *stream);
+
+/*
+ * FP8 KV cache.
+ *
+ * Defined in "vLLM: Architecture, PagedAttention & Internals", *The knobs
+ * that actually matter*, item 5 (an FP8 KV cache enlarges the effective pool)
+ * and "vLLM: High-Throughput Serving with PagedAttention", *The benefits of
+ * vLLM* (quantized KV cache); the pages fix no format.  This library stores
+ * OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 fraction bits;
+ * largest finite 448; S.1111.111 is NaN) in the same layout
+ * [num_blocks, num_kv_heads, 16, head_dim] (one byte per element), with one
+ * float scale per KV head for K and one for V: code c of KV head j stands for
+ * value(c) * k_scale[j] (or v_scale[j]).  Scales are device arrays float32
+ * [num_kv_heads] owned by the caller; a per-tensor scale is the case where
+ * all entries are equal.  Scales must be positive and finite (others are
+ * not checked; they make the results meaningless, never unsafe).
+ *
+ * pa_reshape_and_cache_fp8 -- the cache write of pa_reshape_and_cache, with
+ * each element x of KV head j stored as E4M3(x / scale_j): the quotient is
+ * rounded to binary32 (IEEE division), then to E4M3 with round to nearest,
+ * ties to even; finite magnitudes above 448 and infinities saturate to
+ * +-448, NaN stays NaN.  k and v are in `dtype` (PA_F32, PA_BF16, PA_F16),
+ * 16-byte aligned with token strides whose byte size is a multiple of 16;
+ * head_dim a multiple of 16; k_cache and v_cache 16-byte aligned.
+ */
+int pa_reshape_and_cache_fp8(const void *k, const void *v, void *k_cache,
+                             void *v_cache, const float *k_scale,
+                             const float *v_scale, const int64_t *slot_mapping,
+                             int64_t num_tokens, int32_t num_kv_heads,
+                             int32_t head_dim, int64_t k_token_stride,
+                             int64_t v_token_stride, int64_t num_blocks,
+                             int32_t block_size, int32_t dtype, void *stream);
+
+/*
+ * pa_decode_fp8 / pa_decode_partitioned_fp8 -- pa_decode and
+ * pa_decode_partitioned over E4M3 caches: K_s[t] = value(code) * k_scale[j]
+ * and V_s[t] = value(code) * v_scale[j] for KV head j, the attention itself
+ * unchanged.  `dtype` is the type of q and out: PA_BF16 or PA_F16 (q is
+ * rounded to f16 for the tensor cores, so its entries must lie within the
+ * f16 range, |q| < 65504).  The partitioned form takes the workspace of
+ * pa_decode_partitioned_workspace_size and writes the same statistics.
+ * Other requirements as pa_decode, plus q and out 16-byte aligned with a q
+ * stride whose byte size is a multiple of 16.
+ */
+int pa_decode_fp8(void *out, const void *q, const void *k_cache,
+                  const void *v_cache, const float *k_scale, const float *v_scale,
+                  const int32_t *block_tables, const int32_t *seq_lens,
+                  int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                  int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                  int32_t max_blocks_per_seq, int64_t q_seq_stride, float scale,
+                  int32_t dtype, void *stream);
+
+int pa_decode_partitioned_fp8(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, const float *k_scale,
+                              const float *v_scale, const int32_t *block_tables,
+                              const int32_t *seq_lens, int32_t num_seqs,
+                              int32_t num_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int64_t num_blocks,
+                              int32_t block_size, int32_t max_blocks_per_seq,
+                              int64_t q_seq_stride, float scale, int32_t dtype,
+                              int32_t partition_size, int32_t max_seq_len,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
 
 /*
  * pa_decode_partitioned_noalloc -- pa_decode_partitioned without a caller

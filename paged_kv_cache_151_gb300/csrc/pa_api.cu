@@ -115,33 +115,39 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A 16-bit cache [num_blocks][H_kv][16][D] as the 3-D tensor
-// (D, 16 rows, num_blocks*H_kv), read in boxes of 128 bytes x 16 rows with
-// the 128-byte swizzle.
+// A cache [num_blocks][H_kv][16][D] as the 3-D tensor (D, 16 rows,
+// num_blocks*H_kv).  16-bit caches are read in boxes of 64 elements (128
+// bytes) x 16 rows with the 128-byte swizzle; E4M3 caches in boxes of the
+// whole row (D bytes) x 16 rows with the D-byte swizzle.
 bool encode_cache_map(CUtensorMap *m, const void *base, int64_t num_blocks, int32_t hkv,
-                      int32_t head_dim, int32_t dtype) {
+                      int32_t head_dim, int32_t kv_dtype) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
+    const bool f8 = kv_dtype == PA_E4M3;
+    const cuuint64_t es = f8 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, 16, (cuuint64_t)(num_blocks * hkv)};
-    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * 2 * 16};
-    const cuuint32_t box[3] = {64, 16, 1};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * es, (cuuint64_t)head_dim * es * 16};
+    const cuuint32_t box[3] = {f8 ? (cuuint32_t)head_dim : 64u, 16, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = (f8 && head_dim == 64) ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                         : CU_TENSOR_MAP_SWIZZLE_128B;
     return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Fill the tensor maps the persistent kernel needs for 16-bit caches.
-bool prepare_maps(pa::DecodeParams &p, int32_t dtype, int32_t head_dim) {
-    if (dtype == PA_F32) return true;
+// Fill the tensor maps the persistent kernel needs for 16-bit and E4M3
+// caches (kv_dtype: the caches' storage type).
+bool prepare_maps(pa::DecodeParams &p, int32_t kv_dtype, int32_t head_dim) {
+    if (kv_dtype == PA_F32) return true;
     if (p.num_blocks <= 0) return true;            // nothing can be read
     return encode_cache_map(&p.tmap_k, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
-                            dtype) &&
+                            kv_dtype) &&
            encode_cache_map(&p.tmap_v, p.v_cache, p.num_blocks, p.num_kv_heads, head_dim,
-                            dtype);
+                            kv_dtype);
 }
 
 // The persistent kernel reads each query row with 16-byte loads.
@@ -400,6 +406,144 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
                         : pa::decode_multi_f16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st);
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// ---- FP8 (E4M3) KV cache --------------------------------------------------
+
+int pa_reshape_and_cache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int64_t k_token_stride,
+                             int64_t v_token_stride, int64_t num_blocks, int32_t block_size,
+                             int32_t dtype, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    const int es = elem_size(dtype);
+    if (es == 0) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16) return PA_ERR_UNSUPPORTED;
+    if (head_dim % 16) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+        return PA_ERR_INVALID_ARG;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (k_token_stride < row || v_token_stride < row) return PA_ERR_INVALID_ARG;
+    // 8 source elements per thread, read with 16-byte loads
+    if (!aligned16(k) || !aligned16(v) || (k_token_stride * es) % 16 ||
+        (v_token_stride * es) % 16 || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    cudaError_t e = pa::reshape_and_cache_fp8(
+        k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+        k_token_stride, v_token_stride, num_blocks * block_size, dtype, k_scale, v_scale,
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared by the FP8 decode entry points: checks, parameters, launch of the
+// persistent kernel (and, for partitions, the merge).
+int decode_fp8_common(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const float *k_scale, const float *v_scale,
+                      const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                      int64_t q_seq_stride, float scale, int32_t dtype, bool partial,
+                      int32_t partition_size, int32_t max_seq_len, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_seq_stride, scale, dtype);
+    if (rc != PA_OK) return rc;
+    if (partial && (partition_size <= 0 || partition_size % 16 || max_seq_len < 0))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (dtype != PA_BF16 && dtype != PA_F16) return PA_ERR_UNSUPPORTED;
+    if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+    if (!q_rows_aligned(q, q_seq_stride, dtype) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.k_scale = k_scale; p.v_scale = v_scale;
+    p.block_tables = block_tables; p.seq_lens = seq_lens;
+    p.num_blocks = num_blocks; p.q_seq_stride = q_seq_stride;
+    p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.scale_log2 = scale * pa::LOG2E;
+    long long unit_bound = (long long)num_seqs * num_kv_heads;
+    int P = 1;
+    WorkspaceLayout w{};
+    if (partial) {
+        if (!workspace_layout(num_seqs, num_heads, head_dim, max_seq_len, partition_size, &w))
+            return PA_ERR_INVALID_ARG;
+        if (!workspace || workspace_bytes < w.total ||
+            (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+            return PA_ERR_WORKSPACE;
+        const int64_t P64 = ((int64_t)max_seq_len + partition_size - 1) / partition_size;
+        if (P64 > INT32_MAX) return PA_ERR_UNSUPPORTED;
+        P = (int)(P64 > 0 ? P64 : 1);
+        unsigned char *ws = static_cast<unsigned char *>(workspace);
+        p.part_o = reinterpret_cast<float *>(ws + w.o);
+        p.part_m = reinterpret_cast<float *>(ws + w.m);
+        p.part_l = reinterpret_cast<float *>(ws + w.l);
+        p.partition_blocks = partition_size / 16;
+        p.max_parts = P;
+        p.max_seq_len = max_seq_len;
+        unit_bound *= P;
+    }
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    if (!prepare_maps(p, PA_E4M3, head_dim)) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int G = num_heads / num_kv_heads;
+    const int cluster = partial ? 1 : PA_DECODE_CLUSTER;
+    cudaError_t e = dtype == PA_BF16
+                        ? pa::decode_fp8_bf16(p, head_dim, G, partial, unit_bound, cluster, st)
+                        : pa::decode_fp8_f16(p, head_dim, G, partial, unit_bound, cluster, st);
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (!partial) return PA_OK;
+    pa::MergeParams mp;
+    mp.out = out;
+    mp.part_o = p.part_o; mp.part_m = p.part_m; mp.part_l = p.part_l;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads; mp.head_dim = head_dim;
+    mp.max_parts = P; mp.partition_size = partition_size;
+    const int64_t cap = (int64_t)max_blocks_per_seq * 16;
+    mp.seq_cap = (int)(max_seq_len < cap ? max_seq_len : cap);
+    e = run_merge(mp, dtype, num_seqs, st);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                  const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                  const int32_t *seq_lens, int32_t num_seqs, int32_t num_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                  int32_t block_size, int32_t max_blocks_per_seq, int64_t q_seq_stride,
+                  float scale, int32_t dtype, void *stream) {
+    return decode_fp8_common(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                             seq_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
+                             block_size, max_blocks_per_seq, q_seq_stride, scale, dtype,
+                             false, 0, 0, nullptr, 0, stream);
+}
+
+int pa_decode_partitioned_fp8(void *out, const void *q, const void *k_cache,
+                              const void *v_cache, const float *k_scale,
+                              const float *v_scale, const int32_t *block_tables,
+                              const int32_t *seq_lens, int32_t num_seqs, int32_t num_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                              int32_t block_size, int32_t max_blocks_per_seq,
+                              int64_t q_seq_stride, float scale, int32_t dtype,
+                              int32_t partition_size, int32_t max_seq_len, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return decode_fp8_common(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                             seq_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks,
+                             block_size, max_blocks_per_seq, q_seq_stride, scale, dtype, true,
+                             partition_size, max_seq_len, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

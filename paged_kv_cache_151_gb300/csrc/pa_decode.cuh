@@ -69,11 +69,13 @@ struct DecodeParams {
     const int32_t *query_start;  // multi-token queries: [num_seqs + 1] row offsets
     int max_query_len;        // multi-token queries: bound on a sequence's rows
     int num_q_rows;           // multi-token queries: rows of q and out
+    const float *k_scale;     // E4M3 caches: [num_kv_heads] dequantisation scales
+    const float *v_scale;
     float scale_log2;         // scale * log2(e)
     unsigned int *err;        // device error word
-    // 16-bit caches, persistent kernel: the caches as 3-D tensors
+    // 16-bit and E4M3 caches, persistent kernel: the caches as 3-D tensors
     // [num_blocks*num_kv_heads][16 rows][head_dim], read in swizzled boxes
-    // of 16 rows x 128 bytes
+    // of 16 rows x 128 bytes (16-bit) or 16 rows x head_dim bytes (E4M3)
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
 };

@@ -1,0 +1,15 @@
+// pa_fp8_bf16.cu -- persistent decode kernels over E4M3 caches (whole sequences
+// and split-KV partitions), bf16 queries and outputs.
+#include "pa_internal.h"
+#include "pa_persistent.cuh"
+
+namespace pa {
+
+cudaError_t decode_fp8_bf16(const DecodeParams &p, int D, int G, bool partial,
+                          long long unit_bound, int cluster, cudaStream_t st) {
+    return partial
+               ? dispatch_persistent<__nv_bfloat16, MODE_PARTITIONED, e4m3>(p, D, G, unit_bound, cluster, st)
+               : dispatch_persistent<__nv_bfloat16, MODE_DECODE, e4m3>(p, D, G, unit_bound, cluster, st);
+}
+
+}  // namespace pa

@@ -42,6 +42,20 @@ cudaError_t reshape_and_cache(const void *k, const void *v, void *k_cache, void 
                               int64_t v_tok_stride_bytes, int64_t num_slots,
                               cudaStream_t st);
 
+// FP8 (E4M3) cache write; src_dtype 0 f32, 1 bf16, 2 f16; strides in elements
+cudaError_t reshape_and_cache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,
+                                  const int64_t *slot_mapping, int64_t num_tokens,
+                                  int num_kv_heads, int head_dim, int64_t k_tok_stride,
+                                  int64_t v_tok_stride, int64_t num_slots, int src_dtype,
+                                  const float *k_scale, const float *v_scale,
+                                  cudaStream_t st);
+
+// persistent decode over E4M3 caches (q and out bf16 / f16); partial as above
+cudaError_t decode_fp8_bf16(const DecodeParams &p, int D, int G, bool partial,
+                            long long unit_bound, int cluster, cudaStream_t st);
+cudaError_t decode_fp8_f16(const DecodeParams &p, int D, int G, bool partial,
+                           long long unit_bound, int cluster, cudaStream_t st);
+
 // device error word
 cudaError_t device_error_ptr(unsigned int **out);
 cudaError_t read_device_error(unsigned int *flags, bool clear);

@@ -40,6 +40,7 @@
 
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
+#include "pa_fp8.cuh"
 #include "pa_math.cuh"
 #include "pa_mma.cuh"
 
@@ -58,13 +59,14 @@ struct UnitRec {
     int q0, nq;                   // multi: first query row of the sequence, its count
 };
 
-template <typename T, int D, int G, int NW, int S, int MODE>
+// Shared-memory layout; KV is the cache's storage type (T itself, or E4M3).
+template <typename T, typename KV, int D, int G, int NW, int S, int MODE>
 struct PersistentLayout {
     static constexpr bool PARTIAL = MODE == MODE_PARTITIONED;
     static constexpr int ROWS = rows_of_mode(MODE, G);
-    using Sh = Shape<T, D>;
+    static constexpr size_t TILE_BYTES = (size_t)16 * D * sizeof(KV);
     static constexpr int NU_MAX = 128;                    // units per cluster
-    static constexpr size_t STAGES = (size_t)NW * S * 2 * Sh::TILE_BYTES;
+    static constexpr size_t STAGES = (size_t)NW * S * 2 * TILE_BYTES;
     // one partial: O[ROWS][D], M[ROWS], L[ROWS], padded to 16 bytes
     static constexpr size_t PART_FLOATS = ((size_t)ROWS * D + 2 * ROWS + 3) / 4 * 4;
     static constexpr size_t OFF_BARS = STAGES;
@@ -77,7 +79,7 @@ struct PersistentLayout {
     static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
     static constexpr size_t BYTES = OFF_CTL + 256 + 1024;   // + alignment of the base
     static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
-    static_assert(S == 0 || (size_t)S * 2 * Sh::TILE_BYTES >= PART_FLOATS * 4,
+    static_assert(S == 0 || (size_t)S * 2 * TILE_BYTES >= PART_FLOATS * 4,
                   "a warp's stages must hold one partial");
     static_assert(OFF_SCR % 16 == 0 && OFF_PARTS % 16 == 0 && OFF_UNITS % 16 == 0 &&
                       OFF_CTL % 16 == 0 && PART_FLOATS % 4 == 0,
@@ -246,20 +248,27 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 #define PA_UNIT_COST_Q4 4
 #endif
 
-template <typename T, int D, int G, int NW, int S, int MODE>
+// T: the type of q and out; KV: the caches' storage (T, or E4M3 codes with
+// per-KV-head scales, 16-bit T only).
+template <typename T, typename KV, int D, int G, int NW, int S, int MODE>
 __global__ void __launch_bounds__(NW * 32)
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr bool TC = use_tc<T>();
+    constexpr bool F8 = std::is_same<KV, e4m3>::value;
     constexpr bool PARTIAL = MODE == MODE_PARTITIONED;
     constexpr bool MQ = MODE == MODE_MULTI;
     constexpr int ROWS = rows_of_mode(MODE, G);
     static_assert(!MQ || TC, "multi-token queries use the tensor-core path");
-    using W = std::conditional_t<MQ, WarpAttnTC16<T, D>,
-                                 std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>>;
-    using Lay = PersistentLayout<T, D, G, NW, S, MODE>;
-    using Sh = Shape<T, D>;
+    static_assert(F8 || std::is_same<KV, T>::value, "cache type");
+    static_assert(!F8 || (TC && !MQ), "E4M3 caches: 16-bit q, one query token per sequence");
+    using W = std::conditional_t<
+        F8, WarpAttnF8<T, D, G>,
+        std::conditional_t<MQ, WarpAttnTC16<T, D>,
+                           std::conditional_t<TC, WarpAttnTC<T, D, G>, WarpAttn<T, D, G>>>>;
+    using Lay = PersistentLayout<T, KV, D, G, NW, S, MODE>;
+    using Sh = Shape<T, D>;                        // chunks of q / out
     constexpr int E = Sh::E;
-    constexpr int ROWB = Sh::ROW_BYTES, TILE = Sh::TILE_BYTES;
+    constexpr int ROWB = D * (int)sizeof(KV), TILE = 16 * ROWB;   // cache rows and tiles
     constexpr int NT = NW * 32;
     constexpr int NU_MAX = Lay::NU_MAX;
     constexpr int WS = warp_scratch_floats<G>();
@@ -539,7 +548,13 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             return;
         }
         unsigned char *dst = my_stages + (size_t)(k % S) * 2 * TILE;
-        if constexpr (TC) {
+        if constexpr (F8) {
+            // whole 16-row tiles, one box of 16 rows x D bytes each
+            const int z = pbk * Hkv + units[ui].j;
+            mbar_arrive_expect_tx(bar, 2 * TILE);
+            tma_load_3d(dst, &p.tmap_k, 0, 0, z, bar, pol);
+            tma_load_3d(dst + TILE, &p.tmap_v, 0, 0, z, bar, pol);
+        } else if constexpr (TC) {
             // whole 16-row tiles, D/64 boxes each for K and V
             const int z = pbk * Hkv + units[ui].j;
             mbar_arrive_expect_tx(bar, 2 * TILE);
@@ -582,6 +597,12 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                           : reinterpret_cast<float *>(stages + (size_t)(g % NW) * S * 2 * TILE);
     };
 
+    // V's dequantisation scale of unit u (E4M3 caches), applied to results
+    auto v_scale_of = [&](const UnitRec &u) -> float {
+        if constexpr (F8) return __ldg(p.v_scale + u.j);
+        else return 1.f;
+    };
+
     // Output row (in units of D) of row r of unit u's query tile; -1 if the
     // tile's row is past the sequence's query rows.
     auto out_row = [&](const UnitRec &u, int r) -> long long {
@@ -596,7 +617,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
 
     // Write the result of unit u from a merged (M, L, O) of chunk (g, d0).
     auto emit = [&](const UnitRec &u, int g, int d0, float M, float Ls, float *O) {
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float inv = Ls > 0.f ? v_scale_of(u) / Ls : 0.f;
         if constexpr (PARTIAL) {
             const long long row = ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
             float *po = p.part_o + row * D + d0;
@@ -625,8 +646,11 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         const bool from_before = u_lo < my_lo, to_after = u_hi > my_hi;
         if (!from_before && !to_after) {
             // a unit only this warp touched: write its result from registers
+            const float vsc = v_scale_of(u);
             wa.for_each_result([&](int g, int d, float v0, float v1, bool first, float m,
                                    float l) {
+                v0 *= vsc;
+                v1 *= vsc;
                 if constexpr (PARTIAL) {
                     const long long row =
                         ((long long)u.s * H + u.j * G + g) * p.max_parts + u.part;
@@ -702,6 +726,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     };
 
     int cur = -1, qnext = -1;                      // unit whose query is loaded ahead
+    float unit_scale = p.scale_log2;               // score scale (x K's scale for E4M3)
     int k_done = 0;
     bool ok = true;
     for (int k = 0; k < n_mine; ++k) {
@@ -737,6 +762,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                 if (qnext != ui) wa.prefetch_q(qptr(ui));
                 if constexpr (TC) wa.take_q();
                 else wa.take_q(p.scale_log2);
+                if constexpr (F8) unit_scale = p.scale_log2 * __ldg(p.k_scale + units[ui].j);
                 // load the next unit's query while this one streams
                 qnext = -1;
                 if (ui + 1 < nu && cum[ui + 1] < my_hi && units[ui + 1].nb > 0) {
@@ -754,14 +780,15 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             const int rows = rows_of(k, ui);
             if constexpr (TC) {
                 if (rows < 16) {                   // tail rows hold other tokens' data
-                    WarpAttnTC<T, D, G>::zero_rows(Kt + TILE, rows, lane);
+                    if constexpr (F8) W::zero_rows(Kt + TILE, rows, lane);
+                    else WarpAttnTC<T, D, G>::zero_rows(Kt + TILE, rows, lane);
                     // these generic writes must be ordered before the next
                     // bulk copy into the stage
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 if constexpr (MQ) wa.block(smem_u32(Kt), smem_u32(Kt + TILE), pos_of(k, ui), p.scale_log2);
-                else wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, p.scale_log2);
+                else wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, unit_scale);
             } else {
                 wa.block(Kt, Kt + TILE, rows, Sc, Pb, Al);
             }
@@ -794,39 +821,39 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
 #ifndef PA_STAGE_KB
 #define PA_STAGE_KB 16
 #endif
-template <typename T, int D, int G, int MODE>
+template <typename T, typename KV, int D, int G, int MODE>
 __host__ __device__ constexpr int persistent_stages() {
-    int s = PA_STAGE_KB * 1024 / (2 * Shape<T, D>::TILE_BYTES);
+    int s = PA_STAGE_KB * 1024 / (int)(2 * 16 * D * sizeof(KV));
     s = s < 2 ? 2 : (s > 6 ? 6 : s);
-    while (s > 2 && PersistentLayout<T, D, G, 4, 0, MODE>::BYTES +
-                            (size_t)4 * s * (2 * Shape<T, D>::TILE_BYTES + 8) > 113 * 1024)
+    while (s > 2 && PersistentLayout<T, KV, D, G, 4, 0, MODE>::BYTES +
+                            (size_t)4 * s * (2 * 16 * D * sizeof(KV) + 8) > 113 * 1024)
         --s;
     return s;
 }
 
-template <typename T, int D, int G, int MODE>
+template <typename T, typename KV, int D, int G, int MODE>
 struct PersistentConfig {
     static constexpr int NW = 4;
-    static constexpr int S = persistent_stages<T, D, G, MODE>();
-    using Lay = PersistentLayout<T, D, G, NW, S, MODE>;
+    static constexpr int S = persistent_stages<T, KV, D, G, MODE>();
+    using Lay = PersistentLayout<T, KV, D, G, NW, S, MODE>;
 };
 
 // Largest num_seqs the persistent kernel sorts in shared memory.
-template <typename T, int D, int G, int MODE>
+template <typename T, typename KV, int D, int G, int MODE>
 constexpr int persistent_max_seqs() {
-    return PersistentConfig<T, D, G, MODE>::Lay::MAX_SEQS;
+    return PersistentConfig<T, KV, D, G, MODE>::Lay::MAX_SEQS;
 }
 
 // Clusters of `cluster` blocks, as many as fit on the GPU at once (looked up
 // once per device and cluster size), but at least enough that no cluster
 // gets more than NU_MAX units.
-template <typename T, int D, int G, int MODE>
+template <typename T, typename KV, int D, int G, int MODE>
 cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int cluster,
                               cudaStream_t st) {
-    using C = PersistentConfig<T, D, G, MODE>;
+    using C = PersistentConfig<T, KV, D, G, MODE>;
     constexpr size_t smem = C::Lay::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory");
-    auto kern = decode_persistent_kernel<T, D, G, C::NW, C::S, MODE>;
+    auto kern = decode_persistent_kernel<T, KV, D, G, C::NW, C::S, MODE>;
     if (p.num_seqs > C::Lay::MAX_SEQS) return cudaErrorNotSupported;
     if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
     static int fitted[64][4];                      // clusters resident per device, per size
@@ -868,11 +895,11 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
 }
 
 // Launch mode MODE for the built shapes: D in {64, 128}, G in {1, 2, 4, 8}.
-template <typename T, int MODE>
+template <typename T, int MODE, typename KV = T>
 cudaError_t dispatch_persistent(const DecodeParams &p, int D, int G, long long unit_bound,
                                 int cluster, cudaStream_t st) {
 #define PA_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_persistent<T, DD, GG, MODE>(p, unit_bound, cluster, st);
+    if (D == DD && G == GG) return launch_persistent<T, KV, DD, GG, MODE>(p, unit_bound, cluster, st);
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
 #undef PA_CASE

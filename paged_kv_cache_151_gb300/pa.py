@@ -20,7 +20,7 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
-PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_F32, PA_BF16, PA_F16, PA_E4M3 = 0, 1, 2, 3
 _DTYPE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
 
 PA_DEVERR_BLOCK_ID = 0x1
@@ -72,6 +72,14 @@ def load():
         lib.pa_decode_multi.restype = ctypes.c_int
         lib.pa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                         i64, i32, i32, i64, f32, i32, P]
+        lib.pa_reshape_and_cache_fp8.restype = ctypes.c_int
+        lib.pa_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i64, i64,
+                                                 i64, i32, i32, P]
+        dec8 = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i64, i32, i32, i64, f32, i32]
+        lib.pa_decode_fp8.restype = ctypes.c_int
+        lib.pa_decode_fp8.argtypes = dec8 + [P]
+        lib.pa_decode_partitioned_fp8.restype = ctypes.c_int
+        lib.pa_decode_partitioned_fp8.argtypes = dec8 + [i32, i32, P, sz, P]
         lib.pa_device_error.restype = ctypes.c_int
         lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         _lib = lib
@@ -259,6 +267,100 @@ def pa_decode_multi(out, q, k_cache, v_cache, block_tables, seq_lens, query_star
     _check("pa_decode_multi", rc)
 
 
+# ---- FP8 (E4M3) cache ------------------------------------------------------
+
+_FP8_TYPES = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t)
+
+
+def _fp8_cache_dims(k_cache, v_cache, k_scale, v_scale):
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_scale", k_scale),
+                 ("v_scale", v_scale)):
+        _dev(t, n)
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("caches must both be [num_blocks, num_kv_heads, block_size, head_dim]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    if k_cache.dtype not in _FP8_TYPES or v_cache.dtype not in _FP8_TYPES:
+        raise ValueError("FP8 caches hold E4M3 codes (uint8 or float8_e4m3fn tensors)")
+    Hkv = k_cache.shape[1]
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or t.shape != (Hkv,) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 [num_kv_heads]")
+    return k_cache.shape
+
+
+def pa_reshape_and_cache_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                             stream=None):
+    """Write k[t], v[t] ([T, H_kv, D] in f32/bf16/f16) into E4M3 caches as
+    E4M3(x / scale[j])."""
+    for n, t in (("k", k), ("v", v), ("slot_mapping", slot_mapping)):
+        _dev(t, n)
+    N, Hkv, bs, D = _fp8_cache_dims(k_cache, v_cache, k_scale, v_scale)
+    if k.dim() != 3 or k.shape != v.shape or tuple(k.shape[1:]) != (Hkv, D):
+        raise ValueError("k and v must be [num_tokens, num_kv_heads, head_dim]")
+    if k.dtype not in _DTYPE or v.dtype != k.dtype:
+        raise ValueError("k and v must share a dtype in {float32, bfloat16, float16}")
+    if k.stride(2) != 1 or k.stride(1) != D or v.stride(2) != 1 or v.stride(1) != D:
+        raise ValueError("k and v must have contiguous heads")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.dim() != 1 or \
+            slot_mapping.shape[0] != k.shape[0] or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 [num_tokens]")
+    rc = load().pa_reshape_and_cache_fp8(
+        k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        k_scale.data_ptr(), v_scale.data_ptr(), slot_mapping.data_ptr(), k.shape[0], Hkv, D,
+        k.stride(0), v.stride(0), N, bs, _DTYPE[k.dtype], _stream(stream))
+    _check("pa_reshape_and_cache_fp8", rc)
+
+
+def _decode_fp8_args(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens):
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables),
+                 ("seq_lens", seq_lens)):
+        _dev(t, n)
+    N, Hkv, bs, D = _fp8_cache_dims(k_cache, v_cache, k_scale, v_scale)
+    if q.dim() != 3 or q.shape[2] != D or q.stride(2) != 1 or q.stride(1) != D:
+        raise ValueError("q must be [num_seqs, num_heads, head_dim] with contiguous heads")
+    if out.shape != q.shape or not out.is_contiguous() or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be bfloat16 or float16")
+    B, H = q.shape[0], q.shape[1]
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != B or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks]")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,) or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 [num_seqs]")
+    return [out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+            k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+            seq_lens.data_ptr(), B, H, Hkv, D, N, bs, block_tables.shape[1], q.stride(0)]
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                  scale, num_kv_heads, stream=None):
+    """Decode-step paged attention over E4M3 caches into ``out``."""
+    args = _decode_fp8_args(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                            seq_lens)
+    if num_kv_heads != k_cache.shape[1]:
+        raise ValueError("num_kv_heads does not match the cache")
+    rc = load().pa_decode_fp8(*args, float(scale), _DTYPE[q.dtype], _stream(stream))
+    _check("pa_decode_fp8", rc)
+
+
+def pa_decode_partitioned_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                              seq_lens, scale, num_kv_heads, partition_size, max_seq_len,
+                              workspace, stream=None):
+    """Split-KV decode over E4M3 caches (workspace as pa_decode_partitioned)."""
+    args = _decode_fp8_args(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                            seq_lens)
+    if num_kv_heads != k_cache.shape[1]:
+        raise ValueError("num_kv_heads does not match the cache")
+    _dev(workspace, "workspace")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load().pa_decode_partitioned_fp8(*args, float(scale), _DTYPE[q.dtype],
+                                          int(partition_size), int(max_seq_len),
+                                          workspace.data_ptr(), nbytes, _stream(stream))
+    _check("pa_decode_partitioned_fp8", rc)
+
+
 def workspace_views(workspace, num_seqs, num_heads, head_dim, max_seq_len, partition_size):
     """(o_part, m_part, l_part) fp32 views of a partitioned-decode workspace,
     following the layout documented in include/pa.h."""
@@ -288,6 +390,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_partitioned_workspace_size", "pa_decode_partitioned", "pa_decode_multi",
     "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",
+    "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_partitioned_fp8",
     "pa_device_error", "workspace_views",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SEQ_LEN", "PA_DEVERR_SLOT", "PA_DEVERR_TIMEOUT",
 ]

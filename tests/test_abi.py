@@ -129,3 +129,33 @@ def test_multi_query_host_checks(lib):
     assert _multi_status(lib, num_seqs=0) == 0                 # nothing to do
     assert _multi_status(lib, num_q_rows=0) == 0
     assert _multi_status(lib, max_query_len=0) == 0            # no rows can exist
+
+
+def test_fp8_host_checks(lib):
+    P = 16
+    # cache write: bad head_dim, unaligned source, null scale, zero tokens
+    args = [P, P, P, P, P, P, P, 4, 2, 64, 128, 128, 10, 16, 1, None]
+    a = list(args); a[9] = 40
+    assert lib.pa_reshape_and_cache_fp8(*a) == -2              # head_dim not x16
+    a = list(args); a[0] = 8
+    assert lib.pa_reshape_and_cache_fp8(*a) == -1              # k not 16-byte aligned
+    a = list(args); a[4] = None
+    assert lib.pa_reshape_and_cache_fp8(*a) == -1              # no k_scale
+    a = list(args); a[7] = 0
+    assert lib.pa_reshape_and_cache_fp8(*a) == 0               # nothing to do
+    a = list(args); a[14] = 7
+    assert lib.pa_reshape_and_cache_fp8(*a) == -2              # source dtype
+    # decode: fp32 q unsupported, null scales, zero sequences
+    dec = [P, P, P, P, P, P, P, P, 4, 8, 2, 64, 10, 16, 4, 512, 0.125, 1, None]
+    a = list(dec); a[17] = 0
+    assert lib.pa_decode_fp8(*a) == -2                         # q in fp32
+    a = list(dec); a[4] = None
+    assert lib.pa_decode_fp8(*a) == -1
+    a = list(dec); a[8] = 0
+    assert lib.pa_decode_fp8(*a) == 0
+    part = dec[:-1] + [100, 64, ctypes.c_void_p(256), 1 << 20, None]
+    assert lib.pa_decode_partitioned_fp8(*part) == -1          # partition not x16
+    part = dec[:-1] + [512, 64, ctypes.c_void_p(256), 16, None]
+    assert lib.pa_decode_partitioned_fp8(*part) == -3          # workspace too small
+    # the 16-bit entry points do not take E4M3 as a dtype
+    assert _decode_status(lib, dtype=3) == -2
