@@ -21,6 +21,8 @@ fp64 numpy arrays.  The arithmetic is documented in ``pa_ref.c``:
   their log-sum-exp merge.
 * ``kv_bytes_per_token`` / ``bytes_per_block`` / ``blocks_for_tokens`` --
   the pages' KV sizing arithmetic.
+* ``copy_blocks`` -- the block copies of copy-on-write ("vLLM: Architecture,
+  PagedAttention & Internals", *Copy-on-write for shared blocks*).
 * ``e4m3_encode`` / ``e4m3_decode`` / ``reshape_and_cache_fp8`` and the
   ``kv_scales=`` form of ``decode`` / ``decode_one`` -- the FP8 (E4M3) KV
   cache with one scale per KV head for K and for V.
@@ -92,6 +94,8 @@ def bind(path: str):
     lib.pa_ref_decode_fp8.argtypes = [P] + common + [P, P, i32]
     lib.pa_ref_decode_one_fp8.restype = ctypes.c_int
     lib.pa_ref_decode_one_fp8.argtypes = [P, P, i64, i32] + common + [P, P]
+    lib.pa_ref_copy_blocks.restype = i64
+    lib.pa_ref_copy_blocks.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32, P, i64, i64, i64]
     lib.pa_ref_lse_merge.restype = None
     lib.pa_ref_lse_merge.argtypes = [P, P, P, P, i64, i32]
     return lib
@@ -204,6 +208,26 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, dtype: str):
                                        Hkv, D, Hkv * D, Hkv * D, bs, N,
                                        REF_DTYPE[dtype])
     return kc, vc, int(bad)
+
+
+def copy_blocks(caches, block_mapping):
+    """Copy-on-write block copies: return (copies of the caches, n_bad).
+    ``caches``: arrays/CPU tensors [num_blocks, ...] of one shape and dtype
+    (e.g. K and V of every layer); ``block_mapping``: int64 [P, 2] (src, dst),
+    applied in order."""
+    hs = [_host(c).copy() for c in caches]
+    if not hs:
+        return [], 0
+    n = hs[0].shape[0]
+    for h in hs:
+        if h.shape != hs[0].shape or h.dtype != hs[0].dtype:
+            raise ValueError("caches must share shape and dtype")
+    bb = hs[0].nbytes // max(n, 1)
+    m = _host(block_mapping, np.int64).reshape(-1, 2)
+    ptrs = (ctypes.c_void_p * len(hs))(*[h.ctypes.data for h in hs])
+    bad = _active().pa_ref_copy_blocks(ptrs, len(hs), _p(np.ascontiguousarray(m)),
+                                       m.shape[0], n, bb)
+    return hs, int(bad)
 
 
 def e4m3_encode(x) -> np.ndarray:

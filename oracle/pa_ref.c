@@ -43,6 +43,15 @@
  *        out = sum_p c_p o_p / sum_p c_p,
  *    which equals the unpartitioned softmax exactly in real arithmetic.
  *
+ *  - Block copies for copy-on-write ("vLLM: Architecture, PagedAttention &
+ *    Internals", *Copy-on-write for shared blocks*; "vLLM: High-Throughput
+ *    Serving with PagedAttention", *PagedAttention, the core idea*): when a
+ *    writer must not clobber a shared block, a fresh block receives a copy
+ *    of the shared block's contents.  For every (src, dst) pair of the
+ *    mapping and every cache (K and V of every layer), the bytes of block
+ *    src are copied to block dst; pairs with an id outside the pool are
+ *    skipped and counted.
+ *
  *  - FP8 KV cache (named, without a format, as the way to enlarge the pool in
  *    "vLLM: Architecture, PagedAttention & Internals", *The knobs that
  *    actually matter*, item 5, and "vLLM: High-Throughput Serving with
@@ -227,6 +236,25 @@ int64_t pa_ref_reshape_and_cache_fp8(const void *k, const void *v, uint8_t *k_ca
                 k_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xk / k_scale[j]);
                 v_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xv / v_scale[j]);
             }
+        }
+    }
+    return bad;
+}
+
+/* ---- block copies (copy-on-write) ---------------------------------------- */
+
+/* caches[c] holds num_blocks blocks of block_bytes bytes; mapping is
+ * [num_pairs][2] (src, dst).  Pairs are applied in order.  Returns the number
+ * of pairs skipped because src or dst is outside [0, num_blocks). */
+int64_t pa_ref_copy_blocks(void *const *caches, int32_t num_caches, const int64_t *mapping,
+                           int64_t num_pairs, int64_t num_blocks, int64_t block_bytes) {
+    int64_t bad = 0;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) { ++bad; continue; }
+        for (int32_t c = 0; c < num_caches; ++c) {
+            char *base = (char *)caches[c];
+            memmove(base + dst * block_bytes, base + src * block_bytes, (size_t)block_bytes);
         }
     }
     return bad;

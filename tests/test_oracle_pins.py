@@ -565,6 +565,72 @@ def test_decode_fp8_with_power_of_two_scales_is_decode_of_the_values():
 
 
 # ---------------------------------------------------------------------------
+# block copies for copy-on-write: numpy index assignment
+# ---------------------------------------------------------------------------
+
+def cow_mapping(num_blocks, n, seed):
+    """n (src, dst) pairs with distinct dsts that are never a src (fresh blocks
+    receiving copies of shared ones, as copy-on-write produces them)."""
+    rng = np.random.default_rng(seed)
+    ids = rng.permutation(num_blocks)
+    dst = ids[:n]
+    src = rng.choice(ids[n:], size=n)                   # a shared block may be copied twice
+    return np.stack([src, dst], 1).astype(np.int64)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_copy_blocks_matches_index_assignment(dtype):
+    b = wl.random_batch(25, num_seqs=6, max_len=80, num_heads=8, num_kv_heads=4,
+                        head_dim=64, dtype=dtype, canary=False, new_in_pool=True,
+                        extra_blocks=30)
+    m = cow_mapping(b.num_blocks, 12, 1)
+    layers = [b.k_cache, b.v_cache, b.k_cache * 2, b.v_cache * 3]
+    got, bad = oracle.copy_blocks(layers, m)
+    assert bad == 0
+    for c, g in zip(layers, got):
+        ref = oracle._host(c).copy()
+        ref[m[:, 1]] = ref[m[:, 0]]
+        assert np.array_equal(g.view(np.uint8), ref.view(np.uint8))
+
+
+def test_copy_blocks_skips_out_of_range_pairs_and_keeps_the_rest():
+    pool = np.arange(10 * 48, dtype=np.float32).reshape(10, 3, 16)
+    m = np.array([[2, 7], [11, 3], [4, -1], [5, 5], [1, 8]], dtype=np.int64)
+    (got,), bad = oracle.copy_blocks([pool], m)
+    assert bad == 2
+    ref = pool.copy()
+    ref[7] = pool[2]
+    ref[8] = pool[1]
+    assert np.array_equal(got, ref)                       # src == dst is a no-op
+    (same,), bad = oracle.copy_blocks([pool], np.zeros((0, 2), np.int64))
+    assert bad == 0 and np.array_equal(same, pool)
+
+
+def test_copy_on_write_fork_leaves_the_reader_unchanged():
+    """A sequence forked from another shares its blocks; before the child
+    appends into the shared last block, that block is copied to a fresh one
+    and the child's table points at the copy.  The parent's attention is
+    unchanged and the child's equals attention over the same data."""
+    b = wl.random_batch(26, num_seqs=2, max_len=40, min_len=20, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype="f32", new_in_pool=True, extra_blocks=4)
+    bt = b.block_tables.copy()
+    L = int(b.seq_lens[0])
+    nb = -(-L // 16)
+    fresh = int(np.setdiff1d(np.arange(b.num_blocks), bt[bt != wl.PAD])[0])
+    child = bt[0].copy()
+    child[nb - 1] = fresh                                # the child's private copy
+    (kc, vc), bad = oracle.copy_blocks([b.k_cache, b.v_cache],
+                                       np.array([[bt[0, nb - 1], fresh]], np.int64))
+    assert bad == 0
+    tables = np.stack([bt[0], child])
+    lens = np.array([L, L], np.int32)
+    q = torch.stack([b.q[0], b.q[0]])
+    out = oracle.decode(q, kc, vc, tables, lens, b.scale, 2, "f32")
+    ref = oracle.decode(b.q[:1], b.k_cache, b.v_cache, bt[:1], lens[:1], b.scale, 2, "f32")
+    assert np.array_equal(out[0], ref[0]) and np.array_equal(out[1], ref[0])
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: each must make at least one pin fail
 # ---------------------------------------------------------------------------
 
@@ -589,6 +655,8 @@ MUTATIONS = {
                              "k_cache[dst + d] = (uint8_t)pa_ref_e4m3_from_float(xk * k_scale[j]);"),
     "fp8_read_head_scale": ("const double vs = a->v_scale ? (double)a->v_scale[j] : 1.0;",
                             "const double vs = a->v_scale ? (double)a->v_scale[0] : 1.0;"),
+    "copy_direction": ("memmove(base + dst * block_bytes, base + src * block_bytes,",
+                       "memmove(base + src * block_bytes, base + dst * block_bytes,"),
 }
 
 
@@ -629,6 +697,13 @@ def _pins_hold() -> bool:
             if not np.allclose(mo[int(qs[s]):int(qs[s]) + ns], ref.numpy(), rtol=0,
                                atol=1e-9):
                 return False
+        # block copies
+        pool = np.arange(6 * 32, dtype=np.float32).reshape(6, 2, 16)
+        (cp,), nbad = oracle.copy_blocks([pool], np.array([[1, 4], [2, 5]], np.int64))
+        ref = pool.copy()
+        ref[[4, 5]] = pool[[1, 2]]
+        if nbad != 0 or not np.array_equal(cp, ref):
+            return False
         # FP8: every code's value, the ties of the encoder, the write and the read
         vals = oracle.e4m3_decode(ALL_CODES)
         ref = torch_e4m3_values(ALL_CODES)
