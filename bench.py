@@ -333,6 +333,7 @@ def gpu_arm(args, rank, world, device):
         result["paging_overhead"] = paging_overhead_arm(args, device, flush, pa)
         result["multi_query"] = multi_query_arm(args, device, flush, pa)
         result["fp8"] = fp8_arm(args, device, flush, pa)
+        result["copy_blocks"] = copy_blocks_arm(args, device, flush, pa)
     return result, b
 
 
@@ -494,6 +495,28 @@ def fp8_arm(args, device, flush, pa):
     del b, ws, out
     torch.cuda.empty_cache()
     return res
+
+
+def copy_blocks_arm(args, device, flush, pa):
+    """Copy-on-write copies of one step: 256 (src, dst) pairs in K and V of
+    32 Llama-3-8B-shaped layers (32 KiB blocks), one pa_copy_blocks call."""
+    peak, kind = measured_peak()
+    w = wl.cow_step(device=device, layers=32, num_blocks=2048, pairs=256, fill=False)
+    m = torch.from_numpy(w["mapping"]).to(device)
+
+    def call():
+        pa.pa_copy_blocks(w["caches"], m)
+    for _ in range(3):
+        call()
+    t = statistics.mean(time_calls(call, 30, flush, torch.cuda.current_stream())) * 1e-3
+    moved = 2 * len(w["caches"]) * w["mapping"].shape[0] * w["block_bytes"]   # read + write
+    del w, m
+    torch.cuda.empty_cache()
+    return {"workload": "cow_step: 256 block copies x K,V of 32 layers (bf16 8 x 16 x 128 "
+                        "blocks, 32 KiB), one call",
+            "us_per_call": t * 1e6, "bytes_read_plus_written": moved,
+            "achieved_gbs": moved / t / 1e9, "frac_of_peak": moved / t / 1e9 / peak,
+            "peak_kind": kind}
 
 
 def paging_overhead_arm(args, device, flush, pa):
@@ -674,6 +697,13 @@ def single_kernel(args, device):
         def call():
             pa.pa_decode_partitioned_fp8(out, b.q, b.k_cache, b.v_cache, ks, vs, bt, sl,
                                          b.scale, b.num_kv_heads, 512, msl, ws)
+    elif args.only == "copy_blocks":
+        w = wl.cow_step(device=device, layers=32, num_blocks=2048, pairs=256, fill=False)
+        m = torch.from_numpy(w["mapping"]).to(device)
+        b = wl.serving_mix(device="cpu", canary=False)     # byte accounting only
+
+        def call():
+            pa.pa_copy_blocks(w["caches"], m)
     elif args.only in ("multi_spec", "multi_prefill"):
         b = (wl.spec_verify if args.only == "multi_spec" else wl.chunked_prefill_mix)(
             device=device, canary=False)
@@ -719,12 +749,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="approximate seconds of oracle work for the reference arm")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the long-context, paging-overhead, multi-query and FP8 "
-                         "measurements")
+                    help="skip the long-context, paging-overhead, multi-query, FP8 and "
+                         "copy-on-write measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["decode", "partitioned", "cache_write", "multi_spec",
                                        "multi_prefill", "decode_fp8", "cache_write_fp8",
-                                       "partitioned_fp8"],
+                                       "partitioned_fp8", "copy_blocks"],
                     help="launch one kernel alone (for profiling); prints timings only")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -14,6 +14,7 @@
  *   pa_decode_multi        several new query tokens per sequence (a
  *                          prompt chunk or speculative positions), causal
  *                          among themselves, over the same paged cache
+ *   pa_copy_blocks         block copies of copy-on-write, all layers at once
  *   *_fp8                  the cache write, decode and split-KV decode
  *                          over an FP8 (E4M3) cache with per-KV-head scales
  *
@@ -252,6 +253,36 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache,
                     int64_t num_blocks, int32_t block_size,
                     int32_t max_blocks_per_seq, int64_t q_row_stride,
                     float scale, int32_t dtype, void *stream);
+
+/*
+ * pa_copy_blocks -- the GPU half of copy-on-write.
+ *
+ * Defined in "vLLM: Architecture, PagedAttention & Internals", *Copy-on-write
+ * for shared blocks* (a writer about to append into a block whose refcount is
+ * above one gets a fresh block holding a copy of the shared one; the
+ * scheduler emits the copy) and "vLLM: High-Throughput Serving with
+ * PagedAttention", *PagedAttention, the core idea* (parallel sampling, beam
+ * search and prefix caching share blocks until one writer diverges).
+ * For every pair i and every cache c, bytes
+ * [src_i * block_bytes, (src_i + 1) * block_bytes) of caches[c] are copied to
+ * the same range at dst_i.  One launch covers K and V of every layer.
+ *
+ * caches        HOST array of num_caches (0..256) DEVICE pointers, each the
+ *               base of a cache of num_blocks blocks of block_bytes bytes
+ *               (any storage type: K, V, of any layer, 16-bit or E4M3), each
+ *               16-byte aligned.
+ * block_mapping DEVICE int64 [num_pairs][2]: (src, dst) block ids.
+ * block_bytes   bytes of one block of one cache, a positive multiple of 16
+ *               (num_kv_heads * block_size * head_dim * element size).
+ * Pairs run in parallel: no dst may appear twice or also be a src (what
+ * copy-on-write produces: fresh destinations, shared sources, possibly one
+ * source copied several times).  A pair with src or dst outside
+ * [0, num_blocks) is skipped and sets PA_DEVERR_BLOCK_ID.  num_pairs == 0 or
+ * num_caches == 0 launches nothing.
+ */
+int pa_copy_blocks(void *const *caches, int32_t num_caches,
+                   const int64_t *block_mapping, int64_t num_pairs,
+                   int64_t num_blocks, int64_t block_bytes, void *stream);
 
 /*
  * FP8 KV cache.

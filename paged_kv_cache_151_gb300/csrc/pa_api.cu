@@ -408,6 +408,33 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// ---- block copies for copy-on-write ---------------------------------------
+
+int pa_copy_blocks(void *const *caches, int32_t num_caches, const int64_t *block_mapping,
+                   int64_t num_pairs, int64_t num_blocks, int64_t block_bytes, void *stream) {
+    if (num_pairs < 0 || num_blocks < 0 || block_bytes <= 0 || num_caches < 0)
+        return PA_ERR_INVALID_ARG;
+    if (block_bytes % 16) return PA_ERR_UNSUPPORTED;
+    if (num_caches > pa::COPY_MAX_CACHES) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0 || num_caches == 0) return PA_OK;
+    if (!caches || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (num_blocks > INT64_MAX / block_bytes) return PA_ERR_INVALID_ARG;
+    pa::CopyParams p;
+    std::memset(&p, 0, sizeof p);
+    for (int32_t c = 0; c < num_caches; ++c) {
+        if (!caches[c] || !aligned16(caches[c])) return PA_ERR_INVALID_ARG;
+        p.caches[c] = static_cast<unsigned char *>(caches[c]);
+    }
+    p.num_caches = num_caches;
+    p.mapping = block_mapping;
+    p.num_pairs = num_pairs;
+    p.num_blocks = num_blocks;
+    p.block_bytes = block_bytes;
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    cudaError_t e = pa::copy_blocks(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 // ---- FP8 (E4M3) KV cache --------------------------------------------------
 
 int pa_reshape_and_cache_fp8(const void *k, const void *v, void *k_cache, void *v_cache,

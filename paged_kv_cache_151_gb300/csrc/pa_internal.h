@@ -56,6 +56,17 @@ cudaError_t decode_fp8_bf16(const DecodeParams &p, int D, int G, bool partial,
 cudaError_t decode_fp8_f16(const DecodeParams &p, int D, int G, bool partial,
                            long long unit_bound, int cluster, cudaStream_t st);
 
+// block copies for copy-on-write: every (src, dst) pair of `mapping`, in every cache
+constexpr int COPY_MAX_CACHES = 256;
+struct CopyParams {
+    unsigned char *caches[COPY_MAX_CACHES];   // device bases, 16-byte aligned
+    const int64_t *mapping;                   // device [num_pairs][2]
+    int64_t num_pairs, num_blocks, block_bytes;
+    int num_caches;
+    unsigned int *err;
+};
+cudaError_t copy_blocks(const CopyParams &p, cudaStream_t st);
+
 // device error word
 cudaError_t device_error_ptr(unsigned int **out);
 cudaError_t read_device_error(unsigned int *flags, bool clear);

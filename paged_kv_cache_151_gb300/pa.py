@@ -80,6 +80,9 @@ def load():
         lib.pa_decode_fp8.argtypes = dec8 + [P]
         lib.pa_decode_partitioned_fp8.restype = ctypes.c_int
         lib.pa_decode_partitioned_fp8.argtypes = dec8 + [i32, i32, P, sz, P]
+        lib.pa_copy_blocks.restype = ctypes.c_int
+        lib.pa_copy_blocks.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32, P, i64, i64, i64,
+                                       P]
         lib.pa_device_error.restype = ctypes.c_int
         lib.pa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         _lib = lib
@@ -267,6 +270,34 @@ def pa_decode_multi(out, q, k_cache, v_cache, block_tables, seq_lens, query_star
     _check("pa_decode_multi", rc)
 
 
+def pa_copy_blocks(caches, block_mapping, stream=None):
+    """Copy-on-write block copies: for every (src, dst) row of ``block_mapping``
+    (CUDA int64 [P, 2]) copy block src to block dst in every tensor of
+    ``caches`` (contiguous CUDA tensors [num_blocks, ...] of one shape, e.g. K
+    and V of every layer)."""
+    caches = list(caches)
+    _dev(block_mapping, "block_mapping")
+    if block_mapping.dtype != torch.int64 or block_mapping.dim() != 2 or \
+            block_mapping.shape[1] != 2 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be a contiguous int64 [num_pairs, 2]")
+    if not caches:
+        return
+    shape = caches[0].shape
+    nbytes = caches[0].numel() * caches[0].element_size()
+    for i, c in enumerate(caches):
+        _dev(c, f"caches[{i}]")
+        if c.shape != shape or not c.is_contiguous() or \
+                c.numel() * c.element_size() != nbytes:
+            raise ValueError("caches must be contiguous tensors of one shape and size")
+    num_blocks = shape[0]
+    block_bytes = nbytes // max(num_blocks, 1)
+    ptrs = (ctypes.c_void_p * len(caches))(*[c.data_ptr() for c in caches])
+    rc = load().pa_copy_blocks(ptrs, len(caches), block_mapping.data_ptr(),
+                               block_mapping.shape[0], num_blocks, block_bytes,
+                               _stream(stream))
+    _check("pa_copy_blocks", rc)
+
+
 # ---- FP8 (E4M3) cache ------------------------------------------------------
 
 _FP8_TYPES = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t)
@@ -391,6 +422,7 @@ __all__ = [
     "pa_decode_partitioned_workspace_size", "pa_decode_partitioned", "pa_decode_multi",
     "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_partitioned_fp8",
+    "pa_copy_blocks",
     "pa_device_error", "workspace_views",
     "PA_DEVERR_BLOCK_ID", "PA_DEVERR_SEQ_LEN", "PA_DEVERR_SLOT", "PA_DEVERR_TIMEOUT",
 ]

@@ -488,6 +488,42 @@ def chunked_prefill_mix(device="cpu", canary=True, batch=128, chunks=4, chunk=51
 
 
 # ---------------------------------------------------------------------------
+# Copy-on-write
+# ---------------------------------------------------------------------------
+
+def cow_mapping(num_blocks: int, pairs: int, seed: int) -> np.ndarray:
+    """int64 [pairs, 2] (src, dst): distinct fresh destinations that are never
+    a source, sources drawn from the other blocks (a shared block may be
+    copied more than once), as copy-on-write produces them."""
+    rng = np.random.default_rng(seed)
+    ids = rng.permutation(num_blocks)
+    dst = ids[:pairs]
+    src = rng.choice(ids[pairs:], size=pairs)
+    return np.stack([src, dst], 1).astype(np.int64)
+
+
+def cow_step(device="cpu", layers=32, num_blocks=2048, pairs=256, seed=14,
+             fill=True) -> dict:
+    """One step's copy-on-write copies for a Llama-3-8B-shaped cache: K and V
+    of ``layers`` layers, each [num_blocks, 8, 16, 128] bf16 (32 KiB per
+    block), and ``pairs`` (src, dst) copies -- e.g. 256 parallel-sampling
+    children each diverging inside their shared last block.  ``fill`` draws
+    N(0, 0.5^2) contents (else zeros)."""
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(int(seed))
+    shape = (num_blocks, 8, BLOCK_SIZE, 128)
+    caches = []
+    for _ in range(2 * layers):
+        if fill:
+            caches.append((torch.randn(shape, generator=gen, device=torch.device(device))
+                           * 0.5).to(torch.bfloat16))
+        else:
+            caches.append(torch.zeros(shape, dtype=torch.bfloat16, device=torch.device(device)))
+    return {"caches": caches, "mapping": cow_mapping(num_blocks, pairs, seed),
+            "block_bytes": 8 * BLOCK_SIZE * 128 * 2, "layers": layers}
+
+
+# ---------------------------------------------------------------------------
 # FP8 (E4M3) pools
 # ---------------------------------------------------------------------------
 

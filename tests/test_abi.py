@@ -159,3 +159,16 @@ def test_fp8_host_checks(lib):
     assert lib.pa_decode_partitioned_fp8(*part) == -3          # workspace too small
     # the 16-bit entry points do not take E4M3 as a dtype
     assert _decode_status(lib, dtype=3) == -2
+
+
+def test_copy_blocks_host_checks(lib):
+    arr = (ctypes.c_void_p * 3)(16, 32, 48)
+    assert lib.pa_copy_blocks(arr, 3, 16, 0, 10, 4096, None) == 0        # no pairs
+    assert lib.pa_copy_blocks(arr, 0, 16, 5, 10, 4096, None) == 0        # no caches
+    assert lib.pa_copy_blocks(arr, 3, 16, 5, 10, 4100, None) == -2       # not x16
+    assert lib.pa_copy_blocks(arr, 3, 16, 5, 10, 0, None) == -1
+    assert lib.pa_copy_blocks(arr, 3, 16, -1, 10, 4096, None) == -1
+    assert lib.pa_copy_blocks(arr, 300, 16, 5, 10, 4096, None) == -2     # too many caches
+    assert lib.pa_copy_blocks(arr, 3, None, 5, 10, 4096, None) == -1     # no mapping
+    bad = (ctypes.c_void_p * 2)(16, 24)                                  # unaligned cache
+    assert lib.pa_copy_blocks(bad, 2, 16, 5, 10, 4096, None) == -1
