@@ -334,6 +334,7 @@ def gpu_arm(args, rank, world, device):
         result["multi_query"] = multi_query_arm(args, device, flush, pa)
         result["fp8"] = fp8_arm(args, device, flush, pa)
         result["copy_blocks"] = copy_blocks_arm(args, device, flush, pa)
+        result["block_manager"] = block_manager_arm(args)
     return result, b
 
 
@@ -517,6 +518,50 @@ def copy_blocks_arm(args, device, flush, pa):
             "us_per_call": t * 1e6, "bytes_read_plus_written": moved,
             "achieved_gbs": moved / t / 1e9, "frac_of_peak": moved / t / 1e9 / peak,
             "peak_kind": kind}
+
+
+def block_manager_arm(args):
+    """Host-side cost of the native block manager (no GPU work): the serving
+    loop over 256 serving-mix requests with 64 new tokens each in a pool of
+    60 % of their final size (so requests get preempted), and prefix-cached
+    admissions of 2000-token chats sharing a 1500-token system prompt."""
+    from paged_kv_cache_151_gb300 import blocks
+    rng = np.random.default_rng(21)
+    lens = wl.lognormal_lengths(rng, 256, hi=4096)
+    new = 64
+    pool = int(0.6 * sum(-(-(int(L) + new) // 16) for L in lens))
+    loop = blocks.ServingLoop(blocks.BlockManager(pool, 16))
+    for i, L in enumerate(lens):
+        loop.submit(i, int(L), new)
+    steps, tokens, preempts = 0, 0, 0
+    t0 = time.perf_counter()
+    more = True
+    while more:
+        more, steps, ev, wr = loop.step()
+        tokens += len(wr)
+        preempts += sum(e[1] == "preempt" for e in ev)
+    t_loop = time.perf_counter() - t0
+    bm = blocks.BlockManager(40000, 16, prefix_caching=True)
+    system = np.arange(1500, dtype=np.int32)
+    n_chats = 2000
+    t0 = time.perf_counter()
+    hits = 0
+    for i in range(n_chats):
+        toks = np.concatenate([system, np.arange(10**6 + 500 * i, 10**6 + 500 * (i + 1),
+                                                 dtype=np.int32)])
+        hits += bm.add_sequence(i, toks) or 0
+        if i >= 16:
+            bm.free_sequence(i - 16)
+    t_add = time.perf_counter() - t0
+    return {"workload": "serving loop: 256 serving-mix requests x 64 new tokens, pool 60% of "
+                        f"their final blocks ({pool}); prefix cache: {n_chats} 2000-token chats "
+                        "sharing a 1500-token prompt (16 live at a time)",
+            "loop_steps": steps, "loop_tokens": tokens, "loop_preemptions": preempts,
+            "loop_us_per_step": t_loop / max(steps, 1) * 1e6,
+            "loop_tokens_per_s": tokens / t_loop,
+            "prefix_adds_per_s": n_chats / t_add,
+            "prefix_cached_tokens_per_add": hits / n_chats,
+            "includes": "ctypes call overhead per operation"}
 
 
 def paging_overhead_arm(args, device, flush, pa):

@@ -1,8 +1,9 @@
 """Build the CUDA library in-tree: ``paged_kv_cache_151_gb300/_build/libpa.so``.
 
-Every translation unit under ``csrc/`` is compiled for sm_103a only
-(``-gencode arch=compute_103a,code=sm_103a``) in parallel, then linked into one
-shared library exporting the C ABI of ``include/pa.h``.  A unit is rebuilt
+Every translation unit under ``csrc/`` is compiled in parallel -- the CUDA
+units (``.cu``) for sm_103a only (``-gencode arch=compute_103a,code=sm_103a``),
+the host-only units (``.cpp``: the block manager) by nvcc's host compiler --
+then linked into one shared library exporting the C ABI of ``include/*.h``.  A unit is rebuilt
 when it, a header it may include, or the flags changed.
 
     python -m paged_kv_cache_151_gb300.build [--force] [--verbose]
@@ -38,12 +39,12 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _headers():
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hs.append(os.path.join(INCLUDE, "pa.h"))
+    hs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return sorted(hs)
 
 
@@ -58,7 +59,7 @@ def _digest(src: str, flags) -> str:
 
 def _compile(src_name: str, force: bool, verbose: bool, extra, out_dir: str) -> str:
     src = os.path.join(CSRC, src_name)
-    obj = os.path.join(out_dir, src_name[:-3] + ".o")
+    obj = os.path.join(out_dir, os.path.splitext(src_name)[0] + ".o")
     flags = ARCH + NVCC_FLAGS + list(extra)
     stamp = obj + ".sha"
     dig = _digest(src, flags)

@@ -15,7 +15,8 @@ HEADER = os.path.join(ROOT, "include", "pa.h")
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(os.path.join(ROOT, "include", f)).read()
+                   for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pa_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
