@@ -25,9 +25,13 @@
 //     half- or quarter-warp load below touches distinct banks, and the value
 //     product's k index follows the score fragment, so P still never leaves
 //     registers;
-//   - the order of d in the value product is free too (the output is
-//     unpermuted when written): column n of value tile j is d = NT*n + j, so
-//     lane g reads NT consecutive bytes of each of its four V rows.
+//   - the value product is taken transposed, O^T[d][head] += V^T[d][token]
+//     P^T[token][head]: the heads (at most 8) fill the 8 columns of the MMA
+//     tile instead of half of its 16 rows, so no accumulator is wasted, and
+//     the probabilities of the score fragment are exactly its B operand;
+//     its d order is free too (the output is unpermuted when written): lane
+//     g owns d = (D/8)g .. (D/8)g + D/8-1, one contiguous run of each of its
+//     four V rows.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -101,16 +105,19 @@ struct WarpAttnF8 {
     static_assert(sizeof(T) == 2, "q and out are 16-bit");
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(G >= 1 && G <= 8, "group size");
-    static constexpr int KK = D / 32;     // 32-wide d groups (two k-steps each)
-    static constexpr int NT = D / 8;      // n-tiles of the value product
+    static constexpr int KK = D / 32;     // 32-wide d groups of the score product (two k-steps each)
+    static constexpr int MT = D / 16;     // 16-row d tiles of the transposed value product
+    static constexpr int DL = D / 8;      // d values of one lane in the value product
     static constexpr int TILE_BYTES = 16 * D;
 
     int lane, g, t;
-    bool head_ok;
+    bool head_ok;                          // row g of the score tile is a real head
     uint32_t qa0[2 * KK], qa2[2 * KK];     // f16 A fragments of q (rows 0..7), d permuted
     uint4 qn[KK];                          // the next unit's q, raw (8 elements per kk)
-    float acc[NT][4];                      // [0]: d = NT*2t + j, [1]: d = NT*(2t+1) + j
-    float m_run, l_run;
+    // O^T tiles: acc[mt][0], [1]: d = DL*g + 2mt for heads 2t, 2t+1;
+    //            acc[mt][2], [3]: d = DL*g + 2mt + 1 for heads 2t, 2t+1
+    float acc[MT][4];
+    float m_run, l_run;                    // statistics of head g (score layout)
 
     __device__ __forceinline__ void init(int lane_) {
         lane = lane_;
@@ -124,7 +131,7 @@ struct WarpAttnF8 {
         m_run = -INFINITY;
         l_run = 0.f;
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+        for (int j = 0; j < MT; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
     }
@@ -157,24 +164,37 @@ struct WarpAttnF8 {
         }
     }
 
-    // f(g, d, v0, v1, first, m, l): normalised outputs of head g at d, d+1
+    // The running statistics of heads 2t and 2t+1 (held by the lanes of
+    // score rows 2t and 2t+1).
+    __device__ __forceinline__ void head_stats(float v, float &a, float &b) const {
+        a = __shfl_sync(0xffffffffu, v, (8 * t) & 31);
+        b = __shfl_sync(0xffffffffu, v, (8 * t + 4) & 31);
+    }
+
+    // After finish(): f(head, d, v0, v1, first, m, l) for the normalised
+    // outputs at d, d+1 of this lane's heads 2t and 2t+1.
     template <typename Fn>
     __device__ __forceinline__ void for_each_result(Fn &&f) const {
-        if (!head_ok) return;
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        float ma, mb, la, lb;
+        head_stats(m_run, ma, mb);
+        head_stats(l_run, la, lb);
+        const int ha = 2 * t, hb = 2 * t + 1;
+        const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
 #pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            f(g, NT * 2 * t + j, acc[j][0] * inv, acc[j + 1][0] * inv, t == 0 && j == 0, m_run,
-              l_run);
-            f(g, NT * (2 * t + 1) + j, acc[j][1] * inv, acc[j + 1][1] * inv, false, m_run, l_run);
+        for (int mt = 0; mt < MT; ++mt) {
+            const int d = DL * g + 2 * mt;
+            if (ha < G) f(ha, d, acc[mt][0] * ia, acc[mt][2] * ia, g == 0 && mt == 0, ma, la);
+            if (hb < G) f(hb, d, acc[mt][1] * ib, acc[mt][3] * ib, g == 0 && mt == 0, mb, lb);
         }
     }
 
     // One block of E4M3 tiles at shared addresses kt, vt; rows in 1..16.
     // scale_log2 already carries K's scale.
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int rows, float scale_log2) {
-        // -- scores: tile 0 column n = token PERM[n], tile 1 = 8 + PERM[n]
+        // -- scores S[head][token]: tile 0 column n = token PERM[n], tile 1 = 8 + PERM[n];
+        // the odd k-steps accumulate separately (shorter MMA chains)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
         const int r0 = fp8_tile_token(g), r1 = 8 + r0;
 #pragma unroll
         for (int kk = 0; kk < KK; ++kk) {
@@ -182,17 +202,17 @@ struct WarpAttnF8 {
             const uint2 k1 = lds64(kt + fp8_swz<D>(r1, 32 * kk + 8 * t));
             Mma<__half>::run(s0, qa0[2 * kk], qa2[2 * kk], f16x2_from_e4m3x2(k0.x),
                              f16x2_from_e4m3x2(k0.x >> 16));
-            Mma<__half>::run(s0, qa0[2 * kk + 1], qa2[2 * kk + 1], f16x2_from_e4m3x2(k0.y),
+            Mma<__half>::run(s2, qa0[2 * kk + 1], qa2[2 * kk + 1], f16x2_from_e4m3x2(k0.y),
                              f16x2_from_e4m3x2(k0.y >> 16));
             Mma<__half>::run(s1, qa0[2 * kk], qa2[2 * kk], f16x2_from_e4m3x2(k1.x),
                              f16x2_from_e4m3x2(k1.x >> 16));
-            Mma<__half>::run(s1, qa0[2 * kk + 1], qa2[2 * kk + 1], f16x2_from_e4m3x2(k1.y),
+            Mma<__half>::run(s3, qa0[2 * kk + 1], qa2[2 * kk + 1], f16x2_from_e4m3x2(k1.y),
                              f16x2_from_e4m3x2(k1.y >> 16));
         }
         // this lane's four tokens: columns 2t, 2t+1 of both tiles
         const int ta = fp8_tile_token(2 * t), tb = fp8_tile_token(2 * t + 1);
-        float sc[4] = {s0[0] * scale_log2, s0[1] * scale_log2, s1[0] * scale_log2,
-                       s1[1] * scale_log2};
+        float sc[4] = {(s0[0] + s2[0]) * scale_log2, (s0[1] + s2[1]) * scale_log2,
+                       (s1[0] + s3[0]) * scale_log2, (s1[1] + s3[1]) * scale_log2};
         const int tk[4] = {ta, tb, 8 + ta, 8 + tb};
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[e] = tk[e] < rows ? sc[e] : -INFINITY;
@@ -202,24 +222,30 @@ struct WarpAttnF8 {
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float m_new = fmaxf(m_run, mx);
         const float alpha = ex2(m_run - m_new);
-        const uint32_t pa0 = Mma<__half>::pack(ex2(sc[0] - m_new), ex2(sc[1] - m_new));
-        const uint32_t pa2 = Mma<__half>::pack(ex2(sc[2] - m_new), ex2(sc[3] - m_new));
+        // P[head g][tokens]: exactly the B fragments of the transposed value
+        // product (k = the tokens of columns 2t, 2t+1 of tiles 0 and 1)
+        const uint32_t pb0 = Mma<__half>::pack(ex2(sc[0] - m_new), ex2(sc[1] - m_new));
+        const uint32_t pb1 = Mma<__half>::pack(ex2(sc[2] - m_new), ex2(sc[3] - m_new));
         float p0, p1, p2, p3;
-        Mma<__half>::unpack(pa0, p0, p1);
-        Mma<__half>::unpack(pa2, p2, p3);
+        Mma<__half>::unpack(pb0, p0, p1);
+        Mma<__half>::unpack(pb1, p2, p3);
         l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
         m_run = m_new;
+        // the accumulator columns are heads 2t and 2t+1: rescale with theirs
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            float aa, ab;
+            head_stats(alpha, aa, ab);
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                acc[j][0] *= alpha;
-                acc[j][1] *= alpha;
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] *= aa;
+                acc[mt][1] *= ab;
+                acc[mt][2] *= aa;
+                acc[mt][3] *= ab;
             }
         }
 
-        // -- P.V: k index follows the score columns (tokens ta, tb, 8+ta, 8+tb);
-        // lane g reads bytes NT*g .. NT*g + NT-1 (d of column g in tiles j) of
-        // its four V rows and pairs them per d
+        // -- O^T[d][head] += V^T[d][token] P^T[token][head]: A fragments from the
+        // four V rows of this lane's tokens, bytes DL*g .. DL*g + DL-1, paired per d
         if constexpr (D == 128) {
             const uint4 va = lds128(vt + fp8_swz<D>(ta, 16 * g));
             const uint4 vb = lds128(vt + fp8_swz<D>(tb, 16 * g));
@@ -229,16 +255,14 @@ struct WarpAttnF8 {
             const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
+                // bytes 4w .. 4w+3 = d rows (g of tile 2w), (g+8 of 2w), (g of 2w+1), (g+8 of 2w+1)
                 const uint32_t lo01 = prmt(wa[w], wb[w], 0x5140), lo23 = prmt(wa[w], wb[w], 0x7362);
                 const uint32_t hi01 = prmt(wc[w], wd[w], 0x5140), hi23 = prmt(wc[w], wd[w], 0x7362);
-                Mma<__half>::run(acc[4 * w + 0], pa0, pa2, f16x2_from_e4m3x2(lo01),
-                                 f16x2_from_e4m3x2(hi01));
-                Mma<__half>::run(acc[4 * w + 1], pa0, pa2, f16x2_from_e4m3x2(lo01 >> 16),
-                                 f16x2_from_e4m3x2(hi01 >> 16));
-                Mma<__half>::run(acc[4 * w + 2], pa0, pa2, f16x2_from_e4m3x2(lo23),
-                                 f16x2_from_e4m3x2(hi23));
-                Mma<__half>::run(acc[4 * w + 3], pa0, pa2, f16x2_from_e4m3x2(lo23 >> 16),
-                                 f16x2_from_e4m3x2(hi23 >> 16));
+                Mma<__half>::run4(acc[2 * w], f16x2_from_e4m3x2(lo01), f16x2_from_e4m3x2(lo01 >> 16),
+                                  f16x2_from_e4m3x2(hi01), f16x2_from_e4m3x2(hi01 >> 16), pb0, pb1);
+                Mma<__half>::run4(acc[2 * w + 1], f16x2_from_e4m3x2(lo23),
+                                  f16x2_from_e4m3x2(lo23 >> 16), f16x2_from_e4m3x2(hi23),
+                                  f16x2_from_e4m3x2(hi23 >> 16), pb0, pb1);
             }
         } else {
             const uint2 va = lds64(vt + fp8_swz<D>(ta, 8 * g));
@@ -251,14 +275,11 @@ struct WarpAttnF8 {
             for (int w = 0; w < 2; ++w) {
                 const uint32_t lo01 = prmt(wa[w], wb[w], 0x5140), lo23 = prmt(wa[w], wb[w], 0x7362);
                 const uint32_t hi01 = prmt(wc[w], wd[w], 0x5140), hi23 = prmt(wc[w], wd[w], 0x7362);
-                Mma<__half>::run(acc[4 * w + 0], pa0, pa2, f16x2_from_e4m3x2(lo01),
-                                 f16x2_from_e4m3x2(hi01));
-                Mma<__half>::run(acc[4 * w + 1], pa0, pa2, f16x2_from_e4m3x2(lo01 >> 16),
-                                 f16x2_from_e4m3x2(hi01 >> 16));
-                Mma<__half>::run(acc[4 * w + 2], pa0, pa2, f16x2_from_e4m3x2(lo23),
-                                 f16x2_from_e4m3x2(hi23));
-                Mma<__half>::run(acc[4 * w + 3], pa0, pa2, f16x2_from_e4m3x2(lo23 >> 16),
-                                 f16x2_from_e4m3x2(hi23 >> 16));
+                Mma<__half>::run4(acc[2 * w], f16x2_from_e4m3x2(lo01), f16x2_from_e4m3x2(lo01 >> 16),
+                                  f16x2_from_e4m3x2(hi01), f16x2_from_e4m3x2(hi01 >> 16), pb0, pb1);
+                Mma<__half>::run4(acc[2 * w + 1], f16x2_from_e4m3x2(lo23),
+                                  f16x2_from_e4m3x2(lo23 >> 16), f16x2_from_e4m3x2(hi23),
+                                  f16x2_from_e4m3x2(hi23 >> 16), pb0, pb1);
             }
         }
     }
@@ -277,17 +298,16 @@ struct WarpAttnF8 {
 
     // merge slot: Mw[G], Lw[G], Aw[G][D] in natural d order
     __device__ __forceinline__ void store_partial(float *Mw, float *Lw, float *Aw) const {
-        if (!head_ok) return;
-        if (t == 0) {
+        if (head_ok && t == 0) {
             Mw[g] = m_run;
             Lw[g] = l_run;
         }
+        const int ha = 2 * t, hb = 2 * t + 1;
 #pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            *reinterpret_cast<float2 *>(Aw + g * D + NT * 2 * t + j) =
-                make_float2(acc[j][0], acc[j + 1][0]);
-            *reinterpret_cast<float2 *>(Aw + g * D + NT * (2 * t + 1) + j) =
-                make_float2(acc[j][1], acc[j + 1][1]);
+        for (int mt = 0; mt < MT; ++mt) {
+            const int d = DL * g + 2 * mt;
+            if (ha < G) *reinterpret_cast<float2 *>(Aw + ha * D + d) = make_float2(acc[mt][0], acc[mt][2]);
+            if (hb < G) *reinterpret_cast<float2 *>(Aw + hb * D + d) = make_float2(acc[mt][1], acc[mt][3]);
         }
     }
 };

@@ -28,6 +28,10 @@
 
 namespace pa {
 
+#ifndef PA_QK_SPLIT
+#define PA_QK_SPLIT 0
+#endif
+
 // smem byte offset of 16-byte chunk `chunk` (0..D/8-1) of row `row` (0..15)
 // in a tile stored as D/64 boxes of [16 rows][128 bytes], each box swizzled
 // with the 128-byte pattern (chunk position XOR row mod 8).
@@ -183,15 +187,30 @@ struct WarpAttnTC {
         // -- scores S^T[g][tok] for tok in {2t, 2t+1} (s0) and {8+2t, 9+2t} (s1)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         const int rr = lane & 7, mi = lane >> 3;
+#if PA_QK_SPLIT
+        // even and odd k-steps accumulate separately: two shorter MMA chains
+        float s2[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
+#endif
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             // matrices: (tok 0-7, chunk 2ks), (tok 0-7, 2ks+1), (tok 8-15, 2ks), (tok 8-15, 2ks+1)
             const int tok = (mi >> 1) * 8 + rr, chunk = 2 * ks + (mi & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kt + swz_offset(tok, chunk), b0, b1, b2, b3);
+#if PA_QK_SPLIT
+            if (ks & 1) {
+                Mma<T>::run(s2, qa0[ks], qa2[ks], b0, b1);
+                Mma<T>::run(s3, qa0[ks], qa2[ks], b2, b3);
+                continue;
+            }
+#endif
             Mma<T>::run(s0, qa0[ks], qa2[ks], b0, b1);
             Mma<T>::run(s1, qa0[ks], qa2[ks], b2, b3);
         }
+#if PA_QK_SPLIT
+        s0[0] += s2[0]; s0[1] += s2[1];
+        s1[0] += s3[0]; s1[1] += s3[1];
+#endif
         float sc[4] = {s0[0] * scale_log2, s0[1] * scale_log2, s1[0] * scale_log2,
                        s1[1] * scale_log2};
         const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};

@@ -242,6 +242,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
 template <typename T>
 __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
+#ifndef PA_F8_BLOCKS_PER_SM
+#define PA_F8_BLOCKS_PER_SM 3
+#endif
+
 // What a warp pays to enter a unit (load its query, park or write its
 // result), in quarters of one 16-token block; used to split the stream.
 #ifndef PA_UNIT_COST_Q4
@@ -250,8 +254,15 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
 // T: the type of q and out; KV: the caches' storage (T, or E4M3 codes with
 // per-KV-head scales, 16-bit T only).
+// Blocks per SM the kernel is built for: E4M3 tiles are half the bytes, so
+// three blocks (12 warps) fit and hide more latency; 16-bit tiles, two.
+template <typename KV>
+__host__ __device__ constexpr int persistent_blocks_per_sm() {
+    return sizeof(KV) == 1 ? PA_F8_BLOCKS_PER_SM : 2;
+}
+
 template <typename T, typename KV, int D, int G, int NW, int S, int MODE>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, persistent_blocks_per_sm<KV>())
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr bool TC = use_tc<T>();
     constexpr bool F8 = std::is_same<KV, e4m3>::value;
@@ -816,8 +827,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     if (C > 1) cluster_sync();
 }
 
-// Stages per warp: as many as keep two blocks per SM (<= 113 KiB of shared
-// memory each), up to about PA_STAGE_KB KiB of K+V in flight per warp.
+// Stages per warp: as many as keep the blocks per SM the kernel is built for
+// (two, or three for E4M3 tiles) within shared memory, up to about
+// PA_STAGE_KB KiB of K+V in flight per warp.
 #ifndef PA_STAGE_KB
 #define PA_STAGE_KB 16
 #endif
@@ -825,8 +837,9 @@ template <typename T, typename KV, int D, int G, int MODE>
 __host__ __device__ constexpr int persistent_stages() {
     int s = PA_STAGE_KB * 1024 / (int)(2 * 16 * D * sizeof(KV));
     s = s < 2 ? 2 : (s > 6 ? 6 : s);
+    const size_t cap = (size_t)(227 / persistent_blocks_per_sm<KV>()) * 1024;
     while (s > 2 && PersistentLayout<T, KV, D, G, 4, 0, MODE>::BYTES +
-                            (size_t)4 * s * (2 * 16 * D * sizeof(KV) + 8) > 113 * 1024)
+                            (size_t)4 * s * (2 * 16 * D * sizeof(KV) + 8) > cap)
         --s;
     return s;
 }
