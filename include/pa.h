@@ -52,7 +52,13 @@
  *
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
  * Every call only enqueues kernels on it and never synchronises, except
- * pa_device_error, which reads device memory synchronously.
+ * pa_device_error, which reads device memory synchronously.  The decode
+ * kernels are launched with programmatic stream serialization: when the
+ * kernel before them in the stream is a cache write of this library
+ * (pa_reshape_and_cache, pa_reshape_and_cache_fp8), they start while it
+ * finishes and read seq_lens, block_tables and query_start meanwhile -- the
+ * cache writes never touch those -- and touch the caches, q and out only
+ * after it has completed.  After any other kernel they start as usual.
  *
  * Errors.  Calls return PA_OK (0) or a negative pa_status; nothing is
  * launched when the host-side checks fail.  Contents of device arrays are not

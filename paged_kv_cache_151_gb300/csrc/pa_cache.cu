@@ -43,6 +43,7 @@ reshape_and_cache_kernel(const unsigned char *__restrict__ k,
                          int num_kv_heads, int row_bytes, int64_t k_tok_stride_bytes,
                          int64_t v_tok_stride_bytes, int64_t num_slots,
                          unsigned int *err) {
+    launch_dependents();      // a decode launched next may set up meanwhile
     const int per_row = row_bytes / (int)sizeof(U);
     const int64_t per_tok = (int64_t)num_kv_heads * per_row;
     const int64_t total = num_tokens * per_tok;
@@ -101,6 +102,7 @@ cudaError_t reshape_and_cache(const void *k, const void *v, void *k_cache, void 
     auto *kc = static_cast<unsigned char *>(k_cache);
     auto *vc = static_cast<unsigned char *>(v_cache);
 #define PA_RC(U)                                                                     \
+    prefer_shared_carveout<reshape_and_cache_kernel<U>>();                            \
     reshape_and_cache_kernel<U><<<(unsigned)blocks, 256, 0, st>>>(                    \
         kb, vb, kc, vc, slot_mapping, num_tokens, num_kv_heads, row_bytes,            \
         k_tok_stride_bytes, v_tok_stride_bytes, num_slots, err)
@@ -154,6 +156,7 @@ reshape_and_cache_fp8_kernel(const TS *__restrict__ k, const TS *__restrict__ v,
                              int64_t v_tok_stride, int64_t num_slots,
                              const float *__restrict__ k_scale,
                              const float *__restrict__ v_scale, unsigned int *err) {
+    launch_dependents();      // a decode launched next may set up meanwhile
     const int per_row = head_dim / 8;
     const int64_t per_tok = (int64_t)num_kv_heads * per_row;
     const int64_t total = num_tokens * per_tok;
@@ -197,6 +200,7 @@ cudaError_t reshape_and_cache_fp8(const void *k, const void *v, void *k_cache, v
     auto *kc = static_cast<unsigned char *>(k_cache);
     auto *vc = static_cast<unsigned char *>(v_cache);
 #define PA_RC8(TS)                                                                       \
+    prefer_shared_carveout<reshape_and_cache_fp8_kernel<TS>>();                           \
     reshape_and_cache_fp8_kernel<TS><<<(unsigned)blocks, 256, 0, st>>>(                   \
         static_cast<const TS *>(k), static_cast<const TS *>(v), kc, vc, slot_mapping,      \
         num_tokens, num_kv_heads, head_dim, k_tok_stride, v_tok_stride, num_slots, k_scale, \

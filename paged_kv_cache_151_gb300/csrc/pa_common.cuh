@@ -202,6 +202,20 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
     return r;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the kernel before it in the stream
+// is still running once every block of that kernel has called
+// launch_dependents(); grid_dependency_wait() then blocks until that kernel
+// has completed and its writes are visible (it returns at once when there is
+// no such kernel).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -7,6 +7,21 @@
 
 namespace pa {
 
+// Kernels that let a following decode start early (they call
+// launch_dependents()) keep the shared-memory carveout the decode needs:
+// an SM cannot change its L1 / shared split while one of their blocks is
+// resident, and a decode block that cannot be placed would wait for that.
+// Set once per kernel (and per process: the attribute is the function's).
+template <auto Kernel>
+inline void prefer_shared_carveout() {
+    static const bool done = [] {
+        cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+        return true;
+    }();
+    (void)done;
+}
+
 struct DecodeParams;
 struct MergeParams;
 

@@ -242,6 +242,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
 template <typename T>
 __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
+#ifndef PA_DECODE_PDL
+#define PA_DECODE_PDL 1
+#endif
+
 #ifndef PA_F8_BLOCKS_PER_SM
 #define PA_F8_BLOCKS_PER_SM 3
 #endif
@@ -481,21 +485,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     __syncthreads();
     if (C > 1) cluster_sync();                     // peers' counters are initialised
 
-    // units with no tokens (pa_decode only): their output is zero
-    if (!PARTIAL && !MQ && rank == 0 && warp == NW - 1) {
-        for (int q = 0; q < nu; ++q) {
-            const UnitRec u = units[q];
-            if (u.nb != 0) continue;
-            T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G) * D;
-            for (int i = lane; i < G * D / E; i += 32) {
-                float z[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) z[e] = 0.f;
-                store_chunk<T>(o + i * E, z);
-            }
-        }
-    }
-
     // ---- 4. stream this warp's range of the cluster's blocks ------------------
     auto range_lo = [&](int g) -> int { return bound[g]; };
     auto owner = [&](int f) -> int {               // warp whose range holds position f
@@ -582,6 +571,27 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             bulk_g2s(dst + TILE, vbase + off, bytes, bar, pol);
         }
     };
+
+    // Everything above reads only seq_lens, query_start and block_tables.
+    // The caches (and q, out) are touched only after the kernel before this
+    // one in the stream -- typically the cache write of the same step, which
+    // lets this kernel start early -- has completed.
+    grid_dependency_wait();
+
+    // units with no tokens (pa_decode only): their output is zero
+    if (!PARTIAL && !MQ && rank == 0 && warp == NW - 1) {
+        for (int q = 0; q < nu; ++q) {
+            const UnitRec u = units[q];
+            if (u.nb != 0) continue;
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)u.s * H + u.j * G) * D;
+            for (int i = lane; i < G * D / E; i += 32) {
+                float z[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) z[e] = 0.f;
+                store_chunk<T>(o + i * E, z);
+            }
+        }
+    }
 
     const int pre = n_mine < S ? n_mine : S;
     for (int k = 0; k < pre; ++k) {
@@ -880,13 +890,17 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
     cfg.blockDim = dim3(C::NW * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the previous kernel in the stream finishes, if that
+    // kernel allows it (the cache write does); see grid_dependency_wait()
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = PA_DECODE_PDL;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (nc <= 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

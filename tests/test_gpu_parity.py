@@ -386,3 +386,43 @@ def test_full_long_context_partitioned(cuda_lib):
     b = wl.long_context(device="cuda", new_in_pool=True)
     out, _, _ = gpu_partitioned(cuda_lib, b, 512, max_seq_len=131072)
     sampled_check(b, out, 12, 4, "bf16")
+
+
+def test_decode_sees_the_cache_write_it_follows(cuda_lib):
+    """The decode is launched to overlap the cache write before it (it sets up
+    while the write finishes); every step writes a token whose key dominates
+    the softmax, and the decode issued right after must already attend to it:
+    the output is that token's value."""
+    B, Hkv, G, D = 64, 8, 4, 128
+    b = wl.random_batch(900, num_seqs=B, max_len=300, min_len=40, num_heads=G * Hkv,
+                        num_kv_heads=Hkv, head_dim=D, dtype="bf16", device="cuda",
+                        keep_seq=False, extra_blocks=B * 20 + 8)
+    bt = [list(r[r != wl.PAD]) for r in b.block_tables]
+    free = sorted(set(range(b.num_blocks)) - {x for r in bt for x in r})
+    kc, vc = b.k_cache.clone(), b.v_cache.clone()
+    lens = b.ctx_lens.astype(np.int64).copy()
+    q = b.q
+    for step in range(20):
+        slots = []
+        for s in range(B):
+            if lens[s] // 16 >= len(bt[s]):
+                bt[s].append(free.pop())
+            slots.append(bt[s][lens[s] // 16] * 16 + lens[s] % 16)
+        # the new key is 60 x the mean query direction of each group: it dominates
+        qg = q.float().view(B, Hkv, G, D).mean(2)
+        k_new = (60.0 * qg / qg.norm(dim=-1, keepdim=True)).to(torch.bfloat16).contiguous()
+        v_new = torch.randn((B, Hkv, D), device="cuda").to(torch.bfloat16)
+        lens += 1
+        width = max(len(r) for r in bt)
+        tab = np.full((B, width), wl.PAD, np.int32)
+        for s in range(B):
+            tab[s, :len(bt[s])] = bt[s]
+        tab_t = torch.from_numpy(tab).cuda()
+        sl_t = torch.from_numpy(lens.astype(np.int32)).cuda()
+        sm_t = torch.tensor(slots, dtype=torch.int64, device="cuda")
+        out = torch.empty_like(q)
+        cuda_lib.pa_reshape_and_cache(k_new, v_new, kc, vc, sm_t)
+        cuda_lib.pa_decode(out, q, kc, vc, tab_t, sl_t, b.scale, Hkv)
+        torch.cuda.synchronize()
+        want = v_new.float().repeat_interleave(G, dim=1)
+        assert (out.float() - want).abs().max().item() < 0.1, f"step {step}"
