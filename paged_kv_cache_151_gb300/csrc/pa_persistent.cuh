@@ -236,6 +236,84 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
     return before + x - v;
 }
 
+// Stable counting sort for small batches: keys[i] = ((0xffff - nb_i) << 16) | i
+// for i < B (B <= 256, every nb_i < CS_BINS); out receives them in
+// ascending order (block count descending, index ascending), exactly what
+// sort_keys gives.  The sequences fall into 32-wide chunks; inside a chunk
+// the lanes with equal block counts find each other with match.any (their
+// rank is the number of such lanes below them); per (chunk, count) the
+// totals turn into offsets by a running sum over chunks, and per count into
+// the number of sequences with more blocks by a scan over counts.
+constexpr int CS_BINS = 512;
+constexpr int CS_MAX_SEQS = 256;
+template <int NT>
+__host__ __device__ constexpr size_t counting_sort_scratch_bytes() {
+    return (size_t)(CS_MAX_SEQS / 32) * CS_BINS * 4 + CS_MAX_SEQS * 4 + CS_BINS * 4;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+template <int NT>
+__device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int *scratch,
+                              int *wtot) {
+    constexpr int NW = NT / 32;
+    constexpr int PER = CS_BINS / NT;               // bins per thread in the scan
+    static_assert(CS_BINS % NT == 0, "bins per thread");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nch = (B + 31) >> 5;
+    int *hist = scratch;                            // [nch][CS_BINS]: counts, then offsets
+    int *rin = hist + (CS_MAX_SEQS / 32) * CS_BINS; // [B] rank among equal counts in the chunk
+    int *larger = rin + CS_MAX_SEQS;                // [CS_BINS] sequences with more blocks
+    for (int i = tid; i < nch * CS_BINS; i += NT) hist[i] = 0;
+    __syncthreads();
+    for (int c = warp; c < nch; c += NW) {
+        const int i = 32 * c + lane;
+        const bool valid = i < B;
+        const int nb = valid ? 0xffff - (int)(keys[i] >> 16) : CS_BINS;   // CS_BINS: no bin
+        const uint32_t m = __match_any_sync(0xffffffffu, nb);
+        if (valid) {
+            const uint32_t below = m & lanemask_lt();
+            rin[i] = __popc(below);
+            if (below == 0) hist[c * CS_BINS + nb] = __popc(m);
+        }
+    }
+    __syncthreads();
+    // per count: offsets of the chunks, and the total; then, highest count
+    // first, the number of sequences above each count
+    int tot[PER];
+    int local = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const int b = CS_BINS - 1 - (tid * PER + e);   // descending counts
+        int run = 0;
+        for (int c = 0; c < nch; ++c) {
+            const int x = hist[c * CS_BINS + b];
+            hist[c * CS_BINS + b] = run;
+            run += x;
+        }
+        tot[e] = run;
+        local += run;
+    }
+    int all;
+    int before = block_exclusive_scan<NT>(local, wtot, &all);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const int b = CS_BINS - 1 - (tid * PER + e);
+        larger[b] = before;
+        before += tot[e];
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += NT) {
+        const int nb = 0xffff - (int)(keys[i] >> 16);
+        out[larger[nb] + hist[(i >> 5) * CS_BINS + nb] + rin[i]] = keys[i];
+    }
+    __syncthreads();
+}
+
 // 16-bit caches use the tensor cores (pa_mma.cuh) on swizzled tiles placed
 // by tensor-map copies of whole 16-row blocks; fp32 caches use the CUDA-core
 // path (pa_math.cuh) on tiles placed by 1-D copies of the valid rows.
@@ -332,6 +410,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);   // [B]
     int *lens = start + B;                                           // [B], clamped
     uint32_t *sort_tmp = reinterpret_cast<uint32_t *>(lens + ((B + 3) & ~3));  // [Bp] if Bp <= 2*NT
+    int nb_max = 0;                                // this thread's largest block count
     for (int i = tid; i < Bp; i += NT) {
         uint32_t key = 0xffffffffu;
         if (i < B) {
@@ -343,12 +422,26 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                 if (blockIdx.x == 0 && !mq_valid(i, L)) set_error(p.err, ERR_SEQ_LEN);
             }
             const int nb = (L + 15) >> 4;
+            nb_max = max(nb_max, nb);
             key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
         }
         keys[i] = key;
     }
+    nb_max = __reduce_max_sync(0xffffffffu, nb_max);
+    if (lane == 0) wtot[warp] = nb_max;
     __syncthreads();
-    keys = sort_keys<NT>(keys, sort_tmp, Bp);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) nb_max = max(nb_max, wtot[w]);
+    __syncthreads();
+    static_assert(Lay::STAGES >= 4096 + counting_sort_scratch_bytes<NT>(),
+                  "the stage region holds the counting sort's scratch");
+    if (B <= CS_MAX_SEQS && nb_max < CS_BINS) {
+        int *cs = reinterpret_cast<int *>(sort_tmp + Bp);
+        counting_sort<NT>(keys, sort_tmp, B, cs, wtot);
+        keys = sort_tmp;
+    } else {
+        keys = sort_keys<NT>(keys, sort_tmp, Bp);
+    }
 
     // ---- 2. number the units: exclusive scan of units per sorted sequence -----
     auto units_of = [&](int pos) -> int {          // pos < B

@@ -408,9 +408,11 @@ def test_decode_sees_the_cache_write_it_follows(cuda_lib):
             if lens[s] // 16 >= len(bt[s]):
                 bt[s].append(free.pop())
             slots.append(bt[s][lens[s] // 16] * 16 + lens[s] % 16)
-        # the new key is 60 x the mean query direction of each group: it dominates
+        # the new key points along the mean query of each group, longer than
+        # every earlier step's: it dominates the softmax
         qg = q.float().view(B, Hkv, G, D).mean(2)
-        k_new = (60.0 * qg / qg.norm(dim=-1, keepdim=True)).to(torch.bfloat16).contiguous()
+        k_new = ((60.0 + 30.0 * step) * qg / qg.norm(dim=-1, keepdim=True)).to(
+            torch.bfloat16).contiguous()
         v_new = torch.randn((B, Hkv, D), device="cuda").to(torch.bfloat16)
         lens += 1
         width = max(len(r) for r in bt)
