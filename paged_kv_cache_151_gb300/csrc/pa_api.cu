@@ -382,10 +382,14 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
     if (dtype == PA_F32) return PA_ERR_UNSUPPORTED;
     if (!q_rows_aligned(q, q_row_stride, dtype) || !aligned16(out)) return PA_ERR_INVALID_ARG;
     const int G = num_heads / num_kv_heads;
-    // work units: (sequence, KV head, 16-row tile of the sequence's rows x G heads)
+    // Sequences with at least PREFILL_GROUP_ROWS (token, head) rows go to the prefill
+    // kernel (blocks of 64 rows sharing one K/V ring), the others to the persistent
+    // kernel's work units: (sequence, KV head, 16-row tile of the rows).
     const int64_t rows = (int64_t)(max_query_len < num_q_rows ? max_query_len : num_q_rows) * G;
-    const int64_t tiles = (rows + 15) / 16;
-    if (tiles == 0) return PA_OK;
+    const bool split = rows >= pa::PREFILL_GROUP_ROWS;
+    const int64_t small_rows = split ? pa::PREFILL_GROUP_ROWS - 1 : rows;
+    const int64_t tiles = (small_rows + 15) / 16;
+    if (rows == 0) return PA_OK;
     pa::DecodeParams p;
     std::memset(&p, 0, sizeof p);
     p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
@@ -397,9 +401,17 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
     p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
     p.max_blocks = max_blocks_per_seq;
     p.scale_log2 = scale * pa::LOG2E;
+    p.mq_split_rows = split ? pa::PREFILL_GROUP_ROWS : 0;
     if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
     if (!prepare_maps(p, dtype, head_dim)) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (split) {
+        const int groups = (int)((rows + pa::PREFILL_GROUP_ROWS - 1) / pa::PREFILL_GROUP_ROWS);
+        cudaError_t e = dtype == PA_BF16 ? pa::prefill_bf16(p, head_dim, G, groups, st)
+                                         : pa::prefill_f16(p, head_dim, G, groups, st);
+        if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
     const long long unit_bound = (long long)num_seqs * num_kv_heads * tiles;
     cudaError_t e = dtype == PA_BF16
                         ? pa::decode_multi_bf16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st)

@@ -189,6 +189,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// L2 policy for data several blocks read in turn (K/V of a long query run).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // ---- clusters -------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -69,6 +69,8 @@ struct DecodeParams {
     const int32_t *query_start;  // multi-token queries: [num_seqs + 1] row offsets
     int max_query_len;        // multi-token queries: bound on a sequence's rows
     int num_q_rows;           // multi-token queries: rows of q and out
+    int mq_split_rows;        // multi-token queries: > 0: sequences with at least this
+                              // many (token, head) rows are left to the prefill kernel
     const float *k_scale;     // E4M3 caches: [num_kv_heads] dequantisation scales
     const float *v_scale;
     float scale_log2;         // scale * log2(e)

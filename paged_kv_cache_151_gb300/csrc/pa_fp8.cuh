@@ -117,7 +117,8 @@ struct WarpAttnF8 {
     // O^T tiles: acc[mt][0], [1]: d = DL*g + 2mt for heads 2t, 2t+1;
     //            acc[mt][2], [3]: d = DL*g + 2mt + 1 for heads 2t, 2t+1
     float acc[MT][4];
-    float m_run, l_run;                    // statistics of head g (score layout)
+    float m_run, l_run;                    // reference level and sum of head g (score layout)
+    float m_max;                           // largest score of head g so far
 
     __device__ __forceinline__ void init(int lane_) {
         lane = lane_;
@@ -128,7 +129,7 @@ struct WarpAttnF8 {
     }
 
     __device__ __forceinline__ void reset() {
-        m_run = -INFINITY;
+        m_run = m_max = -INFINITY;
         l_run = 0.f;
 #pragma unroll
         for (int j = 0; j < MT; ++j)
@@ -220,12 +221,14 @@ struct WarpAttnF8 {
         float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = ex2(m_run - m_new);
+        m_max = fmaxf(m_max, mx);
+        const float m_new = mx > m_run + RESCALE_LOG2 ? mx : m_run;   // lazy rescaling
+        const float ms = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2(m_run - ms);
         // P[head g][tokens]: exactly the B fragments of the transposed value
         // product (k = the tokens of columns 2t, 2t+1 of tiles 0 and 1)
-        const uint32_t pb0 = Mma<__half>::pack(ex2(sc[0] - m_new), ex2(sc[1] - m_new));
-        const uint32_t pb1 = Mma<__half>::pack(ex2(sc[2] - m_new), ex2(sc[3] - m_new));
+        const uint32_t pb0 = Mma<__half>::pack(ex2(sc[0] - ms), ex2(sc[1] - ms));
+        const uint32_t pb1 = Mma<__half>::pack(ex2(sc[2] - ms), ex2(sc[3] - ms));
         float p0, p1, p2, p3;
         Mma<__half>::unpack(pb0, p0, p1);
         Mma<__half>::unpack(pb1, p2, p3);
@@ -291,7 +294,22 @@ struct WarpAttnF8 {
         for (int i = lane; i < n; i += 32) p[i] = make_uint4(0, 0, 0, 0);
     }
 
+    // Bring the state to the true maximum, then sum the lanes of each row.
     __device__ __forceinline__ void finish() {
+        const float f = m_max == -INFINITY ? 1.f : ex2((m_run == -INFINITY ? m_max : m_run) - m_max);
+        if (__any_sync(0xffffffffu, f != 1.f)) {
+            float fa, fb;
+            head_stats(f, fa, fb);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] *= fa;
+                acc[mt][1] *= fb;
+                acc[mt][2] *= fa;
+                acc[mt][3] *= fb;
+            }
+        }
+        l_run *= f;
+        m_run = m_max;
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     }

@@ -46,6 +46,10 @@ cudaError_t decode_multi_bf16(const DecodeParams &p, int D, int G, long long uni
                               int cluster, cudaStream_t st);
 cudaError_t decode_multi_f16(const DecodeParams &p, int D, int G, long long unit_bound,
                              int cluster, cudaStream_t st);
+// the rows of sequences with many (token, head) rows: groups of 64 rows per block
+cudaError_t prefill_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
+cudaError_t prefill_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
+constexpr int PREFILL_GROUP_ROWS = 64;     // rows of one prefill block (= its minimum)
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

@@ -32,6 +32,15 @@ namespace pa {
 #define PA_QK_SPLIT 0
 #endif
 
+// Lazy rescaling of the online softmax: the reference level m of a row moves
+// only when a block's maximum exceeds it by more than RESCALE_LOG2 (log2
+// units), so the accumulators are rescaled on few blocks instead of nearly
+// every one; probabilities exp2(s - m) then stay below 2^RESCALE_LOG2, well
+// inside bf16 / f16 range.  The true maximum is tracked alongside and the
+// state is brought to it once, when the unit ends, so (m, l, acc) keep their
+// exact meaning: l = sum exp2(s - max s), acc = sum exp2(s - max s) v.
+constexpr float RESCALE_LOG2 = 8.f;
+
 // smem byte offset of 16-byte chunk `chunk` (0..D/8-1) of row `row` (0..15)
 // in a tile stored as D/64 boxes of [16 rows][128 bytes], each box swizzled
 // with the 128-byte pattern (chunk position XOR row mod 8).
@@ -125,7 +134,8 @@ struct WarpAttnTC {
     uint32_t qa0[KS], qa2[KS];             // A fragments of Q (rows 0..7)
     uint32_t qn0[KS], qn2[KS];             // the next unit's, loaded ahead
     float acc[NT][4];                      // O fragments ([2],[3]: rows 8..15, unused)
-    float m_run, l_run;
+    float m_run, l_run;                    // reference level and sum of head g
+    float m_max;                           // largest score of head g so far
 
     __device__ __forceinline__ void init(int lane_) {
         lane = lane_;
@@ -136,7 +146,7 @@ struct WarpAttnTC {
     }
 
     __device__ __forceinline__ void reset() {
-        m_run = -INFINITY;
+        m_run = m_max = -INFINITY;
         l_run = 0.f;
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -221,10 +231,12 @@ struct WarpAttnTC {
         float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = ex2(m_run - m_new);
-        const uint32_t pa0 = Mma<T>::pack(ex2(sc[0] - m_new), ex2(sc[1] - m_new));
-        const uint32_t pa2 = Mma<T>::pack(ex2(sc[2] - m_new), ex2(sc[3] - m_new));
+        m_max = fmaxf(m_max, mx);
+        const float m_new = mx > m_run + RESCALE_LOG2 ? mx : m_run;
+        const float ms = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2(m_run - ms);
+        const uint32_t pa0 = Mma<T>::pack(ex2(sc[0] - ms), ex2(sc[1] - ms));
+        const uint32_t pa2 = Mma<T>::pack(ex2(sc[2] - ms), ex2(sc[3] - ms));
         float p0, p1, p2, p3;
         Mma<T>::unpack(pa0, p0, p1);
         Mma<T>::unpack(pa2, p2, p3);
@@ -260,8 +272,19 @@ struct WarpAttnTC {
         }
     }
 
-    // Sum the per-lane partial sums of each head (the four lanes of row g).
+    // Bring the state to the true maximum and sum the per-lane partial sums of
+    // each head (the four lanes of row g).
     __device__ __forceinline__ void finish() {
+        const float f = m_max == -INFINITY ? 1.f : ex2((m_run == -INFINITY ? m_max : m_run) - m_max);
+        if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                acc[j][0] *= f;
+                acc[j][1] *= f;
+            }
+        }
+        l_run *= f;
+        m_run = m_max;
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     }
@@ -295,7 +318,8 @@ struct WarpAttnTC16 {
     int lim_lo, lim_hi;                    // last visible position per row (-1: no row)
     uint32_t qa[KS][4];                    // A fragments (lo k-lo, hi k-lo, lo k-hi, hi k-hi)
     float acc[NT][4];                      // [0],[1]: row lo; [2],[3]: row hi
-    float m_lo, m_hi, l_lo, l_hi;
+    float m_lo, m_hi, l_lo, l_hi;          // reference levels and sums of the two rows
+    float x_lo, x_hi;                      // their largest scores so far
 
     __device__ __forceinline__ void init(int lane_) {
         lane = lane_;
@@ -306,7 +330,7 @@ struct WarpAttnTC16 {
     }
 
     __device__ __forceinline__ void reset() {
-        m_lo = m_hi = -INFINITY;
+        m_lo = m_hi = x_lo = x_hi = -INFINITY;
         l_lo = l_hi = 0.f;
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -329,8 +353,12 @@ struct WarpAttnTC16 {
         }
     }
 
-    // One block whose row 0 is at sequence position pos0.
-    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int pos0, float scale_log2) {
+    // One block whose row 0 is at sequence position pos0.  With vrows < 16 the
+    // V rows from vrows on (past the sequence's end: other tokens' data, or
+    // anything) are dropped from this lane's fragments, so they need not be
+    // cleared in shared memory.
+    __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int pos0, float scale_log2,
+                                          int vrows = 16) {
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
         const int rr = lane & 7, mi = lane >> 3;
 #pragma unroll
@@ -357,8 +385,11 @@ struct WarpAttnTC16 {
         mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 1));
         mxl = fmaxf(mxl, __shfl_xor_sync(0xffffffffu, mxl, 2));
         mxh = fmaxf(mxh, __shfl_xor_sync(0xffffffffu, mxh, 2));
+        x_lo = fmaxf(x_lo, mxl);
+        x_hi = fmaxf(x_hi, mxh);
         // a row may see nothing yet (all -inf): keep its state at zero weight
-        const float nl = fmaxf(m_lo, mxl), nh = fmaxf(m_hi, mxh);
+        const float nl = mxl > m_lo + RESCALE_LOG2 ? mxl : m_lo;
+        const float nh = mxh > m_hi + RESCALE_LOG2 ? mxh : m_hi;
         const float sl = nl == -INFINITY ? 0.f : nl, sh = nh == -INFINITY ? 0.f : nh;
         const float al = ex2(m_lo - sl), ah = ex2(m_hi - sh);
         const uint32_t pa0 = Mma<T>::pack(ex2(lo[0] - sl), ex2(lo[1] - sl));
@@ -383,17 +414,41 @@ struct WarpAttnTC16 {
                 acc[j][3] *= ah;
             }
         }
+        // after the transposing load a lane holds tokens 2t, 2t+1 (b0, b2) and
+        // 2t+8, 2t+9 (b1, b3) of its d column
+        const bool tail = vrows < 16;
+        const uint32_t keep0 = (2 * t < vrows ? 0xffffu : 0u) | (2 * t + 1 < vrows ? 0xffff0000u : 0u);
+        const uint32_t keep1 = (2 * t + 8 < vrows ? 0xffffu : 0u) | (2 * t + 9 < vrows ? 0xffff0000u : 0u);
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
             const int tok = (mi & 1) * 8 + rr, chunk = j + (mi >> 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            if (tail) {
+                b0 &= keep0; b2 &= keep0;
+                b1 &= keep1; b3 &= keep1;
+            }
             Mma<T>::run4(acc[j], pa0, pa1, pa2, pa3, b0, b1);
             Mma<T>::run4(acc[j + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
     }
 
     __device__ __forceinline__ void finish() {
+        const float fl = x_lo == -INFINITY ? 1.f : ex2((m_lo == -INFINITY ? x_lo : m_lo) - x_lo);
+        const float fh = x_hi == -INFINITY ? 1.f : ex2((m_hi == -INFINITY ? x_hi : m_hi) - x_hi);
+        if (__any_sync(0xffffffffu, fl != 1.f || fh != 1.f)) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                acc[j][0] *= fl;
+                acc[j][1] *= fl;
+                acc[j][2] *= fh;
+                acc[j][3] *= fh;
+            }
+        }
+        l_lo *= fl;
+        l_hi *= fh;
+        m_lo = x_lo;
+        m_hi = x_hi;
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);

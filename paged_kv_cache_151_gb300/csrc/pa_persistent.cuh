@@ -448,7 +448,8 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         const int nb = 0xffff - (int)(keys[pos] >> 16);
         if constexpr (MQ) {
             const int s = (int)(keys[pos] & 0xffffu);
-            const int nq = mq_valid(s, lens[s]) ? p.query_start[s + 1] - p.query_start[s] : 0;
+            int nq = mq_valid(s, lens[s]) ? p.query_start[s + 1] - p.query_start[s] : 0;
+            if (p.mq_split_rows > 0 && nq * G >= p.mq_split_rows) nq = 0;   // the prefill path's
             return Hkv * ((nq * G + 15) / 16);
         }
         return PARTIAL ? Hkv * ((nb + PB - 1) / PB) : Hkv;

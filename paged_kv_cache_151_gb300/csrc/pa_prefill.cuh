@@ -1,0 +1,248 @@
+// pa_prefill.cuh -- multi-token queries with many rows per sequence (a chunk
+// of a long prompt): the rows of one (sequence, KV head) are cut into groups
+// of 16*NWC, one group per thread block, and the block's NWC warps -- 16
+// rows each -- consume ONE ring of K/V tiles that a producer warp fills with
+// tensor-map copies.  Every tile read from L2 or HBM thus serves 16*NWC
+// query rows instead of 16.
+//
+// "vLLM: Architecture, PagedAttention & Internals", *Prefill, decode, and
+// chunked prefill*: one forward pass carries a slice of a long prompt next
+// to one-token decodes.  Row r of sequence s's slice (token i = r / G, head
+// r % G of the KV head's group) attends over positions 0 .. L - n + i of
+// the paged cache, like the rows of pa_decode_multi's other path; a block
+// handles the rows of one group from their first block to the block of the
+// group's last visible position, and each warp masks its rows' limits.
+//
+// Work items: (row group, sequence, KV head) of the worst case (max_query_len
+// rows), ordered by row group from the last (which sees the most keys) to
+// the first, dealt in turn to as many blocks as are resident; items of
+// sequences with fewer rows, or with fewer than p.mq_split_rows rows (the
+// persistent kernel's), are skipped at once.
+#pragma once
+
+#include "pa_common.cuh"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+#include "pa_math.cuh"
+#include "pa_mma.cuh"
+
+namespace pa {
+
+template <typename T, int D, int NWC, int S>
+struct PrefillLayout {
+    static constexpr int TILE = 16 * D * (int)sizeof(T);
+    static constexpr size_t STAGES = (size_t)S * 2 * TILE;
+    static constexpr size_t OFF_BARS = STAGES;                       // full[S], empty[S]
+    static constexpr size_t OFF_OK = OFF_BARS + (size_t)2 * S * 8;    // int valid[S]
+    static constexpr size_t BYTES = (OFF_OK + (size_t)S * 4 + 15) / 16 * 16 + 1024;
+    static_assert(STAGES % 1024 == 0, "1024-byte aligned tiles");
+};
+
+#ifndef PA_PREFILL_BLOCKS_PER_SM
+#define PA_PREFILL_BLOCKS_PER_SM 3
+#endif
+#ifndef PA_PREFILL_WAVES
+#define PA_PREFILL_WAVES 4
+#endif
+
+template <typename T, int D, int G, int NWC, int S>
+__global__ void __launch_bounds__((NWC + 1) * 32, PA_PREFILL_BLOCKS_PER_SM)
+prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
+    static_assert(sizeof(T) == 2, "16-bit caches");
+    using W = WarpAttnTC16<T, D>;
+    using Lay = PrefillLayout<T, D, NWC, S>;
+    constexpr int TILE = Lay::TILE;
+    constexpr int ROWS = 16 * NWC;                 // query rows of one work item
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);
+    uint64_t *empty = full + S;
+    int *valid = reinterpret_cast<int *>(smem + Lay::OFF_OK);
+    __shared__ int abort_flag;                     // a wait timed out: everyone stops
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
+    const int cap = p.max_blocks * 16;
+
+    if (tid == 0) {
+        prefetch_tensormap(&p.tmap_k);
+        prefetch_tensormap(&p.tmap_v);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    // the caches (and q, out) only after the kernel before this one is done
+    grid_dependency_wait();
+
+    // Work items (row group, sequence, KV head), last row groups first, dealt
+    // to the resident blocks in turn; the ring of stages runs on across items,
+    // so the producer streams the next item while the consumers finish one.
+    const long long items = (long long)groups * B * Hkv;
+    long long kglob = 0;                           // blocks through the ring so far
+    const uint64_t pol = policy_evict_last();      // the sequence's other groups reread them
+    W wa;
+    wa.init(lane);
+    for (long long x = blockIdx.x; x < items; x += gridDim.x) {
+        if (*(volatile int *)&abort_flag) break;
+        const int j = (int)(x % Hkv);
+        const int s = (int)((x / Hkv) % B);
+        const int grp = groups - 1 - (int)(x / ((long long)Hkv * B));
+        const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
+        const int nq = q1 - q0;
+        const int L = p.seq_lens[s];
+        // sequences with fewer rows are the persistent kernel's, which flags bad ranges
+        if (nq < 0 || nq * G < p.mq_split_rows || grp * ROWS >= nq * G) continue;
+        if (q0 < 0 || q1 > p.num_q_rows || nq > p.max_query_len || L < nq || L > cap) {
+            if (grp == 0 && j == 0 && tid == 0) set_error(p.err, ERR_SEQ_LEN);
+            continue;
+        }
+        const int last_row = min(grp * ROWS + ROWS, nq * G) - 1;
+        const int nb = (L - nq + last_row / G) / 16 + 1;   // through the group's last position
+
+        if (warp == NWC) {
+            // ---- producer: one lane streams the item's blocks through the ring
+            if (lane == 0) {
+                const int32_t *tab = p.block_tables + (long long)s * p.max_blocks;
+                for (int k = 0; k < nb; ++k) {
+                    const long long kk = kglob + k;
+                    const int st = (int)(kk % S);
+                    if (kk >= S &&
+                        !mbar_wait_bounded(&empty[st], (uint32_t)(((kk / S) - 1) & 1), p.err)) {
+                        abort_flag = 1;
+                        kglob += k;                // what was issued
+                        goto producer_done;
+                    }
+                    const int pb = tab[k];
+                    if (pb < 0 || (long long)pb >= p.num_blocks) {
+                        set_error(p.err, ERR_BLOCK_ID);
+                        valid[st] = 0;
+                        mbar_arrive(&full[st]);
+                        continue;
+                    }
+                    valid[st] = 1;
+                    unsigned char *dst = smem + (size_t)st * 2 * TILE;
+                    const int z = pb * Hkv + j;
+                    mbar_arrive_expect_tx(&full[st], 2 * TILE);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        tma_load_3d(dst + h * 2048, &p.tmap_k, h * 64, 0, z, &full[st], pol);
+                        tma_load_3d(dst + TILE + h * 2048, &p.tmap_v, h * 64, 0, z, &full[st], pol);
+                    }
+                }
+            }
+        } else {
+            // ---- consumers: rows g and g+8 of this warp's 16-row tile
+            const int r_lo = grp * ROWS + warp * 16 + (lane >> 2), r_hi = r_lo + 8;
+            auto qrow = [&](int r) -> const T * {
+                if (r >= nq * G) return nullptr;
+                return reinterpret_cast<const T *>(p.q) + (long long)(q0 + r / G) * p.q_seq_stride +
+                       (long long)(j * G + r % G) * D;
+            };
+            wa.reset();
+            wa.load_q(qrow(r_lo), qrow(r_hi), L - nq + r_lo / G, L - nq + r_hi / G);
+            bool ok = true;
+            for (int k = 0; k < nb; ++k) {
+                const long long kk = kglob + k;
+                const int st = (int)(kk % S);
+                const bool got = mbar_wait_bounded(&full[st], (uint32_t)((kk / S) & 1), p.err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (valid[st]) {
+                    const unsigned char *kt = smem + (size_t)st * 2 * TILE;
+                    wa.block(smem_u32(kt), smem_u32(kt + TILE), 16 * k, p.scale_log2,
+                             min(16, L - 16 * k));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+            if (!ok) {
+                if (lane == 0) abort_flag = 1;
+                break;
+            }
+            wa.finish();
+            wa.for_each_result([&](int row, int d, float v0, float v1, bool, float, float) {
+                const int rr = grp * ROWS + warp * 16 + row;
+                T *o = reinterpret_cast<T *>(p.out) +
+                       ((long long)(q0 + rr / G) * H + j * G + rr % G) * D + d;
+                store_pair<T>(o, v0, v1);
+            });
+        }
+        kglob += nb;
+    }
+    if (warp == NWC && lane == 0) {
+    producer_done:
+        // no copy may still be landing when the block exits: wait (bounded) for
+        // the last stages issued
+        for (long long i = (kglob > S ? kglob - S : 0); i < kglob; ++i)
+            mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.err);
+    }
+    __syncthreads();
+}
+
+// Consumer warps and ring stages of the prefill path (16 rows per warp).
+constexpr int PREFILL_NWC = PREFILL_GROUP_ROWS / 16;
+template <typename T, int D>
+__host__ __device__ constexpr int prefill_stages() {
+    return (16 * 1024 * 4) / (2 * 16 * D * (int)sizeof(T));   // 64 KiB of K/V in flight
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_prefill(const DecodeParams &p, int groups, cudaStream_t st) {
+    constexpr int S = prefill_stages<T, D>();
+    using Lay = PrefillLayout<T, D, PREFILL_NWC, S>;
+    constexpr size_t smem = Lay::BYTES;
+    static_assert(smem <= 227 * 1024, "shared memory");
+    auto kern = prefill_kernel<T, D, G, PREFILL_NWC, S>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+    const long long items = (long long)groups * p.num_seqs * p.num_kv_heads;
+    if (items <= 0) return cudaSuccess;
+    static int per_sm[64] = {};                    // resident blocks per SM, per device
+    if (dev >= 0 && dev < 64 && per_sm[dev] == 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (PREFILL_NWC + 1) * 32, smem);
+        if (e != cudaSuccess) return e;
+        per_sm[dev] = n > 0 ? n : 1;
+    }
+    const int sms = sm_count_of_current_device();
+    // a few waves of blocks: the hardware then evens out items of unequal cost
+    const long long resident = (long long)(sms > 0 ? sms : 152) *
+                               ((dev >= 0 && dev < 64) ? per_sm[dev] : 1) * PA_PREFILL_WAVES;
+    const long long blocks = items < resident ? items : resident;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3((PREFILL_NWC + 1) * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, groups);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_prefill(const DecodeParams &p, int D, int G, int groups, cudaStream_t st) {
+#define PA_CASE(DD, GG) \
+    if (D == DD && G == GG) return launch_prefill<T, DD, GG>(p, groups, st);
+    PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
+    PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
+#undef PA_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace pa

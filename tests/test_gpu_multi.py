@@ -188,6 +188,61 @@ def test_multi_padding_entries_never_read(cuda_lib):
 
 
 # ---------------------------------------------------------------------------
+# sequences with 64 or more (token, head) rows: the prefill path (blocks of 64
+# rows sharing one K/V ring), next to sequences on the other path
+# ---------------------------------------------------------------------------
+
+PREFILL_CASES = [(dt, D, G, Hkv) for dt in ("bf16", "f16") for D in (64, 128)
+                 for G, Hkv in ((1, 4), (4, 2), (8, 1))]
+
+
+@pytest.mark.parametrize("dtype,D,G,Hkv", PREFILL_CASES,
+                         ids=[f"{c[0]}-d{c[1]}-g{c[2]}" for c in PREFILL_CASES])
+def test_multi_prefill_path_parity(cuda_lib, dtype, D, G, Hkv):
+    """Slices of 1..150 new tokens over 0..400 cached ones: with G heads per
+    KV head, slices of 64/G tokens or more take the prefill path, the rest the
+    persistent kernel; every row group, ragged tails of groups and blocks."""
+    b = wl.multi_query_batch(600 + D + G, num_seqs=10, min_ctx=0, max_ctx=400,
+                             n_new=[150, 1, 70, 3, 33, 64, 17, 2, 129, 8], num_heads=G * Hkv,
+                             num_kv_heads=Hkv, head_dim=D, dtype=dtype, device="cuda",
+                             keep_seq=False)
+    assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), f"{dtype} d{D} g{G}")
+
+
+def test_multi_prefill_whole_prompt(cuda_lib):
+    """A first chunk of 300 tokens with nothing cached: row i sees 0..i, the
+    first row exactly its own V."""
+    b = wl.multi_query_batch(640, num_seqs=3, min_ctx=0, max_ctx=0, n_new=[300, 97, 16],
+                             num_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+                             device="cuda", keep_seq=False)
+    out = gpu_multi(cuda_lib, b)
+    assert_close(out, oracle_multi(b), "whole prompt")
+    qs = b.meta["query_start"]
+    for s in range(b.num_seqs):
+        blk = int(b.block_tables[s, 0])
+        assert torch.equal(out[qs[s]], b.v_cache[blk, :, 0, :].repeat_interleave(4, dim=0))
+
+
+def test_multi_prefill_block_permutation_bit_identical(cuda_lib):
+    b = wl.multi_query_batch(650, num_seqs=4, min_ctx=10, max_ctx=300, n_new=(40, 120),
+                             num_heads=16, num_kv_heads=4, head_dim=128, dtype="bf16",
+                             device="cuda", keep_seq=False)
+    p = wl.permute_blocks(b, seed=3)
+    p.meta["query_start"] = b.meta["query_start"]
+    assert torch.equal(gpu_multi(cuda_lib, b), gpu_multi(cuda_lib, p))
+
+
+def test_multi_prefill_bad_block_is_flagged(cuda_lib):
+    b = wl.multi_query_batch(660, num_seqs=2, min_ctx=20, max_ctx=60, n_new=[80, 5],
+                             num_heads=8, num_kv_heads=2, head_dim=64, dtype="bf16",
+                             device="cuda", keep_seq=False)
+    bt = b.block_tables.copy()
+    bt[0, 1] = b.num_blocks + 3
+    gpu_multi(cuda_lib, b, block_tables=bt)
+    assert cuda_lib.pa_device_error(clear=True) & cuda_lib.PA_DEVERR_BLOCK_ID
+
+
+# ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences against the oracle
 # ---------------------------------------------------------------------------
 
