@@ -143,7 +143,9 @@ int pa_reshape_and_cache(const void *k, const void *v, void *k_cache,
  *
  * Requirements: block_size == 16; head_dim in {64, 128}; num_heads a
  * multiple of num_kv_heads with G = num_heads/num_kv_heads in {1, 2, 4, 8};
- * num_seqs <= 65535; num_kv_heads <= 65535; k_cache and v_cache 16-byte
+ * num_seqs <= 65535 (batches larger than one thread block orders in shared
+ * memory -- 4096 sequences at head_dim 128 -- run as consecutive slices);
+ * num_kv_heads <= 65535; k_cache and v_cache 16-byte
  * aligned.  num_seqs == 0 launches nothing.
  */
 int pa_decode(void *out, const void *q, const void *k_cache,

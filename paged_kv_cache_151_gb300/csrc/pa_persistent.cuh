@@ -971,7 +971,34 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
     constexpr size_t smem = C::Lay::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory");
     auto kern = decode_persistent_kernel<T, KV, D, G, C::NW, C::S, MODE>;
-    if (p.num_seqs > C::Lay::MAX_SEQS) return cudaErrorNotSupported;
+    if (p.num_seqs > C::Lay::MAX_SEQS) {
+        // more sequences than one block sorts in shared memory: launch on
+        // consecutive slices of the batch (sequences are independent)
+        const int chunk = C::Lay::MAX_SEQS, B = p.num_seqs;
+        for (int a = 0; a < B; a += chunk) {
+            const int n = B - a < chunk ? B - a : chunk;
+            DecodeParams q = p;
+            q.num_seqs = n;
+            q.seq_lens = p.seq_lens + a;
+            q.block_tables = p.block_tables + (long long)a * p.max_blocks;
+            if (MODE == MODE_MULTI) {
+                q.query_start = p.query_start + a;        // rows stay absolute
+            } else {
+                q.q = reinterpret_cast<const T *>(p.q) + (long long)a * p.q_seq_stride;
+                q.out = reinterpret_cast<T *>(p.out) + (long long)a * p.num_heads * D;
+            }
+            if (MODE == MODE_PARTITIONED) {
+                const long long rows = (long long)a * p.num_heads * p.max_parts;
+                q.part_o = p.part_o + rows * D;
+                q.part_m = p.part_m + rows;
+                q.part_l = p.part_l + rows;
+            }
+            const long long ub = (unit_bound * n + B - 1) / B;
+            cudaError_t e = launch_persistent<T, KV, D, G, MODE>(q, ub > 0 ? ub : 1, cluster, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
     static int fitted[64][4];                      // clusters resident per device, per size
     int dev = 0;

@@ -433,9 +433,10 @@ def multi_query_batch(seed: int, *, num_seqs: int, min_ctx: int, max_ctx: int,
     else:
         n = np.asarray(n_new, dtype=np.int64)
     total = ctx + n
-    need = sum(math.ceil(int(L) / BLOCK_SIZE) for L in total)
+    # every sequence gets at least one block (an empty one holds no tokens)
+    need = sum(math.ceil(max(int(L), 1) / BLOCK_SIZE) for L in total)
     fl = FreeList(need + 8, rng)
-    tables = [fl.allocate(int(L)) for L in total]
+    tables = [fl.allocate(max(int(L), 1)) for L in total]
     b = build_batch(f"multi{seed}", ctx_lens=np.maximum(total - 1, 0), num_heads=num_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim, dtype=dtype,
                     num_blocks=need + 8, tables=tables, seed=seed, device=device,

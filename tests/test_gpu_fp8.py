@@ -236,6 +236,13 @@ def test_fp8_step_write_then_decode(cuda_lib):
                  "fp8 step")
 
 
+def test_decode_fp8_batch_larger_than_one_sort(cuda_lib):
+    b = fp8_batch(770, num_seqs=3500, max_len=40, num_heads=8, num_kv_heads=2, head_dim=128)
+    ref = oracle_fp8(b)
+    assert_close(gpu_decode_fp8(cuda_lib, b), ref, "3500 seqs")
+    assert_close(gpu_partitioned_fp8(cuda_lib, b, 32), ref, "3500 seqs split-KV")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled (sequence, head) outputs
 # ---------------------------------------------------------------------------

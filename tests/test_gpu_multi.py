@@ -242,6 +242,15 @@ def test_multi_prefill_bad_block_is_flagged(cuda_lib):
     assert cuda_lib.pa_device_error(clear=True) & cuda_lib.PA_DEVERR_BLOCK_ID
 
 
+def test_multi_batch_larger_than_one_sort(cuda_lib):
+    """More sequences than one thread block orders in shared memory: the batch
+    runs as consecutive slices with absolute query rows."""
+    b = wl.multi_query_batch(670, num_seqs=4500, min_ctx=0, max_ctx=30, n_new=(0, 3),
+                             num_heads=8, num_kv_heads=2, head_dim=64, dtype="bf16",
+                             device="cuda", keep_seq=False)
+    assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), "4500 seqs")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences against the oracle
 # ---------------------------------------------------------------------------

@@ -428,3 +428,16 @@ def test_decode_sees_the_cache_write_it_follows(cuda_lib):
         torch.cuda.synchronize()
         want = v_new.float().repeat_interleave(G, dim=1)
         assert (out.float() - want).abs().max().item() < 0.1, f"step {step}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_batch_larger_than_one_sort(cuda_lib, dtype):
+    """More sequences than one thread block orders in shared memory: the batch
+    runs as consecutive slices.  Checked against the oracle, whole-sequence and
+    split-KV."""
+    b = wl.random_batch(910, num_seqs=5000, max_len=40, num_heads=8, num_kv_heads=2,
+                        head_dim=64, dtype=dtype, device="cuda", new_in_pool=True,
+                        keep_seq=False)
+    ref = oracle_decode(b)
+    assert_close(gpu_decode(cuda_lib, b), ref, dtype, "5000 seqs")
+    assert_close(gpu_partitioned(cuda_lib, b, 16)[0], ref, dtype, "5000 seqs split-KV")
