@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -91,25 +92,38 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(tu: str) -> str:
+    """Hash of one kernel translation unit and every local header it
+    includes, directly or through another header: a recorded DRAM figure
+    stays valid while none of the sources it was compiled from changed."""
     csrc = os.path.join(ROOT, "paged_kv_cache_151_gb300", "csrc")
+    inc = re.compile(rb'^\s*#\s*include\s+"([^"]+)"', re.M)
+    seen, todo = set(), [os.path.normpath(os.path.join(csrc, tu))]
+    while todo:
+        p = todo.pop()
+        if p in seen:
+            continue
+        seen.add(p)
+        with open(p, "rb") as fh:
+            for m in inc.finditer(fh.read()):
+                todo.append(os.path.normpath(os.path.join(os.path.dirname(p), m.group(1).decode())))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for p in sorted(seen):
+        with open(p, "rb") as fh:
+            h.update(os.path.relpath(p, ROOT).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(name: str):
     """DRAM bytes per launch of `name` from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+    was taken on the current sources of that kernel's translation unit;
+    else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d[name]
-        if e.get("kernel_src_sha") != kernel_source_digest():
+        if e.get("kernel_src_sha") != kernel_source_digest(e["tu"]):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:

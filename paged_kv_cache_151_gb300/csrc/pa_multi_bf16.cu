@@ -1,18 +1,13 @@
-// pa_multi_bf16.cu -- persistent kernel and prefill kernel for multi-token queries
-// (several new tokens per sequence attending causally over the paged cache), bf16 storage.
+// pa_multi_bf16.cu -- persistent kernel for multi-token queries (a few new tokens
+// per sequence attending causally over the paged cache), bf16 storage.
 #include "pa_internal.h"
 #include "pa_persistent.cuh"
-#include "pa_prefill.cuh"
 
 namespace pa {
 
 cudaError_t decode_multi_bf16(const DecodeParams &p, int D, int G, long long unit_bound,
                           int cluster, cudaStream_t st) {
     return dispatch_persistent<__nv_bfloat16, MODE_MULTI>(p, D, G, unit_bound, cluster, st);
-}
-
-cudaError_t prefill_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st) {
-    return dispatch_prefill<__nv_bfloat16>(p, D, G, groups, st);
 }
 
 }  // namespace pa
