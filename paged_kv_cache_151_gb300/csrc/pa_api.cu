@@ -86,7 +86,12 @@ cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 g
 // each cluster's block stream over several SMs so that long sequences
 // spread out; partitions are already uniform work units.
 #ifndef PA_DECODE_CLUSTER
-#define PA_DECODE_CLUSTER 4
+#define PA_DECODE_CLUSTER 8
+#endif
+// E4M3 caches run three blocks per SM; clusters of four deal their units
+// more evenly there.
+#ifndef PA_F8_CLUSTER
+#define PA_F8_CLUSTER 4
 #endif
 
 cudaError_t run_persistent(const pa::DecodeParams &p, int dtype, int D, int G, bool partial,
@@ -535,7 +540,7 @@ int decode_fp8_common(void *out, const void *q, const void *k_cache, const void 
     if (!prepare_maps(p, PA_E4M3, head_dim)) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int G = num_heads / num_kv_heads;
-    const int cluster = partial ? 1 : PA_DECODE_CLUSTER;
+    const int cluster = partial ? 1 : PA_F8_CLUSTER;
     cudaError_t e = dtype == PA_BF16
                         ? pa::decode_fp8_bf16(p, head_dim, G, partial, unit_bound, cluster, st)
                         : pa::decode_fp8_f16(p, head_dim, G, partial, unit_bound, cluster, st);

@@ -223,6 +223,25 @@ __device__ __forceinline__ void launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The two halves of cluster_sync(), for work in between: arrive (release)
+// once, and wait (acquire) before the first access to a peer's shared memory.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bring the 128-byte lines of [base, base + bytes) into L2, spread over every
+// thread of the grid (a hint: no data moves into the SM).
+__device__ __forceinline__ void prefetch_l2_range(const void *base, size_t bytes) {
+    const char *b = reinterpret_cast<const char *>(base);
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 128;
+    for (size_t off = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 128; off < bytes; off += stride)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(b + off));
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -192,7 +192,8 @@ struct WarpAttnTC {
     }
 
     // One block: kt, vt are shared-memory addresses of the swizzled tiles.
-    // rows in 1..16; rows past `rows` may hold anything and are ignored.
+    // rows in 1..16; rows past `rows` may hold anything and are ignored (their
+    // scores are masked, their values dropped from the fragments).
     __device__ __forceinline__ void block(uint32_t kt, uint32_t vt, int rows, float scale_log2) {
         // -- scores S^T[g][tok] for tok in {2t, 2t+1} (s0) and {8+2t, 9+2t} (s1)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -250,13 +251,23 @@ struct WarpAttnTC {
             }
         }
 
-        // -- P.V: for each pair of 8-wide d tiles, V^T fragments via ldmatrix.trans
+        // -- P.V: for each pair of 8-wide d tiles, V^T fragments via ldmatrix.trans.
+        // A lane's B fragments hold tokens {2t, 2t+1} (b0, b2) and {8+2t, 9+2t}
+        // (b1, b3), the tokens of its P fragment; V rows past `rows` may hold
+        // anything (NaN included), so their halves are cleared here and 0 * NaN
+        // never reaches the accumulators.
+        const uint32_t vm0 = (tk[0] < rows ? 0x0000ffffu : 0u) | (tk[1] < rows ? 0xffff0000u : 0u);
+        const uint32_t vm1 = (tk[2] < rows ? 0x0000ffffu : 0u) | (tk[3] < rows ? 0xffff0000u : 0u);
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
             // matrices: (tok 0-7, chunk j), (tok 8-15, j), (tok 0-7, j+1), (tok 8-15, j+1)
             const int tok = (mi & 1) * 8 + rr, chunk = j + (mi >> 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + swz_offset(tok, chunk), b0, b1, b2, b3);
+            b0 &= vm0;
+            b1 &= vm1;
+            b2 &= vm0;
+            b3 &= vm1;
             Mma<T>::run(acc[j], pa0, pa2, b0, b1);
             Mma<T>::run(acc[j + 1], pa0, pa2, b2, b3);
         }

@@ -77,7 +77,10 @@ struct PersistentLayout {
     static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * PART_FLOATS * 4;
     static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
     static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
-    static constexpr size_t BYTES = OFF_CTL + 256 + 1024;   // + alignment of the base
+    // control words: arrival counters [NW], scan scratch [NW], warp ranges of
+    // the cluster's stream [16*NW + 1] (clusters of up to 16 blocks)
+    static constexpr size_t CTL_BYTES = ((size_t)(2 * NW + 16 * NW + 1) * 4 + 15) / 16 * 16;
+    static constexpr size_t BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment of the base
     static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
     static_assert(S == 0 || (size_t)S * 2 * TILE_BYTES >= PART_FLOATS * 4,
                   "a warp's stages must hold one partial");
@@ -258,17 +261,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 template <int NT>
-__device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int *scratch,
+__device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int nb_max, int *scratch,
                               int *wtot) {
     constexpr int NW = NT / 32;
+    constexpr int NCH_MAX = CS_MAX_SEQS / 32;
     constexpr int PER = CS_BINS / NT;               // bins per thread in the scan
     static_assert(CS_BINS % NT == 0, "bins per thread");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = (B + 31) >> 5;
-    int *hist = scratch;                            // [nch][CS_BINS]: counts, then offsets
-    int *rin = hist + (CS_MAX_SEQS / 32) * CS_BINS; // [B] rank among equal counts in the chunk
+    const int nbins = nb_max + 1;                   // bins in use (nb_max < CS_BINS)
+    int *hist = scratch;                            // [NCH_MAX][CS_BINS]: counts, then offsets
+    int *rin = hist + NCH_MAX * CS_BINS;            // [B] rank among equal counts in the chunk
     int *larger = rin + CS_MAX_SEQS;                // [CS_BINS] sequences with more blocks
-    for (int i = tid; i < nch * CS_BINS; i += NT) hist[i] = 0;
+    for (int c = 0; c < nch; ++c)
+        for (int b = tid; b < nbins; b += NT) hist[c * CS_BINS + b] = 0;
     __syncthreads();
     for (int c = warp; c < nch; c += NW) {
         const int i = 32 * c + lane;
@@ -283,17 +289,24 @@ __device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int *s
     }
     __syncthreads();
     // per count: offsets of the chunks, and the total; then, highest count
-    // first, the number of sequences above each count
+    // first, the number of sequences above each count.  The chunk counts of
+    // a bin are read together (fixed trip count), so a bin costs one
+    // shared-memory round trip.
     int tot[PER];
     int local = 0;
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-        const int b = CS_BINS - 1 - (tid * PER + e);   // descending counts
+        const int b = nbins - 1 - (tid * PER + e);      // descending counts
         int run = 0;
-        for (int c = 0; c < nch; ++c) {
-            const int x = hist[c * CS_BINS + b];
-            hist[c * CS_BINS + b] = run;
-            run += x;
+        if (b >= 0) {
+            int x[NCH_MAX];
+#pragma unroll
+            for (int c = 0; c < NCH_MAX; ++c) x[c] = c < nch ? hist[c * CS_BINS + b] : 0;
+#pragma unroll
+            for (int c = 0; c < NCH_MAX; ++c) {
+                if (c < nch) hist[c * CS_BINS + b] = run;
+                run += x[c];
+            }
         }
         tot[e] = run;
         local += run;
@@ -302,8 +315,8 @@ __device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int *s
     int before = block_exclusive_scan<NT>(local, wtot, &all);
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-        const int b = CS_BINS - 1 - (tid * PER + e);
-        larger[b] = before;
+        const int b = nbins - 1 - (tid * PER + e);
+        if (b >= 0) larger[b] = before;
         before += tot[e];
     }
     __syncthreads();
@@ -391,13 +404,30 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     const int NWC = C * NW;                  // warps of the cluster
     const int gw = rank * NW + warp;         // this warp's index in the cluster
 
-    // ---- 1. sort the sequences by block count (longest first) ----------------
-    if constexpr (TC) {
-        if (tid == 0) {                            // fetch the descriptors early
+    // ---- 0. barriers, and the first reads after the set-up started early -----
+    if (tid == 0) {
+        if constexpr (TC) {                        // fetch the descriptors early
             prefetch_tensormap(&p.tmap_k);
             prefetch_tensormap(&p.tmap_v);
         }
+        for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
     }
+    if (tid < NW) arrive[tid] = 0;
+    // block tables, and the queries, are read as soon as the set-up is done:
+    // start bringing them into L2 (at most 4 MiB of each; L2 is coherent, so
+    // this is safe even while the previous kernel may still write q)
+    {
+        constexpr size_t PF_MAX = (size_t)4 << 20;
+        const size_t bt_bytes = (size_t)B * p.max_blocks * 4;
+        const size_t q_rows = MQ ? (size_t)p.num_q_rows : (size_t)B;   // rows of H x D
+        const size_t q_bytes =
+            q_rows > 0 ? ((q_rows - 1) * p.q_seq_stride + (size_t)H * D) * sizeof(T) : 0;
+        prefetch_l2_range(p.block_tables, bt_bytes < PF_MAX ? bt_bytes : PF_MAX);
+        prefetch_l2_range(p.q, q_bytes < PF_MAX ? q_bytes : PF_MAX);
+    }
+
+    // ---- 1. sort the sequences by block count (longest first) ----------------
     // multi-token queries: rows query_start[s] .. query_start[s+1]-1 belong to
     // sequence s; a range outside its bounds is flagged and gets no rows
     auto mq_valid = [&](int s, int L) -> bool {
@@ -437,7 +467,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                   "the stage region holds the counting sort's scratch");
     if (B <= CS_MAX_SEQS && nb_max < CS_BINS) {
         int *cs = reinterpret_cast<int *>(sort_tmp + Bp);
-        counting_sort<NT>(keys, sort_tmp, B, cs, wtot);
+        counting_sort<NT>(keys, sort_tmp, B, nb_max, cs, wtot);
         keys = sort_tmp;
     } else {
         keys = sort_keys<NT>(keys, sort_tmp, Bp);
@@ -569,15 +599,12 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             bound[g] = real;
         }
     }
-    if (tid < NW) arrive[tid] = 0;
-    if (tid == 0) {
-        for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
-        fence_mbar_init();
-    }
     // the sort scratch in the stage region is overwritten by bulk copies next
     fence_proxy_async_smem();
     __syncthreads();
-    if (C > 1) cluster_sync();                     // peers' counters are initialised
+    // this block's arrival counters are initialised; peers wait for that
+    // (cluster_wait below) before their first access to them
+    if (C > 1) cluster_arrive();
 
     // ---- 4. stream this warp's range of the cluster's blocks ------------------
     auto range_lo = [&](int g) -> int { return bound[g]; };
@@ -752,13 +779,106 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         }
     };
 
-    // Leave unit `ui`: park this warp's partial; the last warp of the unit
-    // merges every partial of the unit (in warp order) and writes the result.
-    auto leave_unit = [&](int ui) {
+    // Merge every partial of unit `ui` (in warp order) and write the unit's
+    // result; run by the last of the unit's warps to arrive.
+    auto merge_unit = [&](int ui) {
+        const UnitRec u = units[ui];
+        const int g_first = owner(cum[ui]), g_last = owner(cum[ui] + u.nb - 1);
+        {
+            // Merge the unit's partials in warp order with a running maximum.
+            // A lane owns chunks lane, lane + 32, ... (E outputs each), taken
+            // CG at a time; all loads of one partial for those chunks are
+            // issued before any is used, so each partial costs one round trip
+            // to cluster shared memory rather than one per load.
+            constexpr int NCH = ROWS * (D / E);
+            constexpr int CPL = (NCH + 31) / 32;
+            constexpr int CG = CPL < 16 / E ? CPL : (16 / E > 0 ? 16 / E : 1);
+#pragma unroll 1
+            for (int c0g = 0; c0g < CPL; c0g += CG) {
+                float M[CG], Ls[CG], O[CG][E];
+                int gg[CG], dd[CG];
+#pragma unroll
+                for (int c = 0; c < CG; ++c) {
+                    const int ch = lane + 32 * (c0g + c);
+                    const int chv = ch < NCH ? ch : 0;     // out-of-range chunks read chunk 0
+                    gg[c] = chv / (D / E);
+                    dd[c] = (chv % (D / E)) * E;
+                    M[c] = -INFINITY;
+                    Ls[c] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) O[c][e] = 0.f;
+                }
+                for (int w = g_first; w <= g_last; ++w) {
+                    if (range_lo(w) == range_lo(w + 1)) continue;
+                    const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
+                    const uint32_t rw = (uint32_t)(w / NW);
+                    float mw[CG], lw[CG];
+                    float4 ow[CG][E / 4];
+#pragma unroll
+                    for (int c = 0; c < CG; ++c) {
+                        mw[c] = ld_dsmem_f32(map_to_rank(pw + ROWS * D + gg[c], rw));
+                        lw[c] = ld_dsmem_f32(map_to_rank(pw + ROWS * D + ROWS + gg[c], rw));
+#pragma unroll
+                        for (int e = 0; e < E / 4; ++e)
+                            ow[c][e] = ld_dsmem_f32x4(map_to_rank(pw + gg[c] * D + dd[c] + 4 * e, rw));
+                    }
+#pragma unroll
+                    for (int c = 0; c < CG; ++c) {
+                        const float Mn = fmaxf(M[c], mw[c]);
+                        if (Mn == -INFINITY) continue;     // nothing seen yet
+                        const float a = M[c] == -INFINITY ? 0.f : ex2(M[c] - Mn);
+                        const float b = mw[c] == -INFINITY ? 0.f : ex2(mw[c] - Mn);
+                        Ls[c] = fmaf(b, lw[c], Ls[c] * a);
+#pragma unroll
+                        for (int e = 0; e < E / 4; ++e) {
+                            O[c][4 * e] = fmaf(b, ow[c][e].x, O[c][4 * e] * a);
+                            O[c][4 * e + 1] = fmaf(b, ow[c][e].y, O[c][4 * e + 1] * a);
+                            O[c][4 * e + 2] = fmaf(b, ow[c][e].z, O[c][4 * e + 2] * a);
+                            O[c][4 * e + 3] = fmaf(b, ow[c][e].w, O[c][4 * e + 3] * a);
+                        }
+                        M[c] = Mn;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < CG; ++c) {
+                    if (c0g + c >= CPL || lane + 32 * (c0g + c) >= NCH) continue;
+                    if (MQ && out_row(u, gg[c]) < 0) continue;
+                    emit(u, gg[c], dd[c], M[c], Ls[c], O[c]);
+                }
+            }
+        }
+        __syncwarp();
+    };
+
+    // Count this warp in at the first warp of unit `ui`; returns the old count.
+    auto arrive_at = [&](int ui) -> int {          // lane 0 only
+        const int g_first = owner(cum[ui]);
+        return atom_add_acq_rel_dsmem(map_to_rank(&arrive[g_first % NW], g_first / NW), 1);
+    };
+    // Warps (with non-empty ranges) that hold a partial of unit `ui`.
+    auto parts_of = [&](int ui) -> int {
+        const int g_first = owner(cum[ui]), g_last = owner(cum[ui] + units[ui].nb - 1);
+        int n = 0;
+        for (int g = g_first; g <= g_last; ++g) n += range_lo(g) < range_lo(g + 1);
+        return n;
+    };
+
+    // The unit this warp's range starts inside of, once this warp has parked
+    // its partial of it: the arrival (a cluster-scope fence and an atomic) is
+    // deferred to the end of the range, when no copies are in flight, so the
+    // fence does not hold up the stream.
+    int pending = -1;
+
+    // Leave unit `ui`.  A unit only this warp touched is written from
+    // registers; otherwise this warp parks its partial, and at the end of the
+    // range (at_end) it arrives for the pending unit and this one; the last
+    // warp of a unit to arrive merges it.
+    auto leave_unit = [&](int ui, bool at_end) {
         wa.finish();
         const UnitRec u = units[ui];
         const int u_lo = cum[ui], u_hi = cum[ui] + u.nb;
         const bool from_before = u_lo < my_lo, to_after = u_hi > my_hi;
+        int shared_unit = -1;
         if (!from_before && !to_after) {
             // a unit only this warp touched: write its result from registers
             const float vsc = v_scale_of(u);
@@ -779,65 +899,34 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                     store_pair<T>(o, v0, v1);
                 }
             });
-            __syncwarp();
-            wa.reset();
-            return;
-        }
-        float *mine = part_of(gw, (from_before && !to_after) ? 0 : 1);
-        // partial layout: O[ROWS][D], M[ROWS], L[ROWS]
-        wa.store_partial(mine + ROWS * D, mine + ROWS * D + ROWS, mine);
-        __syncwarp();
-        bool last = true;
-        const int g_first = owner(u_lo), g_last = owner(u_hi - 1);
-        if (from_before || to_after) {
-            // count this warp in at the unit's first warp
-            int n_part = 0;                        // warps whose range is not empty
-            for (int g = g_first; g <= g_last; ++g) n_part += range_lo(g) < range_lo(g + 1);
-            int old = 0;
-            if (lane == 0) {
-                fence_acq_rel_cluster();
-                old = atom_add_acq_rel_dsmem(map_to_rank(&arrive[g_first % NW], g_first / NW), 1);
-            }
-            old = __shfl_sync(0xffffffffu, old, 0);
-            last = old == n_part - 1;
-            if (last) fence_acq_rel_cluster();
-        }
-        if (last) {
-            for (int ch = lane; ch < ROWS * (D / E); ch += 32) {
-                const int g = ch / (D / E), d0 = (ch % (D / E)) * E;
-                if (MQ && out_row(u, g) < 0) continue;
-                float M = -INFINITY;
-                for (int w = g_first; w <= g_last; ++w) {
-                    if (range_lo(w) == range_lo(w + 1)) continue;
-                    const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
-                    M = fmaxf(M, ld_dsmem_f32(map_to_rank(pw + ROWS * D + g, w / NW)));
-                }
-                float O[E], Ls = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) O[e] = 0.f;
-                if (M != -INFINITY) {
-                    for (int w = g_first; w <= g_last; ++w) {
-                        if (range_lo(w) == range_lo(w + 1)) continue;
-                        const float *pw = part_of(w, (w == g_last && w != g_first) ? 0 : 1);
-                        const uint32_t rw = (uint32_t)(w / NW);
-                        const float mw = ld_dsmem_f32(map_to_rank(pw + ROWS * D + g, rw));
-                        const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-                        Ls = fmaf(f, ld_dsmem_f32(map_to_rank(pw + ROWS * D + ROWS + g, rw)), Ls);
-#pragma unroll
-                        for (int e = 0; e < E; e += 4) {
-                            const float4 a = ld_dsmem_f32x4(map_to_rank(pw + g * D + d0 + e, rw));
-                            O[e] = fmaf(f, a.x, O[e]);
-                            O[e + 1] = fmaf(f, a.y, O[e + 1]);
-                            O[e + 2] = fmaf(f, a.z, O[e + 2]);
-                            O[e + 3] = fmaf(f, a.w, O[e + 3]);
-                        }
-                    }
-                }
-                emit(u, g, d0, M, Ls, O);
-            }
+        } else {
+            float *mine = part_of(gw, (from_before && !to_after) ? 0 : 1);
+            // partial layout: O[ROWS][D], M[ROWS], L[ROWS]
+            wa.store_partial(mine + ROWS * D, mine + ROWS * D + ROWS, mine);
+            shared_unit = ui;
         }
         __syncwarp();
         wa.reset();
+        if (!at_end) {
+            // only the range's first unit can be shared and end inside it
+            if (shared_unit >= 0) pending = shared_unit;
+            return;
+        }
+        if (pending < 0 && shared_unit < 0) return;
+        int old_p = 0, old_u = 0;
+        if (lane == 0) {
+            fence_acq_rel_cluster();               // the parked partials are visible first
+            if (pending >= 0) old_p = arrive_at(pending);
+            if (shared_unit >= 0) old_u = arrive_at(shared_unit);
+        }
+        old_p = __shfl_sync(0xffffffffu, old_p, 0);
+        old_u = __shfl_sync(0xffffffffu, old_u, 0);
+        const bool last_p = pending >= 0 && old_p == parts_of(pending) - 1;
+        const bool last_u = shared_unit >= 0 && old_u == parts_of(shared_unit) - 1;
+        if (last_p || last_u) fence_acq_rel_cluster();
+        if (last_p) merge_unit(pending);
+        if (last_u) merge_unit(shared_unit);
+        pending = -1;
     };
 
     int cur = -1, qnext = -1;                      // unit whose query is loaded ahead
@@ -854,7 +943,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         int ui, pbk;
         of(k, ui, pbk);
         if (ui != cur) {
-            if (cur >= 0) leave_unit(cur);
+            if (cur >= 0) leave_unit(cur, false);
             cur = ui;
             if constexpr (MQ) {
                 // this lane's rows g and g + 8 of the unit's 16-row tile:
@@ -894,13 +983,17 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             unsigned char *Kt = my_stages + (size_t)st * 2 * TILE;
             const int rows = rows_of(k, ui);
             if constexpr (TC) {
-                if (rows < 16) {                   // tail rows hold other tokens' data
-                    if constexpr (F8) W::zero_rows(Kt + TILE, rows, lane);
-                    else WarpAttnTC<T, D, G>::zero_rows(Kt + TILE, rows, lane);
-                    // these generic writes must be ordered before the next
-                    // bulk copy into the stage
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                // tail rows hold other tokens' data: the one-token block math
+                // drops them in registers; the others clear them in the tile
+                if (F8 || MQ) {
+                    if (rows < 16) {
+                        if constexpr (F8) W::zero_rows(Kt + TILE, rows, lane);
+                        else WarpAttnTC<T, D, G>::zero_rows(Kt + TILE, rows, lane);
+                        // these generic writes must be ordered before the next
+                        // bulk copy into the stage
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
                 }
                 if constexpr (MQ) wa.block(smem_u32(Kt), smem_u32(Kt + TILE), pos_of(k, ui), p.scale_log2);
                 else wa.block(smem_u32(Kt), smem_u32(Kt + TILE), rows, unit_scale);
@@ -918,7 +1011,10 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     }
     // a timeout leaves the unit unmerged (its output is not written; the
     // error word says so); otherwise finish the last unit
-    if (ok && cur >= 0) leave_unit(cur);
+    // every block of the cluster has initialised its counters (the only
+    // accesses to peers' shared memory follow)
+    if (C > 1) cluster_wait();
+    if (ok && cur >= 0) leave_unit(cur, true);
 
     // after a timeout: wait (bounded) for this warp's copies still in flight
     if (!ok) {
@@ -999,12 +1095,12 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
         }
         return cudaSuccess;
     }
-    if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
-    static int fitted[64][4];                      // clusters resident per device, per size
+    if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
+    static int fitted[64][5];                      // clusters resident per device, per size
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int ci = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : 3;
+    const int ci = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : cluster == 8 ? 3 : 4;
     int nc = (dev >= 0 && dev < 64) ? fitted[dev][ci] : 0;
 
     cudaLaunchConfig_t cfg = {};
@@ -1025,6 +1121,10 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
     if (nc <= 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        if (cluster > 8) {                         // 16 blocks: beyond the portable size
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
         cfg.gridDim = dim3((unsigned)(cluster * 64), 1, 1);
         e = cudaOccupancyMaxActiveClusters(&nc, kern, &cfg);
         if (e != cudaSuccess) return e;
