@@ -83,10 +83,15 @@ cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 g
 }
 
 // Blocks per cluster of the persistent kernel.  Whole-sequence decode shares
-// each cluster's block stream over several SMs so that long sequences
-// spread out; partitions are already uniform work units.
+// each cluster's block stream over several SMs (over 16-bit caches: four
+// blocks of eight warps, one block per SM) so that long sequences spread out;
+// partitions are already uniform work units.
 #ifndef PA_DECODE_CLUSTER
-#define PA_DECODE_CLUSTER 8
+#define PA_DECODE_CLUSTER 4
+#endif
+// Multi-token queries run blocks of four warps, in clusters of eight.
+#ifndef PA_MULTI_CLUSTER
+#define PA_MULTI_CLUSTER 8
 #endif
 // E4M3 caches run three blocks per SM; clusters of four deal their units
 // more evenly there.
@@ -419,8 +424,8 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
     }
     const long long unit_bound = (long long)num_seqs * num_kv_heads * tiles;
     cudaError_t e = dtype == PA_BF16
-                        ? pa::decode_multi_bf16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st)
-                        : pa::decode_multi_f16(p, head_dim, G, unit_bound, PA_DECODE_CLUSTER, st);
+                        ? pa::decode_multi_bf16(p, head_dim, G, unit_bound, PA_MULTI_CLUSTER, st)
+                        : pa::decode_multi_f16(p, head_dim, G, unit_bound, PA_MULTI_CLUSTER, st);
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -239,92 +239,47 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
     return before + x - v;
 }
 
-// Stable counting sort for small batches: keys[i] = ((0xffff - nb_i) << 16) | i
-// for i < B (B <= 256, every nb_i < CS_BINS); out receives them in
-// ascending order (block count descending, index ascending), exactly what
-// sort_keys gives.  The sequences fall into 32-wide chunks; inside a chunk
-// the lanes with equal block counts find each other with match.any (their
-// rank is the number of such lanes below them); per (chunk, count) the
-// totals turn into offsets by a running sum over chunks, and per count into
-// the number of sequences with more blocks by a scan over counts.
-constexpr int CS_BINS = 512;
-constexpr int CS_MAX_SEQS = 256;
-template <int NT>
-__host__ __device__ constexpr size_t counting_sort_scratch_bytes() {
-    return (size_t)(CS_MAX_SEQS / 32) * CS_BINS * 4 + CS_MAX_SEQS * 4 + CS_BINS * 4;
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    uint32_t m;
-    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-    return m;
-}
-
-template <int NT>
-__device__ void counting_sort(const uint32_t *keys, uint32_t *out, int B, int nb_max, int *scratch,
-                              int *wtot) {
-    constexpr int NW = NT / 32;
-    constexpr int NCH_MAX = CS_MAX_SEQS / 32;
-    constexpr int PER = CS_BINS / NT;               // bins per thread in the scan
-    static_assert(CS_BINS % NT == 0, "bins per thread");
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = (B + 31) >> 5;
-    const int nbins = nb_max + 1;                   // bins in use (nb_max < CS_BINS)
-    int *hist = scratch;                            // [NCH_MAX][CS_BINS]: counts, then offsets
-    int *rin = hist + NCH_MAX * CS_BINS;            // [B] rank among equal counts in the chunk
-    int *larger = rin + CS_MAX_SEQS;                // [CS_BINS] sequences with more blocks
-    for (int c = 0; c < nch; ++c)
-        for (int b = tid; b < nbins; b += NT) hist[c * CS_BINS + b] = 0;
-    __syncthreads();
-    for (int c = warp; c < nch; c += NW) {
-        const int i = 32 * c + lane;
-        const bool valid = i < B;
-        const int nb = valid ? 0xffff - (int)(keys[i] >> 16) : CS_BINS;   // CS_BINS: no bin
-        const uint32_t m = __match_any_sync(0xffffffffu, nb);
-        if (valid) {
-            const uint32_t below = m & lanemask_lt();
-            rin[i] = __popc(below);
-            if (below == 0) hist[c * CS_BINS + nb] = __popc(m);
-        }
-    }
-    __syncthreads();
-    // per count: offsets of the chunks, and the total; then, highest count
-    // first, the number of sequences above each count.  The chunk counts of
-    // a bin are read together (fixed trip count), so a bin costs one
-    // shared-memory round trip.
-    int tot[PER];
-    int local = 0;
+// Ascending sort of 32*EPT keys (distinct values; `in` padded with
+// 0xffffffff) by one warp, EPT keys per lane in registers: a bitonic network
+// whose strides inside a lane are register swaps and whose longer strides
+// are shuffles, so no step waits on shared memory or a block barrier.
+template <int EPT>
+__device__ __forceinline__ void warp_bitonic_sort(const uint32_t *in, uint32_t *out) {
+    constexpr int N = 32 * EPT;
+    const int lane = threadIdx.x & 31;
+    uint32_t v[EPT];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        const int b = nbins - 1 - (tid * PER + e);      // descending counts
-        int run = 0;
-        if (b >= 0) {
-            int x[NCH_MAX];
+    for (int e = 0; e < EPT; ++e) v[e] = in[lane * EPT + e];
 #pragma unroll
-            for (int c = 0; c < NCH_MAX; ++c) x[c] = c < nch ? hist[c * CS_BINS + b] : 0;
+    for (int k = 2; k <= N; k <<= 1) {
 #pragma unroll
-            for (int c = 0; c < NCH_MAX; ++c) {
-                if (c < nch) hist[c * CS_BINS + b] = run;
-                run += x[c];
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j < EPT) {
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const int e2 = e ^ j;
+                    if (e2 > e) {
+                        const bool up = ((lane * EPT + e) & k) == 0;
+                        const uint32_t x = v[e], y = v[e2];
+                        const bool swap = (x > y) == up;
+                        v[e] = swap ? y : x;
+                        v[e2] = swap ? x : y;
+                    }
+                }
+            } else {
+                const int m = j / EPT;                 // partner lane offset
+                const bool lower = (lane & m) == 0;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const bool up = ((lane * EPT + e) & k) == 0;
+                    const uint32_t y = __shfl_xor_sync(0xffffffffu, v[e], m);
+                    v[e] = (lower == up) ? min(v[e], y) : max(v[e], y);
+                }
             }
         }
-        tot[e] = run;
-        local += run;
     }
-    int all;
-    int before = block_exclusive_scan<NT>(local, wtot, &all);
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        const int b = nbins - 1 - (tid * PER + e);
-        if (b >= 0) larger[b] = before;
-        before += tot[e];
-    }
-    __syncthreads();
-    for (int i = tid; i < B; i += NT) {
-        const int nb = 0xffff - (int)(keys[i] >> 16);
-        out[larger[nb] + hist[(i >> 5) * CS_BINS + nb] + rin[i]] = keys[i];
-    }
-    __syncthreads();
+    for (int e = 0; e < EPT; ++e) out[lane * EPT + e] = v[e];
 }
 
 // 16-bit caches use the tensor cores (pa_mma.cuh) on swizzled tiles placed
@@ -335,6 +290,12 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
 #ifndef PA_DECODE_PDL
 #define PA_DECODE_PDL 1
+#endif
+
+// Tiles a warp asks L2 for beyond its ring of stages: when few warps are
+// left streaming, each keeps more bytes in flight.
+#ifndef PA_L2_AHEAD
+#define PA_L2_AHEAD 0
 #endif
 
 #ifndef PA_F8_BLOCKS_PER_SM
@@ -349,15 +310,27 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
 // T: the type of q and out; KV: the caches' storage (T, or E4M3 codes with
 // per-KV-head scales, 16-bit T only).
-// Blocks per SM the kernel is built for: E4M3 tiles are half the bytes, so
-// three blocks (12 warps) fit and hide more latency; 16-bit tiles, two.
-template <typename KV>
+// Warps per block: whole-sequence decode over 16-bit caches runs one block of
+// eight warps per SM (the set-up, done once per block, then serves all eight);
+// the other modes run blocks of four.
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 8
+#endif
+template <typename KV, int MODE>
+__host__ __device__ constexpr int persistent_warps() {
+    return (sizeof(KV) == 2 && MODE == MODE_DECODE) ? PA_DECODE_WARPS : 4;
+}
+
+// Blocks per SM the kernel is built for: eight warps of 16-bit tiles per SM
+// (one block of eight or two of four); E4M3 tiles are half the bytes, so
+// three blocks of four fit and hide more latency.
+template <typename KV, int NW>
 __host__ __device__ constexpr int persistent_blocks_per_sm() {
-    return sizeof(KV) == 1 ? PA_F8_BLOCKS_PER_SM : 2;
+    return sizeof(KV) == 1 ? PA_F8_BLOCKS_PER_SM : (NW >= 8 ? 1 : 2);
 }
 
 template <typename T, typename KV, int D, int G, int NW, int S, int MODE>
-__global__ void __launch_bounds__(NW * 32, persistent_blocks_per_sm<KV>())
+__global__ void __launch_bounds__(NW * 32, (persistent_blocks_per_sm<KV, NW>()))
 decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     constexpr bool TC = use_tc<T>();
     constexpr bool F8 = std::is_same<KV, e4m3>::value;
@@ -440,7 +413,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     int *start = reinterpret_cast<int *>(stages + (size_t)Bp * 4);   // [B]
     int *lens = start + B;                                           // [B], clamped
     uint32_t *sort_tmp = reinterpret_cast<uint32_t *>(lens + ((B + 3) & ~3));  // [Bp] if Bp <= 2*NT
-    int nb_max = 0;                                // this thread's largest block count
     for (int i = tid; i < Bp; i += NT) {
         uint32_t key = 0xffffffffu;
         if (i < B) {
@@ -452,22 +424,20 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
                 if (blockIdx.x == 0 && !mq_valid(i, L)) set_error(p.err, ERR_SEQ_LEN);
             }
             const int nb = (L + 15) >> 4;
-            nb_max = max(nb_max, nb);
             key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
         }
         keys[i] = key;
     }
-    nb_max = __reduce_max_sync(0xffffffffu, nb_max);
-    if (lane == 0) wtot[warp] = nb_max;
     __syncthreads();
-#pragma unroll
-    for (int w = 0; w < NW; ++w) nb_max = max(nb_max, wtot[w]);
-    __syncthreads();
-    static_assert(Lay::STAGES >= 4096 + counting_sort_scratch_bytes<NT>(),
-                  "the stage region holds the counting sort's scratch");
-    if (B <= CS_MAX_SEQS && nb_max < CS_BINS) {
-        int *cs = reinterpret_cast<int *>(sort_tmp + Bp);
-        counting_sort<NT>(keys, sort_tmp, B, nb_max, cs, wtot);
+    static_assert(Lay::STAGES >= 16 * 256, "the stage region holds the sort's scratch");
+    if (Bp <= 256) {
+        // up to 256 sequences: one warp sorts in registers (the others wait)
+        if (warp == 0) {
+            if (Bp == 256) warp_bitonic_sort<8>(keys, sort_tmp);
+            else if (Bp == 128) warp_bitonic_sort<4>(keys, sort_tmp);
+            else warp_bitonic_sort<2>(keys, sort_tmp);
+        }
+        __syncthreads();
         keys = sort_tmp;
     } else {
         keys = sort_keys<NT>(keys, sort_tmp, Bp);
@@ -714,12 +684,26 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         }
     }
 
+    // the K and V tiles of block k into L2 (whole tiles, lane 0)
+    auto prefetch = [&](int k) {                   // warp-uniform k
+        if (k >= n_mine) return;
+        int ui, pbk;
+        of(k, ui, pbk);
+        if (lane == 0 && pbk >= 0 && (long long)pbk < p.num_blocks) {
+            const size_t off = ((size_t)pbk * Hkv + units[ui].j) * TILE;
+            bulk_prefetch_l2(kbase + off, (uint32_t)TILE);
+            bulk_prefetch_l2(vbase + off, (uint32_t)TILE);
+        }
+    };
+
     const int pre = n_mine < S ? n_mine : S;
     for (int k = 0; k < pre; ++k) {
         int ui, pbk;
         of(k, ui, pbk);
         if (lane == 0) issue(k, ui, pbk);
     }
+#pragma unroll 1
+    for (int a = 0; a < PA_L2_AHEAD; ++a) prefetch(S + a);
 
     W wa;
     wa.init(lane);
@@ -1007,6 +991,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             int uin, pbn;
             of(kn, uin, pbn);
             if (lane == 0) issue(kn, uin, pbn);
+            if (PA_L2_AHEAD > 0) prefetch(kn + PA_L2_AHEAD);
         }
     }
     // a timeout leaves the unit unmerged (its output is not written; the
@@ -1033,21 +1018,21 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
 #ifndef PA_STAGE_KB
 #define PA_STAGE_KB 16
 #endif
-template <typename T, typename KV, int D, int G, int MODE>
+template <typename T, typename KV, int D, int G, int MODE, int NW>
 __host__ __device__ constexpr int persistent_stages() {
     int s = PA_STAGE_KB * 1024 / (int)(2 * 16 * D * sizeof(KV));
     s = s < 2 ? 2 : (s > 6 ? 6 : s);
-    const size_t cap = (size_t)(227 / persistent_blocks_per_sm<KV>()) * 1024;
-    while (s > 2 && PersistentLayout<T, KV, D, G, 4, 0, MODE>::BYTES +
-                            (size_t)4 * s * (2 * 16 * D * sizeof(KV) + 8) > cap)
+    const size_t cap = (size_t)(227 / persistent_blocks_per_sm<KV, NW>()) * 1024;
+    while (s > 2 && PersistentLayout<T, KV, D, G, NW, 0, MODE>::BYTES +
+                            (size_t)NW * s * (2 * 16 * D * sizeof(KV) + 8) > cap)
         --s;
     return s;
 }
 
 template <typename T, typename KV, int D, int G, int MODE>
 struct PersistentConfig {
-    static constexpr int NW = 4;
-    static constexpr int S = persistent_stages<T, KV, D, G, MODE>();
+    static constexpr int NW = persistent_warps<KV, MODE>();
+    static constexpr int S = persistent_stages<T, KV, D, G, MODE, NW>();
     using Lay = PersistentLayout<T, KV, D, G, NW, S, MODE>;
 };
 
