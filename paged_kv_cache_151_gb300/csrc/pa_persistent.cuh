@@ -77,9 +77,10 @@ struct PersistentLayout {
     static constexpr size_t OFF_UNITS = OFF_PARTS + (size_t)NW * PART_FLOATS * 4;
     static constexpr size_t OFF_CUM = OFF_UNITS + (size_t)NU_MAX * sizeof(UnitRec);
     static constexpr size_t OFF_CTL = (OFF_CUM + (size_t)(NU_MAX + 1) * 4 + 15) / 16 * 16;
-    // control words: arrival counters [NW], scan scratch [NW], warp ranges of
-    // the cluster's stream [16*NW + 1] (clusters of up to 16 blocks)
-    static constexpr size_t CTL_BYTES = ((size_t)(2 * NW + 16 * NW + 1) * 4 + 15) / 16 * 16;
+    // control words: arrival counters [NW], scan scratch [2*NW] (64-bit
+    // values), warp ranges of the cluster's stream [16*NW + 1] (clusters of up
+    // to 16 blocks)
+    static constexpr size_t CTL_BYTES = ((size_t)(3 * NW + 16 * NW + 1) * 4 + 15) / 16 * 16;
     static constexpr size_t BYTES = OFF_CTL + CTL_BYTES + 1024;   // + alignment of the base
     static_assert(STAGES % 1024 == 0, "stage buffers: 1024-byte aligned boxes");
     static_assert(S == 0 || (size_t)S * 2 * TILE_BYTES >= PART_FLOATS * 4,
@@ -239,6 +240,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *wtot, int *total
     return before + x - v;
 }
 
+// The same for one 64-bit value per thread; wtot holds NT/32 values.
+template <int NT>
+__device__ __forceinline__ long long block_exclusive_scan64(long long v, long long *wtot,
+                                                            long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    long long before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const long long t = wtot[w];
+        if (w < warp) before += t;
+        all += t;
+    }
+    __syncthreads();
+    *total = all;
+    return before + x - v;
+}
+
 // Ascending sort of 32*EPT keys (distinct values; `in` padded with
 // 0xffffffff) by one warp, EPT keys per lane in registers: a bitonic network
 // whose strides inside a lane are register swaps and whose longer strides
@@ -366,8 +392,8 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     int *ctl = reinterpret_cast<int *>(smem + Lay::OFF_CTL);
     int *arrive = ctl;                       // [NW] warps done with the unit that
                                              //      starts in this warp's range
-    int *wtot = ctl + NW;                    // [NW] scan scratch
-    int *bound = ctl + 2 * NW;               // [C*NW + 1] warp ranges of the stream
+    int *wtot = ctl + NW;                    // [2*NW] scan scratch (NW 64-bit values)
+    int *bound = ctl + 3 * NW;               // [C*NW + 1] warp ranges of the stream
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
@@ -443,7 +469,11 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         keys = sort_keys<NT>(keys, sort_tmp, Bp);
     }
 
-    // ---- 2. number the units: exclusive scan of units per sorted sequence -----
+    // ---- 2. number the units ------------------------------------------------
+    // One-token decode gives every sequence Hkv units, so unit r belongs to
+    // sorted position r / Hkv; otherwise an exclusive scan of the units per
+    // sorted sequence, searched per unit below.
+    constexpr bool UNIFORM = !PARTIAL && !MQ;
     auto units_of = [&](int pos) -> int {          // pos < B
         const int nb = 0xffff - (int)(keys[pos] >> 16);
         if constexpr (MQ) {
@@ -455,7 +485,9 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         return PARTIAL ? Hkv * ((nb + PB - 1) / PB) : Hkv;
     };
     int U = 0;
-    {
+    if constexpr (UNIFORM) {
+        U = B * Hkv;
+    } else {
         const int per = (B + NT - 1) / NT;
         const int lo = min(B, tid * per), hi = min(B, lo + per);
         int sum = 0;
@@ -465,8 +497,8 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             start[i] = run;
             run += units_of(i);
         }
+        __syncthreads();
     }
-    __syncthreads();
 
     // ---- 3. this cluster's units (snake over the ranks) -----------------------
     const int NC = gridDim.x / C, me = blockIdx.x / C;
@@ -481,16 +513,25 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         if (tid == 0) set_error(p.err, ERR_SEQ_LEN);
         nu = NU_MAX;
     }
-    for (int q = tid; q < nu; q += NT) {
-        const int r = (int)rank_of(q);
-        int lo = 0, hi = B - 1;                    // last pos with start[pos] <= r
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (start[mid] <= r) lo = mid; else hi = mid - 1;
+    static_assert(NU_MAX <= NT, "one thread per unit");
+    int nb_q = 0;                                  // thread q builds unit q
+    if (tid < nu) {
+        const int r = (int)rank_of(tid);
+        int pos, local;
+        if constexpr (UNIFORM) {
+            pos = r / Hkv;
+            local = r - pos * Hkv;
+        } else {
+            int lo = 0, hi = B - 1;                // last pos with start[pos] <= r
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (start[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            pos = lo;
+            local = r - start[lo];
         }
-        const int s = (int)(keys[lo] & 0xffffu);
-        const int nb = 0xffff - (int)(keys[lo] >> 16);
-        const int local = r - start[lo];
+        const int s = (int)(keys[pos] & 0xffffu);
+        const int nb = 0xffff - (int)(keys[pos] >> 16);
         UnitRec u;
         u.s = s;
         u.L = lens[s];
@@ -520,55 +561,40 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             u.lb0 = 0;
             u.nb = nb;
         }
-        units[q] = u;
+        units[tid] = u;
+        nb_q = u.nb;
     }
-    __syncthreads();
-    if (warp == 0) {                               // cum[q] = blocks before unit q
-        int run = 0;
-        for (int base = 0; base < nu; base += 32) {
-            const int q = base + lane;
-            const int v = q < nu ? units[q].nb : 0;
-            int x = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (q < nu) cum[q] = run + x - v;
-            run += __shfl_sync(0xffffffffu, x, 31);
-        }
-        if (lane == 0) cum[nu] = run;
-        __syncwarp();
-        // Split the stream into C*NW ranges of equal cost, a block costing 4
-        // and each unit a warp enters a further UNIT_COST (quarter blocks):
-        // in a virtual stream where every unit starts with UNIT_COST/4 header
-        // blocks, cut at equal steps and move each cut to a real block.
-        int nz = 0;                                // units with blocks (they come first)
-        for (int base = 0; base < nu; base += 32) {
-            const int q = base + lane;
-            nz += __popc(__ballot_sync(0xffffffffu, q < nu && units[q].nb > 0));
-        }
-        const long long vtot = 4LL * run + (long long)nz * UNIT_COST;
-        auto vstart = [&](int q) -> long long {
-            return 4LL * cum[q] + (long long)min(q, nz) * UNIT_COST;
-        };
-        for (int g = lane; g <= NWC; g += 32) {
-            int real = run;
-            if (g < NWC && nz > 0) {
-                const long long v = (long long)g * vtot / NWC;
-                int lo = 0, hi = nz - 1;           // last unit starting at or before v
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (vstart(mid) <= v) lo = mid; else hi = mid - 1;
-                }
-                const long long o = v - vstart(lo);
-                real = o < UNIT_COST ? cum[lo]
-                                     : min(cum[lo + 1], cum[lo] + (int)((o - UNIT_COST) / 4));
-            }
-            if (g == 0) real = 0;
-            bound[g] = real;
+    // cum[q] = blocks before unit q.  The stream is split into C*NW ranges of
+    // equal cost, a block costing 4 and each unit a warp enters a further
+    // UNIT_COST (quarter blocks): in a virtual stream where every unit with
+    // blocks starts with UNIT_COST/4 header blocks, the cuts fall at equal
+    // steps, and the thread of the unit a cut falls in moves it to a real block.
+    long long tot;
+    const long long ex = block_exclusive_scan64<NT>(((long long)(nb_q > 0) << 32) | (unsigned)nb_q,
+                                                    reinterpret_cast<long long *>(wtot), &tot);
+    const int cum_q = (int)(ex & 0xffffffffLL), nz_before = (int)(ex >> 32);
+    const int run = (int)(tot & 0xffffffffLL), nz = (int)(tot >> 32);
+    if (tid < nu) cum[tid] = cum_q;
+    if (tid == 0) {
+        cum[nu] = run;
+        bound[0] = 0;
+        bound[NWC] = run;
+    }
+    const long long vtot = 4LL * run + (long long)nz * UNIT_COST;
+    if (tid < nu && nb_q > 0) {
+        const long long vs = 4LL * cum_q + (long long)nz_before * UNIT_COST;
+        const long long ve = vs + 4LL * nb_q + UNIT_COST;
+        // cuts g with floor(g * vtot / NWC) in [vs, ve)
+        int g = (int)((vs * NWC + vtot - 1) / vtot);
+        const long long g_end = (ve * NWC + vtot - 1) / vtot;
+        if (g < 1) g = 1;
+        for (; g < g_end && g < NWC; ++g) {
+            const long long o = (long long)g * vtot / NWC - vs;
+            bound[g] = o < UNIT_COST ? cum_q : min(cum_q + nb_q, cum_q + (int)((o - UNIT_COST) / 4));
         }
     }
+    if (nz == 0)
+        for (int g = 1 + tid; g < NWC; g += NT) bound[g] = run;
     // the sort scratch in the stage region is overwritten by bulk copies next
     fence_proxy_async_smem();
     __syncthreads();
