@@ -177,12 +177,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
-// Start bringing [src, src + bytes) into L2 (bulk; src 16-byte aligned,
-// bytes a multiple of 16); a hint: nothing is written to shared memory.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
-}
-
 // Bring a tensor-map descriptor (kernel parameter) into the TMA unit's cache.
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");

@@ -318,12 +318,6 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 #define PA_DECODE_PDL 1
 #endif
 
-// Tiles a warp asks L2 for beyond its ring of stages: when few warps are
-// left streaming, each keeps more bytes in flight.
-#ifndef PA_L2_AHEAD
-#define PA_L2_AHEAD 0
-#endif
-
 #ifndef PA_F8_BLOCKS_PER_SM
 #define PA_F8_BLOCKS_PER_SM 3
 #endif
@@ -413,6 +407,10 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         fence_mbar_init();
     }
     if (tid < NW) arrive[tid] = 0;
+    // this block's arrival counters are initialised; peers wait for that
+    // (cluster_wait below) before their first access to them.  Arriving now,
+    // before any other memory traffic, keeps the release cheap.
+    if (C > 1) cluster_arrive();
     // block tables, and the queries, are read as soon as the set-up is done:
     // start bringing them into L2 (at most 4 MiB of each; L2 is coherent, so
     // this is safe even while the previous kernel may still write q)
@@ -598,9 +596,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     // the sort scratch in the stage region is overwritten by bulk copies next
     fence_proxy_async_smem();
     __syncthreads();
-    // this block's arrival counters are initialised; peers wait for that
-    // (cluster_wait below) before their first access to them
-    if (C > 1) cluster_arrive();
 
     // ---- 4. stream this warp's range of the cluster's blocks ------------------
     auto range_lo = [&](int g) -> int { return bound[g]; };
@@ -710,26 +705,12 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         }
     }
 
-    // the K and V tiles of block k into L2 (whole tiles, lane 0)
-    auto prefetch = [&](int k) {                   // warp-uniform k
-        if (k >= n_mine) return;
-        int ui, pbk;
-        of(k, ui, pbk);
-        if (lane == 0 && pbk >= 0 && (long long)pbk < p.num_blocks) {
-            const size_t off = ((size_t)pbk * Hkv + units[ui].j) * TILE;
-            bulk_prefetch_l2(kbase + off, (uint32_t)TILE);
-            bulk_prefetch_l2(vbase + off, (uint32_t)TILE);
-        }
-    };
-
     const int pre = n_mine < S ? n_mine : S;
     for (int k = 0; k < pre; ++k) {
         int ui, pbk;
         of(k, ui, pbk);
         if (lane == 0) issue(k, ui, pbk);
     }
-#pragma unroll 1
-    for (int a = 0; a < PA_L2_AHEAD; ++a) prefetch(S + a);
 
     W wa;
     wa.init(lane);
@@ -1017,7 +998,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             int uin, pbn;
             of(kn, uin, pbn);
             if (lane == 0) issue(kn, uin, pbn);
-            if (PA_L2_AHEAD > 0) prefetch(kn + PA_L2_AHEAD);
         }
     }
     // a timeout leaves the unit unmerged (its output is not written; the
