@@ -89,9 +89,10 @@ cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 g
 #ifndef PA_DECODE_CLUSTER
 #define PA_DECODE_CLUSTER 4
 #endif
-// Multi-token queries run blocks of four warps, in clusters of eight.
+// Multi-token queries over 16-bit caches: blocks of eight warps, clusters of
+// four, like whole-sequence decode.
 #ifndef PA_MULTI_CLUSTER
-#define PA_MULTI_CLUSTER 8
+#define PA_MULTI_CLUSTER 4
 #endif
 // E4M3 caches run three blocks per SM; clusters of four deal their units
 // more evenly there.

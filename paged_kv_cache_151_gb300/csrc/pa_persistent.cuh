@@ -330,15 +330,15 @@ __host__ __device__ constexpr bool use_tc() { return sizeof(T) == 2; }
 
 // T: the type of q and out; KV: the caches' storage (T, or E4M3 codes with
 // per-KV-head scales, 16-bit T only).
-// Warps per block: whole-sequence decode over 16-bit caches runs one block of
-// eight warps per SM (the set-up, done once per block, then serves all eight);
-// the other modes run blocks of four.
+// Warps per block: whole-sequence decode and multi-token queries over 16-bit
+// caches run one block of eight warps per SM (the set-up, done once per block,
+// then serves all eight); partitions, fp32 and E4M3 caches run blocks of four.
 #ifndef PA_DECODE_WARPS
 #define PA_DECODE_WARPS 8
 #endif
 template <typename KV, int MODE>
 __host__ __device__ constexpr int persistent_warps() {
-    return (sizeof(KV) == 2 && MODE == MODE_DECODE) ? PA_DECODE_WARPS : 4;
+    return (sizeof(KV) == 2 && (MODE == MODE_DECODE || MODE == MODE_MULTI)) ? PA_DECODE_WARPS : 4;
 }
 
 // Blocks per SM the kernel is built for: eight warps of 16-bit tiles per SM
@@ -411,18 +411,6 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     // (cluster_wait below) before their first access to them.  Arriving now,
     // before any other memory traffic, keeps the release cheap.
     if (C > 1) cluster_arrive();
-    // block tables, and the queries, are read as soon as the set-up is done:
-    // start bringing them into L2 (at most 4 MiB of each; L2 is coherent, so
-    // this is safe even while the previous kernel may still write q)
-    {
-        constexpr size_t PF_MAX = (size_t)4 << 20;
-        const size_t bt_bytes = (size_t)B * p.max_blocks * 4;
-        const size_t q_rows = MQ ? (size_t)p.num_q_rows : (size_t)B;   // rows of H x D
-        const size_t q_bytes =
-            q_rows > 0 ? ((q_rows - 1) * p.q_seq_stride + (size_t)H * D) * sizeof(T) : 0;
-        prefetch_l2_range(p.block_tables, bt_bytes < PF_MAX ? bt_bytes : PF_MAX);
-        prefetch_l2_range(p.q, q_bytes < PF_MAX ? q_bytes : PF_MAX);
-    }
 
     // ---- 1. sort the sequences by block count (longest first) ----------------
     // multi-token queries: rows query_start[s] .. query_start[s+1]-1 belong to
@@ -451,6 +439,19 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)i;
         }
         keys[i] = key;
+    }
+    // block tables, and the queries, are read as soon as the set-up is done:
+    // start bringing them into L2 now that seq_lens, which everything waits
+    // for, has arrived (at most 4 MiB of each; L2 is coherent, so this is safe
+    // even while the previous kernel may still write q)
+    {
+        constexpr size_t PF_MAX = (size_t)4 << 20;
+        const size_t bt_bytes = (size_t)B * p.max_blocks * 4;
+        const size_t q_rows = MQ ? (size_t)p.num_q_rows : (size_t)B;   // rows of H x D
+        const size_t q_bytes =
+            q_rows > 0 ? ((q_rows - 1) * p.q_seq_stride + (size_t)H * D) * sizeof(T) : 0;
+        prefetch_l2_range(p.block_tables, bt_bytes < PF_MAX ? bt_bytes : PF_MAX);
+        prefetch_l2_range(p.q, q_bytes < PF_MAX ? q_bytes : PF_MAX);
     }
     __syncthreads();
     static_assert(Lay::STAGES >= 16 * 256, "the stage region holds the sort's scratch");
