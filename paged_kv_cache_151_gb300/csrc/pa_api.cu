@@ -131,14 +131,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // bytes) x 16 rows with the 128-byte swizzle; E4M3 caches in boxes of the
 // whole row (D bytes) x 16 rows with the D-byte swizzle.
 bool encode_cache_map(CUtensorMap *m, const void *base, int64_t num_blocks, int32_t hkv,
-                      int32_t head_dim, int32_t kv_dtype) {
+                      int32_t head_dim, int32_t kv_dtype, uint32_t box_rows = 16) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const bool f8 = kv_dtype == PA_E4M3;
     const cuuint64_t es = f8 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, 16, (cuuint64_t)(num_blocks * hkv)};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * es, (cuuint64_t)head_dim * es * 16};
-    const cuuint32_t box[3] = {f8 ? (cuuint32_t)head_dim : 64u, 16, 1};
+    const cuuint32_t box[3] = {f8 ? (cuuint32_t)head_dim : 64u, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -155,10 +155,18 @@ bool encode_cache_map(CUtensorMap *m, const void *base, int64_t num_blocks, int3
 bool prepare_maps(pa::DecodeParams &p, int32_t kv_dtype, int32_t head_dim) {
     if (kv_dtype == PA_F32) return true;
     if (p.num_blocks <= 0) return true;            // nothing can be read
-    return encode_cache_map(&p.tmap_k, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
-                            kv_dtype) &&
-           encode_cache_map(&p.tmap_v, p.v_cache, p.num_blocks, p.num_kv_heads, head_dim,
-                            kv_dtype);
+    if (!encode_cache_map(&p.tmap_k, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                          kv_dtype) ||
+        !encode_cache_map(&p.tmap_v, p.v_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                          kv_dtype))
+        return false;
+    if (kv_dtype == PA_E4M3) return true;
+    // 8-row boxes: with the 128-byte swizzle they land exactly where rows 0..7
+    // of a 16-row box would
+    return encode_cache_map(&p.tmap_k8, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                            kv_dtype, 8) &&
+           encode_cache_map(&p.tmap_v8, p.v_cache, p.num_blocks, p.num_kv_heads, head_dim,
+                            kv_dtype, 8);
 }
 
 // The persistent kernel reads each query row with 16-byte loads.

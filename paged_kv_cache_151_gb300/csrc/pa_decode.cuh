@@ -80,6 +80,10 @@ struct DecodeParams {
     // of 16 rows x 128 bytes (16-bit) or 16 rows x head_dim bytes (E4M3)
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
+    // 16-bit caches: the same tensors read in boxes of 8 rows, for blocks
+    // holding at most 8 valid tokens (the last block of a sequence)
+    CUtensorMap tmap_k8;
+    CUtensorMap tmap_v8;
 };
 
 // Stages per warp: about 24 KiB of K+V in flight per warp, at least 2.

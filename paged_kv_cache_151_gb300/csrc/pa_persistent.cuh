@@ -402,6 +402,10 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         if constexpr (TC) {                        // fetch the descriptors early
             prefetch_tensormap(&p.tmap_k);
             prefetch_tensormap(&p.tmap_v);
+            if constexpr (!F8) {
+                prefetch_tensormap(&p.tmap_k8);
+                prefetch_tensormap(&p.tmap_v8);
+            }
         }
         for (int i = 0; i < NW * S; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -668,13 +672,18 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             tma_load_3d(dst, &p.tmap_k, 0, 0, z, bar, pol);
             tma_load_3d(dst + TILE, &p.tmap_v, 0, 0, z, bar, pol);
         } else if constexpr (TC) {
-            // whole 16-row tiles, D/64 boxes each for K and V
+            // 16-row tiles, D/64 boxes each for K and V; a block with at most 8
+            // valid tokens takes boxes of 8 rows (the rest of the stage keeps
+            // stale rows, which the block math masks or clears)
             const int z = pbk * Hkv + units[ui].j;
-            mbar_arrive_expect_tx(bar, 2 * TILE);
+            const bool half = rows_of(k, ui) <= 8;
+            mbar_arrive_expect_tx(bar, half ? TILE : 2 * TILE);
+            const CUtensorMap *mk = half ? &p.tmap_k8 : &p.tmap_k;
+            const CUtensorMap *mv = half ? &p.tmap_v8 : &p.tmap_v;
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(dst + h * 2048, &p.tmap_k, h * 64, 0, z, bar, pol);
-                tma_load_3d(dst + TILE + h * 2048, &p.tmap_v, h * 64, 0, z, bar, pol);
+                tma_load_3d(dst + h * 2048, mk, h * 64, 0, z, bar, pol);
+                tma_load_3d(dst + TILE + h * 2048, mv, h * 64, 0, z, bar, pol);
             }
         } else {
             const uint32_t bytes = (uint32_t)(rows_of(k, ui) * ROWB);
