@@ -265,49 +265,6 @@ __device__ __forceinline__ long long block_exclusive_scan64(long long v, long lo
     return before + x - v;
 }
 
-// Ascending sort of 32*EPT keys (distinct values; `in` padded with
-// 0xffffffff) by one warp, EPT keys per lane in registers: a bitonic network
-// whose strides inside a lane are register swaps and whose longer strides
-// are shuffles, so no step waits on shared memory or a block barrier.
-template <int EPT>
-__device__ __forceinline__ void warp_bitonic_sort(const uint32_t *in, uint32_t *out) {
-    constexpr int N = 32 * EPT;
-    const int lane = threadIdx.x & 31;
-    uint32_t v[EPT];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) v[e] = in[lane * EPT + e];
-#pragma unroll
-    for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j < EPT) {
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) {
-                    const int e2 = e ^ j;
-                    if (e2 > e) {
-                        const bool up = ((lane * EPT + e) & k) == 0;
-                        const uint32_t x = v[e], y = v[e2];
-                        const bool swap = (x > y) == up;
-                        v[e] = swap ? y : x;
-                        v[e2] = swap ? x : y;
-                    }
-                }
-            } else {
-                const int m = j / EPT;                 // partner lane offset
-                const bool lower = (lane & m) == 0;
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) {
-                    const bool up = ((lane * EPT + e) & k) == 0;
-                    const uint32_t y = __shfl_xor_sync(0xffffffffu, v[e], m);
-                    v[e] = (lower == up) ? min(v[e], y) : max(v[e], y);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) out[lane * EPT + e] = v[e];
-}
-
 // 16-bit caches use the tensor cores (pa_mma.cuh) on swizzled tiles placed
 // by tensor-map copies of whole 16-row blocks; fp32 caches use the CUDA-core
 // path (pa_math.cuh) on tiles placed by 1-D copies of the valid rows.

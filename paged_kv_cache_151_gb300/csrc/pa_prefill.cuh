@@ -13,11 +13,14 @@
 // handles the rows of one group from their first block to the block of the
 // group's last visible position, and each warp masks its rows' limits.
 //
-// Work items: (row group, sequence, KV head) of the worst case (max_query_len
-// rows), ordered by row group from the last (which sees the most keys) to
-// the first, dealt in turn to as many blocks as are resident; items of
-// sequences with fewer rows, or with fewer than p.mq_split_rows rows (the
-// persistent kernel's), are skipped at once.
+// Work items: (row group, sequence, KV head) of the sequences whose runs have
+// at least p.mq_split_rows rows (the others are the persistent kernel's).
+// Every block lists them in the same order -- sequences by length, longest
+// first (up to 256 sequences; in index order beyond), and within a sequence
+// the last row groups (which see the most keys) first -- and takes item
+// blockIdx.x, blockIdx.x + gridDim.x, ...: with one item per block the
+// hardware starts the costliest items first and gives the cheap ones to the
+// blocks that finish early.
 #pragma once
 
 #include "pa_common.cuh"
@@ -41,9 +44,6 @@ struct PrefillLayout {
 #ifndef PA_PREFILL_BLOCKS_PER_SM
 #define PA_PREFILL_BLOCKS_PER_SM 3
 #endif
-#ifndef PA_PREFILL_WAVES
-#define PA_PREFILL_WAVES 4
-#endif
 
 template <typename T, int D, int G, int NWC, int S>
 __global__ void __launch_bounds__((NWC + 1) * 32, PA_PREFILL_BLOCKS_PER_SM)
@@ -60,6 +60,11 @@ prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
     uint64_t *empty = full + S;
     int *valid = reinterpret_cast<int *>(smem + Lay::OFF_OK);
     __shared__ int abort_flag;                     // a wait timed out: everyone stops
+    // the schedule (up to 256 sequences sorted; index order beyond)
+    __shared__ uint32_t sched_keys[256];           // sort input
+    __shared__ uint32_t sched_order[256];          // sequences, longest first (low 16 bits)
+    __shared__ int sched_first[257];               // items before sorted position i
+    __shared__ int sched_groups[256];              // row groups of sequence s
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
@@ -76,31 +81,121 @@ prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
         abort_flag = 0;
     }
     __syncthreads();
+    // Row groups of sequence s if its run goes to this kernel, else 0 (a run
+    // with a bad range is flagged, by block 0, and skipped).  Reads only
+    // query_start and seq_lens, which the kernel before this one must not write.
+    auto groups_of = [&](int s) -> int {
+        const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
+        const int nq = q1 - q0, L = p.seq_lens[s];
+        // sequences with fewer rows are the persistent kernel's, which flags bad ranges
+        if (nq < 0 || nq * G < p.mq_split_rows) return 0;
+        if (q0 < 0 || q1 > p.num_q_rows || nq > p.max_query_len || L < nq || L > cap) {
+            if (blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
+            return 0;
+        }
+        return min(groups, (nq * G + ROWS - 1) / ROWS);
+    };
+    const bool sorted = B <= 256;
+    int total = 0;                                 // items (every thread)
+    if (sorted) {
+        if (warp == 0) {
+            for (int s = lane; s < 256; s += 32) {
+                uint32_t key = 0xffffffffu;
+                const int gs = s < B ? groups_of(s) : 0;
+                if (s < B) sched_groups[s] = gs;
+                if (gs > 0) {
+                    const int nb = min(0xffff, (p.seq_lens[s] + 15) >> 4);
+                    key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)s;
+                }
+                sched_keys[s] = key;
+            }
+            __syncwarp();
+            warp_bitonic_sort<8>(sched_keys, sched_order);
+            __syncwarp();
+            // items before each sorted position: lane holds positions 8*lane .. 8*lane+7
+            int c[8], sum = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t k = sched_order[8 * lane + e];
+                c[e] = k == 0xffffffffu ? 0 : sched_groups[k & 0xffffu] * Hkv;
+                sum += c[e];
+            }
+            int x = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            int run = x - sum;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sched_first[8 * lane + e] = run;
+                run += c[e];
+            }
+            if (lane == 31) sched_first[256] = run;
+        }
+        __syncthreads();
+        total = sched_first[256];
+    } else {
+        int sum = 0;
+        for (int s = lane; s < B; s += 32) sum += groups_of(s) * Hkv;
+        total = __reduce_add_sync(0xffffffffu, sum);
+    }
+    // Item r -> (sequence, KV head, row group).
+    auto item_of = [&](int r, int &s, int &j, int &grp) {
+        int local;
+        if (sorted) {
+            int lo = 0, hi = 255;                  // last position with sched_first <= r
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sched_first[mid] <= r) lo = mid; else hi = mid - 1;
+            }
+            s = (int)(sched_order[lo] & 0xffffu);
+            local = r - sched_first[lo];
+        } else {
+            // index order: the warp walks the sequences 32 at a time
+            int base = 0;
+            s = -1;
+            local = 0;
+            for (int s0 = 0; s0 < B && s < 0; s0 += 32) {
+                const int n = (s0 + lane < B) ? groups_of(s0 + lane) * Hkv : 0;
+                int x = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && base + x - n <= r && r < base + x);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    s = s0 + l;
+                    local = r - (base + __shfl_sync(0xffffffffu, x - n, l));
+                }
+                base += __shfl_sync(0xffffffffu, x, 31);
+            }
+        }
+        const int q0 = p.query_start[s], nq = p.query_start[s + 1] - q0;
+        const int gs = min(groups, (nq * G + ROWS - 1) / ROWS);
+        j = local % Hkv;
+        grp = gs - 1 - local / Hkv;                // last row groups first
+    };
+
     // the caches (and q, out) only after the kernel before this one is done
     grid_dependency_wait();
 
-    // Work items (row group, sequence, KV head), last row groups first, dealt
-    // to the resident blocks in turn; the ring of stages runs on across items,
-    // so the producer streams the next item while the consumers finish one.
-    const long long items = (long long)groups * B * Hkv;
+    // The ring of stages runs on across the items of a block, so the producer
+    // streams the next item while the consumers finish one.
     long long kglob = 0;                           // blocks through the ring so far
     const uint64_t pol = policy_evict_last();      // the sequence's other groups reread them
     W wa;
     wa.init(lane);
-    for (long long x = blockIdx.x; x < items; x += gridDim.x) {
+    for (int x = blockIdx.x; x < total; x += gridDim.x) {
         if (*(volatile int *)&abort_flag) break;
-        const int j = (int)(x % Hkv);
-        const int s = (int)((x / Hkv) % B);
-        const int grp = groups - 1 - (int)(x / ((long long)Hkv * B));
+        int s, j, grp;
+        item_of(x, s, j, grp);
         const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
         const int nq = q1 - q0;
         const int L = p.seq_lens[s];
-        // sequences with fewer rows are the persistent kernel's, which flags bad ranges
-        if (nq < 0 || nq * G < p.mq_split_rows || grp * ROWS >= nq * G) continue;
-        if (q0 < 0 || q1 > p.num_q_rows || nq > p.max_query_len || L < nq || L > cap) {
-            if (grp == 0 && j == 0 && tid == 0) set_error(p.err, ERR_SEQ_LEN);
-            continue;
-        }
         const int last_row = min(grp * ROWS + ROWS, nq * G) - 1;
         const int nb = (L - nq + last_row / G) / 16 + 1;   // through the group's last position
 
@@ -206,20 +301,17 @@ cudaError_t launch_prefill(const DecodeParams &p, int groups, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    const long long items = (long long)groups * p.num_seqs * p.num_kv_heads;
-    if (items <= 0) return cudaSuccess;
-    static int per_sm[64] = {};                    // resident blocks per SM, per device
-    if (dev >= 0 && dev < 64 && per_sm[dev] == 0) {
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, (PREFILL_NWC + 1) * 32, smem);
-        if (e != cudaSuccess) return e;
-        per_sm[dev] = n > 0 ? n : 1;
-    }
-    const int sms = sm_count_of_current_device();
-    // a few waves of blocks: the hardware then evens out items of unequal cost
-    const long long resident = (long long)(sms > 0 ? sms : 152) *
-                               ((dev >= 0 && dev < 64) ? per_sm[dev] : 1) * PA_PREFILL_WAVES;
-    const long long blocks = items < resident ? items : resident;
+    // One block per item.  The items are at most the worst case (every
+    // sequence with `groups` row groups), and at most 2 * ceil(rows / 64) row
+    // groups per KV head over all runs together, since every run taken here
+    // has at least 64 rows; blocks past the real count return at once.
+    const long long worst = (long long)groups * p.num_seqs * p.num_kv_heads;
+    const long long rows_all = (long long)p.num_q_rows * G;
+    const long long bound =
+        (long long)p.num_kv_heads * 2 * ((rows_all + PREFILL_GROUP_ROWS - 1) / PREFILL_GROUP_ROWS);
+    long long blocks = worst < bound ? worst : bound;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) blocks = 0x7fffffffLL;   // then blocks take several items
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
     cfg.blockDim = dim3((PREFILL_NWC + 1) * 32, 1, 1);
