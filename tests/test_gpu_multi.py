@@ -251,6 +251,22 @@ def test_multi_batch_larger_than_one_sort(cuda_lib):
     assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), "4500 seqs")
 
 
+def test_multi_prefill_more_than_256_sequences(cuda_lib):
+    """Long runs among more than 256 sequences: the prefill kernel lists their
+    work items in sequence order (it sorts them by length only up to 256
+    sequences); every long run and a few one-token rows against the oracle."""
+    n = np.ones(300, dtype=np.int64)
+    long_runs = [3, 77, 150, 255, 256, 299]
+    n[long_runs] = [40, 25, 64, 17, 33, 90]          # 68..360 rows at G = 4
+    b = wl.multi_query_batch(680, num_seqs=300, min_ctx=0, max_ctx=200, n_new=n,
+                             num_heads=8, num_kv_heads=2, head_dim=64, dtype="bf16",
+                             device="cuda", keep_seq=False)
+    out = gpu_multi(cuda_lib, b)
+    seqs = sorted(set(long_runs + [0, 100, 298]))
+    ref, rows = oracle_multi(b, seqs=np.array(seqs))
+    assert_close(out[torch.from_numpy(rows).cuda()], ref, "300 seqs")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences against the oracle
 # ---------------------------------------------------------------------------
