@@ -94,6 +94,11 @@ cudaError_t run_split(const pa::DecodeParams &p, int dtype, int D, int G, dim3 g
 #ifndef PA_MULTI_CLUSTER
 #define PA_MULTI_CLUSTER 4
 #endif
+// The prefill path (long multi-token runs) on the tcgen05 tensor cores (1) or
+// on warp-level MMAs (0).
+#ifndef PA_PREFILL_TC
+#define PA_PREFILL_TC 1
+#endif
 // E4M3 caches run three blocks per SM; clusters of four deal their units
 // more evenly there.
 #ifndef PA_F8_CLUSTER
@@ -425,9 +430,16 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
     if (!prepare_maps(p, dtype, head_dim)) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (split) {
-        const int groups = (int)((rows + pa::PREFILL_GROUP_ROWS - 1) / pa::PREFILL_GROUP_ROWS);
-        cudaError_t e = dtype == PA_BF16 ? pa::prefill_bf16(p, head_dim, G, groups, st)
-                                         : pa::prefill_f16(p, head_dim, G, groups, st);
+        cudaError_t e;
+        if (PA_PREFILL_TC) {                       // tcgen05: items of 128 rows
+            const int groups = (int)((rows + pa::PREFILL_TC_ROWS - 1) / pa::PREFILL_TC_ROWS);
+            e = dtype == PA_BF16 ? pa::prefill_tc_bf16(p, head_dim, G, groups, st)
+                                 : pa::prefill_tc_f16(p, head_dim, G, groups, st);
+        } else {                                   // warp-level MMAs: items of 64 rows
+            const int groups = (int)((rows + pa::PREFILL_GROUP_ROWS - 1) / pa::PREFILL_GROUP_ROWS);
+            e = dtype == PA_BF16 ? pa::prefill_bf16(p, head_dim, G, groups, st)
+                                 : pa::prefill_f16(p, head_dim, G, groups, st);
+        }
         if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }

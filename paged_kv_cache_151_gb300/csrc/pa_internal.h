@@ -50,6 +50,9 @@ cudaError_t decode_multi_f16(const DecodeParams &p, int D, int G, long long unit
 cudaError_t prefill_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
 cudaError_t prefill_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
 constexpr int PREFILL_GROUP_ROWS = 64;     // rows of one prefill block (= its minimum)
+constexpr int PREFILL_TC_ROWS = 128;      // rows of one item of the tcgen05 prefill kernel
+cudaError_t prefill_tc_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
+cudaError_t prefill_tc_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

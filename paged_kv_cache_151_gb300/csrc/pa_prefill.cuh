@@ -45,6 +45,125 @@ struct PrefillLayout {
 #define PA_PREFILL_BLOCKS_PER_SM 3
 #endif
 
+// The schedule of the prefill work items, in shared memory: up to 256
+// sequences are sorted by length, longest first; beyond, index order.
+struct PrefillSched {
+    uint32_t keys[256];      // sort input
+    uint32_t order[256];     // sequences, longest first (low 16 bits)
+    int first[257];          // items before sorted position i
+    int groups[256];         // row groups of sequence s
+};
+
+// Row groups (of ROWS rows) of sequence s if its run goes to a prefill
+// kernel, else 0 (a run with a bad range is flagged, by block 0, and
+// skipped).  Reads only query_start and seq_lens, which the kernel before
+// this one must not write.
+template <int G, int ROWS>
+__device__ __forceinline__ int prefill_groups_of(const DecodeParams &p, int groups, int s) {
+    const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
+    const int nq = q1 - q0, L = p.seq_lens[s];
+    // sequences with fewer rows are the persistent kernel's, which flags bad ranges
+    if (nq < 0 || nq * G < p.mq_split_rows) return 0;
+    if (q0 < 0 || q1 > p.num_q_rows || nq > p.max_query_len || L < nq || L > p.max_blocks * 16) {
+        if (blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
+        return 0;
+    }
+    return min(groups, (nq * G + ROWS - 1) / ROWS);
+}
+
+// All threads of the block: build the schedule; returns the number of items.
+template <int G, int ROWS>
+__device__ int prefill_schedule(const DecodeParams &p, int groups, PrefillSched &sc) {
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (B > 256) {
+        int sum = 0;
+        for (int s = lane; s < B; s += 32) sum += prefill_groups_of<G, ROWS>(p, groups, s) * Hkv;
+        return __reduce_add_sync(0xffffffffu, sum);
+    }
+    if (warp == 0) {
+        for (int s = lane; s < 256; s += 32) {
+            uint32_t key = 0xffffffffu;
+            const int gs = s < B ? prefill_groups_of<G, ROWS>(p, groups, s) : 0;
+            if (s < B) sc.groups[s] = gs;
+            if (gs > 0) {
+                const int nb = min(0xffff, (p.seq_lens[s] + 15) >> 4);
+                key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)s;
+            }
+            sc.keys[s] = key;
+        }
+        __syncwarp();
+        warp_bitonic_sort<8>(sc.keys, sc.order);
+        __syncwarp();
+        // items before each sorted position: lane holds positions 8*lane .. 8*lane+7
+        int c[8], sum = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t k = sc.order[8 * lane + e];
+            c[e] = k == 0xffffffffu ? 0 : sc.groups[k & 0xffffu] * Hkv;
+            sum += c[e];
+        }
+        int x = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int run = x - sum;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            sc.first[8 * lane + e] = run;
+            run += c[e];
+        }
+        if (lane == 31) sc.first[256] = run;
+    }
+    __syncthreads();
+    return sc.first[256];
+}
+
+// Item r -> (sequence s, KV head j, row group grp), last row groups first
+// within a sequence.  All lanes of the calling warp, convergent.
+template <int G, int ROWS>
+__device__ void prefill_item(const DecodeParams &p, int groups, const PrefillSched &sc, int r,
+                             int &s, int &j, int &grp) {
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, lane = threadIdx.x & 31;
+    int local;
+    if (B <= 256) {
+        int lo = 0, hi = 255;                      // last position with first <= r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sc.first[mid] <= r) lo = mid; else hi = mid - 1;
+        }
+        s = (int)(sc.order[lo] & 0xffffu);
+        local = r - sc.first[lo];
+    } else {
+        // index order: the warp walks the sequences 32 at a time
+        int base = 0;
+        s = -1;
+        local = 0;
+        for (int s0 = 0; s0 < B && s < 0; s0 += 32) {
+            const int n = (s0 + lane < B) ? prefill_groups_of<G, ROWS>(p, groups, s0 + lane) * Hkv : 0;
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && base + x - n <= r && r < base + x);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                s = s0 + l;
+                local = r - (base + __shfl_sync(0xffffffffu, x - n, l));
+            }
+            base += __shfl_sync(0xffffffffu, x, 31);
+        }
+    }
+    const int q0 = p.query_start[s], nq = p.query_start[s + 1] - q0;
+    const int gs = min(groups, (nq * G + ROWS - 1) / ROWS);
+    j = local % Hkv;
+    grp = gs - 1 - local / Hkv;                    // last row groups first
+}
+
 template <typename T, int D, int G, int NWC, int S>
 __global__ void __launch_bounds__((NWC + 1) * 32, PA_PREFILL_BLOCKS_PER_SM)
 prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
@@ -60,15 +179,10 @@ prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
     uint64_t *empty = full + S;
     int *valid = reinterpret_cast<int *>(smem + Lay::OFF_OK);
     __shared__ int abort_flag;                     // a wait timed out: everyone stops
-    // the schedule (up to 256 sequences sorted; index order beyond)
-    __shared__ uint32_t sched_keys[256];           // sort input
-    __shared__ uint32_t sched_order[256];          // sequences, longest first (low 16 bits)
-    __shared__ int sched_first[257];               // items before sorted position i
-    __shared__ int sched_groups[256];              // row groups of sequence s
+    __shared__ PrefillSched sched;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int B = p.num_seqs, Hkv = p.num_kv_heads, H = p.num_heads;
-    const int cap = p.max_blocks * 16;
+    const int Hkv = p.num_kv_heads, H = p.num_heads;
 
     if (tid == 0) {
         prefetch_tensormap(&p.tmap_k);
@@ -81,104 +195,7 @@ prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
         abort_flag = 0;
     }
     __syncthreads();
-    // Row groups of sequence s if its run goes to this kernel, else 0 (a run
-    // with a bad range is flagged, by block 0, and skipped).  Reads only
-    // query_start and seq_lens, which the kernel before this one must not write.
-    auto groups_of = [&](int s) -> int {
-        const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
-        const int nq = q1 - q0, L = p.seq_lens[s];
-        // sequences with fewer rows are the persistent kernel's, which flags bad ranges
-        if (nq < 0 || nq * G < p.mq_split_rows) return 0;
-        if (q0 < 0 || q1 > p.num_q_rows || nq > p.max_query_len || L < nq || L > cap) {
-            if (blockIdx.x == 0) set_error(p.err, ERR_SEQ_LEN);
-            return 0;
-        }
-        return min(groups, (nq * G + ROWS - 1) / ROWS);
-    };
-    const bool sorted = B <= 256;
-    int total = 0;                                 // items (every thread)
-    if (sorted) {
-        if (warp == 0) {
-            for (int s = lane; s < 256; s += 32) {
-                uint32_t key = 0xffffffffu;
-                const int gs = s < B ? groups_of(s) : 0;
-                if (s < B) sched_groups[s] = gs;
-                if (gs > 0) {
-                    const int nb = min(0xffff, (p.seq_lens[s] + 15) >> 4);
-                    key = ((uint32_t)(0xffff - nb) << 16) | (uint32_t)s;
-                }
-                sched_keys[s] = key;
-            }
-            __syncwarp();
-            warp_bitonic_sort<8>(sched_keys, sched_order);
-            __syncwarp();
-            // items before each sorted position: lane holds positions 8*lane .. 8*lane+7
-            int c[8], sum = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t k = sched_order[8 * lane + e];
-                c[e] = k == 0xffffffffu ? 0 : sched_groups[k & 0xffffu] * Hkv;
-                sum += c[e];
-            }
-            int x = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            int run = x - sum;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sched_first[8 * lane + e] = run;
-                run += c[e];
-            }
-            if (lane == 31) sched_first[256] = run;
-        }
-        __syncthreads();
-        total = sched_first[256];
-    } else {
-        int sum = 0;
-        for (int s = lane; s < B; s += 32) sum += groups_of(s) * Hkv;
-        total = __reduce_add_sync(0xffffffffu, sum);
-    }
-    // Item r -> (sequence, KV head, row group).
-    auto item_of = [&](int r, int &s, int &j, int &grp) {
-        int local;
-        if (sorted) {
-            int lo = 0, hi = 255;                  // last position with sched_first <= r
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (sched_first[mid] <= r) lo = mid; else hi = mid - 1;
-            }
-            s = (int)(sched_order[lo] & 0xffffu);
-            local = r - sched_first[lo];
-        } else {
-            // index order: the warp walks the sequences 32 at a time
-            int base = 0;
-            s = -1;
-            local = 0;
-            for (int s0 = 0; s0 < B && s < 0; s0 += 32) {
-                const int n = (s0 + lane < B) ? groups_of(s0 + lane) * Hkv : 0;
-                int x = n;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
-                }
-                const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && base + x - n <= r && r < base + x);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    s = s0 + l;
-                    local = r - (base + __shfl_sync(0xffffffffu, x - n, l));
-                }
-                base += __shfl_sync(0xffffffffu, x, 31);
-            }
-        }
-        const int q0 = p.query_start[s], nq = p.query_start[s + 1] - q0;
-        const int gs = min(groups, (nq * G + ROWS - 1) / ROWS);
-        j = local % Hkv;
-        grp = gs - 1 - local / Hkv;                // last row groups first
-    };
+    const int total = prefill_schedule<G, ROWS>(p, groups, sched);
 
     // the caches (and q, out) only after the kernel before this one is done
     grid_dependency_wait();
@@ -192,7 +209,7 @@ prefill_kernel(const __grid_constant__ DecodeParams p, int groups) {
     for (int x = blockIdx.x; x < total; x += gridDim.x) {
         if (*(volatile int *)&abort_flag) break;
         int s, j, grp;
-        item_of(x, s, j, grp);
+        prefill_item<G, ROWS>(p, groups, sched, x, s, j, grp);
         const int q0 = p.query_start[s], q1 = p.query_start[s + 1];
         const int nq = q1 - q0;
         const int L = p.seq_lens[s];
