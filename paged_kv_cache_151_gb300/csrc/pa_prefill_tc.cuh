@@ -26,8 +26,11 @@
 //      V from shared memory MN-major (its rows are keys, head_dim
 //      contiguous); O accumulates in TMEM over the whole item and is read
 //      back, normalised, at the end.
-// One thread issues the copies and the MMAs; completion comes back through
-// mbarriers (tcgen05.commit).  The MMAs of one thread run in order, so when
+// A producer warp (lane 0) follows the same item order and keeps a ring of
+// K/V stages filled with tensor-map copies, each stage freed by a commit after
+// its P.V; one consumer thread issues the MMAs; completion comes back through
+// mbarriers (tcgen05.commit); the four consumer warps synchronise among
+// themselves on a named barrier.  The MMAs of one thread run in order, so when
 // S of step c+1 is complete, P.V of step c is too: its P tile, its K/V stage
 // and O are then free.  A ring of two K/V stages runs ahead of the MMAs;
 // two blocks share an SM (about 100 KB of shared memory and 256 TMEM columns
@@ -61,7 +64,7 @@ struct PrefillTcLayout {
     static constexpr size_t OFF_Q = 0;
     static constexpr size_t OFF_KV = OFF_Q + Q_BYTES;                  // stage st: K, then V
     static constexpr size_t OFF_BARS = OFF_KV + (size_t)STAGES * 2 * KV_BYTES;
-    static constexpr size_t OFF_TMEM = OFF_BARS + (size_t)(STAGES + 2) * 8;
+    static constexpr size_t OFF_TMEM = OFF_BARS + (size_t)(2 * STAGES + 2) * 8;
     static constexpr size_t BYTES = OFF_TMEM + 16 + 1024;              // + alignment of the base
     static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0,
                   "1024-byte aligned swizzle atoms");
@@ -70,9 +73,23 @@ struct PrefillTcLayout {
 // TMEM columns of a block: S 0..63, P 64..95 (bf16/f16 pairs), O 128..128+D-1
 constexpr uint32_t TC_TMEM_COLS = 256;
 constexpr int TC_BLOCKS_PER_SM = 2;
+constexpr int TC_CONSUMERS = 4;          // warps of the softmax (one row per thread)
+
+// The consumer warps' own barrier (named barrier 1), plain and with an AND
+// of a predicate.
+__device__ __forceinline__ void tc_consumers_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ bool tc_consumers_sync_and(bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"((uint32_t)pred) : "memory");
+    return r != 0;
+}
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128, TC_BLOCKS_PER_SM)
+__global__ void __launch_bounds__((TC_CONSUMERS + 1) * 32, TC_BLOCKS_PER_SM)
 prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
     static_assert(sizeof(T) == 2 && (D == 64 || D == 128), "16-bit caches, head_dim 64 or 128");
     using Lay = PrefillTcLayout<T, D>;
@@ -86,8 +103,9 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
     unsigned char *sQ = smem + Lay::OFF_Q;
     unsigned char *sKV = smem + Lay::OFF_KV;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);   // [S]: a stage landed
-    uint64_t *s_done = full + S;                   // S of a step is in TMEM
-    uint64_t *pv_done = full + S + 1;              // the item's last P.V is done
+    uint64_t *empty = full + S;                    // [S]: a stage's P.V is done
+    uint64_t *s_done = full + 2 * S;               // S of a step is in TMEM
+    uint64_t *pv_done = full + 2 * S + 1;          // the item's last P.V is done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
     __shared__ PrefillSched sched;
 
@@ -97,7 +115,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
     if (tid == 0) {
         prefetch_tensormap(&p.tmap_k);
         prefetch_tensormap(&p.tmap_v);
-        for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < 2 * S; ++i) mbar_init(&full[i], 1);   // full and empty
         mbar_init(s_done, 1);
         mbar_init(pv_done, 1);
         fence_mbar_init();
@@ -123,206 +141,237 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
     bool ok = true;
 
     const int R = (int)gridDim.x, me = (int)blockIdx.x;
-    for (int k = 0; ok; ++k) {
+    // The geometry of an item; the producer and the consumers compute it alike.
+    struct Item {
+        int s, j, grp, q0, nq, L, nrows, nsteps, nb_seq;
+    };
+    auto item_at = [&](int k, Item &it) -> bool {  // all lanes of a warp
         const long long xl = (long long)k * R + ((k & 1) ? (R - 1 - me) : me);   // snake
-        if (xl >= total) break;
-        const int x = (int)xl;
-        int s, j, grp;
-        prefill_item<G, TC_ROWS>(p, groups, sched, x, s, j, grp);
-        const int q0 = p.query_start[s], nq = p.query_start[s + 1] - q0;
-        const int L = p.seq_lens[s];
-        const int nrows = min(TC_ROWS, nq * G - grp * TC_ROWS);   // >= 1
-        const int last_tok = (grp * TC_ROWS + nrows - 1) / G;
-        const int n_keys = L - nq + last_tok + 1;                 // keys any row sees
-        const int nsteps = (n_keys + TC_KEYS - 1) / TC_KEYS;
-        const int nb_seq = (L + 15) >> 4;                         // blocks of the sequence
-        // this thread's row
-        const int r = tid;
-        const bool row_ok = r < nrows;
-        const int rr = grp * TC_ROWS + r;
-        const int tok = rr / G, head = rr % G;
-        const int lim = L - nq + tok;                             // last visible position
+        if (xl >= total) return false;
+        prefill_item<G, TC_ROWS>(p, groups, sched, (int)xl, it.s, it.j, it.grp);
+        it.q0 = p.query_start[it.s];
+        it.nq = p.query_start[it.s + 1] - it.q0;
+        it.L = p.seq_lens[it.s];
+        it.nrows = min(TC_ROWS, it.nq * G - it.grp * TC_ROWS);   // >= 1
+        const int last_tok = (it.grp * TC_ROWS + it.nrows - 1) / G;
+        const int n_keys = it.L - it.nq + last_tok + 1;          // keys any row sees
+        it.nsteps = (n_keys + TC_KEYS - 1) / TC_KEYS;
+        it.nb_seq = (it.L + 15) >> 4;                            // blocks of the sequence
+        return true;
+    };
 
-        // -- Q rows into sQ ([NH][128 rows][128 B], 128-byte swizzle); zeros past the run
-        {
-            const uint4 *qr = reinterpret_cast<const uint4 *>(
-                reinterpret_cast<const T *>(p.q) + (long long)(q0 + (row_ok ? tok : 0)) * p.q_seq_stride +
-                (long long)(j * G + head) * D);
+    if (warp == TC_CONSUMERS) {
+        // ---- producer: step kk of the block's items into stage kk % S once its
+        // previous use is done (lane 0 issues)
+        long long kk = 0;
+        bool pok = true;
+        Item it;
+        for (int k = 0; pok && item_at(k, it); ++k) {
+            for (int c = 0; pok && c < it.nsteps; ++c, ++kk) {
+                const int st = (int)(kk % S);
+                bool w = true;
+                if (threadIdx.x % 32 == 0) {
+                    w = kk < S || mbar_wait_bounded(&empty[st], (uint32_t)(((kk / S) - 1) & 1), p.err);
+                    if (w) {
+                        int pbs[TC_KEYS / 16];
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = row_ok ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
-                const int h = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(sQ + h * (TC_ROWS * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+                        for (int b = 0; b < TC_KEYS / 16; ++b) {   // independent loads
+                            const int lb = (TC_KEYS / 16) * c + b;
+                            pbs[b] = lb < it.nb_seq ? p.block_tables[(long long)it.s * p.max_blocks + lb] : -1;
+                        }
+                        unsigned char *dK = sKV + (size_t)st * 2 * KVB, *dV = dK + KVB;
+                        mbar_arrive_expect_tx(&full[st], 2 * KVB);
+#pragma unroll
+                        for (int b = 0; b < TC_KEYS / 16; ++b) {
+                            const int lb = (TC_KEYS / 16) * c + b;
+                            int z = z_none;                // past the sequence: zeros
+                            if (lb < it.nb_seq) {
+                                if (pbs[b] >= 0 && (long long)pbs[b] < p.num_blocks) z = pbs[b] * Hkv + it.j;
+                                else set_error(p.err, ERR_BLOCK_ID);
+                            }
+#pragma unroll
+                            for (int h = 0; h < NH; ++h) {
+                                tma_load_3d(dK + h * (TC_KEYS * 128) + b * 2048, &p.tmap_k, h * 64, 0, z,
+                                            &full[st], pol);
+                                tma_load_3d(dV + h * (TC_KEYS * 128) + b * 2048, &p.tmap_v, h * 64, 0, z,
+                                            &full[st], pol);
+                            }
+                        }
+                    }
+                }
+                pok = __shfl_sync(0xffffffffu, w, 0);
             }
         }
-        fence_proxy_async_smem();                  // before the MMAs read sQ
+        // copies still landing when the block exits: wait (bounded) for the last S
+        if (threadIdx.x % 32 == 0)
+            for (long long i = (kk > S ? kk - S : 0); i < kk; ++i)
+                mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.err);
+    } else {
+        // ---- consumers (thread 0 also issues the MMAs)
+        Item it;
+        for (int k = 0; ok && item_at(k, it); ++k) {
+            const int s = it.s, j = it.j, grp = it.grp, q0 = it.q0, nq = it.nq, L = it.L;
+            const int nrows = it.nrows, nsteps = it.nsteps, nb_seq = it.nb_seq;
+            // this thread's row
+            const int r = tid;
+            const bool row_ok = r < nrows;
+            const int rr = grp * TC_ROWS + r;
+            const int tok = rr / G, head = rr % G;
+            const int lim = L - nq + tok;                         // last visible position
+            (void)s;
 
-        // -- step c's four cache blocks of K and V into stage (kglob + c) % S (thread 0)
-        auto load_step = [&](int c) {
-            const long long kk = kglob + c;
-            const int st = (int)(kk % S);
-            unsigned char *dK = sKV + (size_t)st * 2 * KVB, *dV = dK + KVB;
-            mbar_arrive_expect_tx(&full[st], 2 * KVB);
-#pragma unroll
-            for (int b = 0; b < TC_KEYS / 16; ++b) {
-                const int lb = (TC_KEYS / 16) * c + b;
-                int z = z_none;                    // past the sequence: zeros
-                if (lb < nb_seq) {
-                    const int pb = p.block_tables[(long long)s * p.max_blocks + lb];
-                    if (pb >= 0 && (long long)pb < p.num_blocks) z = pb * Hkv + j;
-                    else set_error(p.err, ERR_BLOCK_ID);
-                }
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    tma_load_3d(dK + h * (TC_KEYS * 128) + b * 2048, &p.tmap_k, h * 64, 0, z, &full[st], pol);
-                    tma_load_3d(dV + h * (TC_KEYS * 128) + b * 2048, &p.tmap_v, h * 64, 0, z, &full[st], pol);
-                }
-            }
-        };
-        // -- S of step c (thread 0, after its stage landed); false on a timeout
-        auto issue_s = [&](int c) -> bool {
-            const long long kk = kglob + c;
-            const int st = (int)(kk % S);
-            if (!mbar_wait_bounded(&full[st], (uint32_t)((kk / S) & 1), p.err)) return false;
-            const uint32_t kaddr = smem_u32(sKV + (size_t)st * 2 * KVB);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes
-                tc5_mma(tS,
-                        tc5_desc_sw128(smem_u32(sQ) + (ks >> 2) * (TC_ROWS * 128) + off, 16, 1024),
-                        tc5_desc_sw128(kaddr + (ks >> 2) * (TC_KEYS * 128) + off, 16, 1024),
-                        ID_S, ks > 0);
-            }
-            tc5_commit(s_done);
-            return true;
-        };
-
-        if (tid == 0)
-            for (int c = 0; c < min(nsteps, S); ++c) load_step(c);
-        float m_run = -INFINITY, l_run = 0.f;
-        tc5_fence_before_sync();
-        __syncthreads();                           // sQ written
-        bool issued = true;
-        if (tid == 0) {
-            tc5_fence_after_sync();
-            issued = issue_s(0);
-        }
-
-        for (int c = 0; c < nsteps; ++c) {
-            const bool got = issued && mbar_wait_bounded(s_done, n_s & 1, p.err);
-            ++n_s;
-            if (!__syncthreads_and(got)) { ok = false; break; }
-            tc5_fence_after_sync();
-            // P.V of step c-1 is complete: its stage takes step c - 1 + S
-            if (tid == 0 && c >= 1 && c - 1 + S < nsteps) load_step(c - 1 + S);
-
-            // -- this row's 64 scores
-            float sv[TC_KEYS];
-            tc5_ld32(tS + lane_off, *reinterpret_cast<float(*)[32]>(&sv[0]));
-            tc5_ld32(tS + lane_off + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-            const int kb = c * TC_KEYS;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < TC_KEYS; ++e) {
-                sv[e] = (row_ok && kb + e <= lim) ? sv[e] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, sv[e]);
-            }
-            // lazy rescaling: the reference level moves only by more than 2^RESCALE_LOG2
-            const float m_new = mx > m_run + RESCALE_LOG2 ? mx : m_run;
-            const float ms = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = m_new == m_run ? 1.f : ex2(m_run - ms);
-            uint32_t pw[TC_KEYS / 2];
-            float psum = 0.f;
-#pragma unroll
-            for (int e = 0; e < TC_KEYS / 2; ++e) {
-                pw[e] = Mma<T>::pack(ex2(sv[2 * e] - ms), ex2(sv[2 * e + 1] - ms));
-                float a, b;
-                Mma<T>::unpack(pw[e], a, b);
-                psum += a + b;
-            }
-            l_run = l_run * alpha + psum;
-            m_run = m_new;
-            // this row of O to the new level (O holds nothing before the first P.V)
-            if (__any_sync(0xffffffffu, c > 0 && alpha != 1.f)) {
-                const float f = c > 0 ? alpha : 1.f;
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float o[32];
-                    tc5_ld32(tO + lane_off + c0, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= f;
-                    tc5_st32(tO + lane_off + c0, o);
-                }
-            }
-            // P row r into TMEM: 64 keys, two per column
-            tc5_st32u(tP + lane_off, pw);
-            // V rows of the sequence's last block past L hold other tokens' data
-            // (zero-weighted, but 0 * NaN is NaN): clear them
+            // -- Q rows into sQ ([NH][128 rows][128 B], 128-byte swizzle); zeros past the run
             {
-                const int st = (int)((kglob + c) % S);
-                unsigned char *dV = sKV + (size_t)st * 2 * KVB + KVB;
-                const int tail = L & 15, lb_last = nb_seq - 1;
-                const int b = lb_last - (TC_KEYS / 16) * c;
-                if (tail != 0 && b >= 0 && b < TC_KEYS / 16) {
-                    const int nclr = (16 - tail) * NH * 8;        // 16-byte pieces
-                    for (int i = tid; i < nclr; i += 128) {
-                        const int h = i / ((16 - tail) * 8), rem = i % ((16 - tail) * 8);
-                        const int row = 16 * b + tail + rem / 8;
-                        *reinterpret_cast<uint4 *>(dV + h * (TC_KEYS * 128) + row * 128 + (rem % 8) * 16) =
-                            make_uint4(0, 0, 0, 0);
+                const uint4 *qr = reinterpret_cast<const uint4 *>(
+                    reinterpret_cast<const T *>(p.q) + (long long)(q0 + (row_ok ? tok : 0)) * p.q_seq_stride +
+                    (long long)(j * G + head) * D);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 v = row_ok ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
+                    const int h = c >> 3, cc = c & 7;
+                    *reinterpret_cast<uint4 *>(sQ + h * (TC_ROWS * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+                }
+            }
+            fence_proxy_async_smem();              // before the MMAs read sQ
+
+            // -- S of step c (thread 0, after its stage landed); false on a timeout
+            auto issue_s = [&](int c) -> bool {
+                const long long kk = kglob + c;
+                const int st = (int)(kk % S);
+                if (!mbar_wait_bounded(&full[st], (uint32_t)((kk / S) & 1), p.err)) return false;
+                const uint32_t kaddr = smem_u32(sKV + (size_t)st * 2 * KVB);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes
+                    tc5_mma(tS,
+                            tc5_desc_sw128(smem_u32(sQ) + (ks >> 2) * (TC_ROWS * 128) + off, 16, 1024),
+                            tc5_desc_sw128(kaddr + (ks >> 2) * (TC_KEYS * 128) + off, 16, 1024),
+                            ID_S, ks > 0);
+                }
+                tc5_commit(s_done);
+                return true;
+            };
+
+            float m_run = -INFINITY, l_run = 0.f;
+            tc5_fence_before_sync();
+            tc_consumers_sync();                   // sQ written
+            bool issued = true;
+            if (tid == 0) {
+                tc5_fence_after_sync();
+                issued = issue_s(0);
+            }
+
+            for (int c = 0; c < nsteps; ++c) {
+                const bool got = issued && mbar_wait_bounded(s_done, n_s & 1, p.err);
+                ++n_s;
+                if (!tc_consumers_sync_and(got)) { ok = false; break; }
+                tc5_fence_after_sync();
+
+                // -- this row's 64 scores
+                float sv[TC_KEYS];
+                tc5_ld32(tS + lane_off, *reinterpret_cast<float(*)[32]>(&sv[0]));
+                tc5_ld32(tS + lane_off + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+                const int kb = c * TC_KEYS;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < TC_KEYS; ++e) {
+                    sv[e] = (row_ok && kb + e <= lim) ? sv[e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[e]);
+                }
+                // lazy rescaling: the reference level moves only by more than 2^RESCALE_LOG2
+                const float m_new = mx > m_run + RESCALE_LOG2 ? mx : m_run;
+                const float ms = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = m_new == m_run ? 1.f : ex2(m_run - ms);
+                uint32_t pw[TC_KEYS / 2];
+                float psum = 0.f;
+#pragma unroll
+                for (int e = 0; e < TC_KEYS / 2; ++e) {
+                    pw[e] = Mma<T>::pack(ex2(sv[2 * e] - ms), ex2(sv[2 * e + 1] - ms));
+                    float a, b;
+                    Mma<T>::unpack(pw[e], a, b);
+                    psum += a + b;
+                }
+                l_run = l_run * alpha + psum;
+                m_run = m_new;
+                // this row of O to the new level (O holds nothing before the first P.V)
+                if (__any_sync(0xffffffffu, c > 0 && alpha != 1.f)) {
+                    const float f = c > 0 ? alpha : 1.f;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        float o[32];
+                        tc5_ld32(tO + lane_off + c0, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= f;
+                        tc5_st32(tO + lane_off + c0, o);
+                    }
+                }
+                // P row r into TMEM: 64 keys, two per column
+                tc5_st32u(tP + lane_off, pw);
+                // V rows of the sequence's last block past L hold other tokens' data
+                // (zero-weighted, but 0 * NaN is NaN): clear them
+                {
+                    const int st = (int)((kglob + c) % S);
+                    unsigned char *dV = sKV + (size_t)st * 2 * KVB + KVB;
+                    const int tail = L & 15, lb_last = nb_seq - 1;
+                    const int b = lb_last - (TC_KEYS / 16) * c;
+                    if (tail != 0 && b >= 0 && b < TC_KEYS / 16) {
+                        const int nclr = (16 - tail) * NH * 8;    // 16-byte pieces
+                        for (int i = tid; i < nclr; i += 128) {
+                            const int h = i / ((16 - tail) * 8), rem = i % ((16 - tail) * 8);
+                            const int row = 16 * b + tail + rem / 8;
+                            *reinterpret_cast<uint4 *>(dV + h * (TC_KEYS * 128) + row * 128 + (rem % 8) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();          // the cleared rows before the MMA
+                tc5_fence_before_sync();
+                tc_consumers_sync();
+                if (tid == 0) {
+                    tc5_fence_after_sync();
+                    const int st = (int)((kglob + c) % S);
+                    const uint32_t vaddr = smem_u32(sKV + (size_t)st * 2 * KVB + KVB);
+#pragma unroll
+                    for (int ks = 0; ks < TC_KEYS / 16; ++ks)
+                        tc5_mma_ta(tO, tP + 8 * ks,
+                                   tc5_desc_sw128(vaddr + ks * 2048, TC_KEYS * 128, 1024), ID_O,
+                                   (c > 0 || ks > 0) ? 1u : 0u);
+                    tc5_commit(&empty[st]);        // the stage is free once P.V is done
+                    if (c + 1 < nsteps) issued = issue_s(c + 1);
+                    else tc5_commit(pv_done);
+                }
+            }
+            if (!ok) break;
+
+            // -- O / l into out (this thread's row)
+            const bool got = mbar_wait_bounded(pv_done, n_pv & 1, p.err);
+            ++n_pv;
+            if (!tc_consumers_sync_and(got)) { ok = false; break; }
+            tc5_fence_after_sync();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)(q0 + tok) * H + j * G + head) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float v[32];
+                tc5_ld32(tO + lane_off + c0, v);
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = Mma<T>::pack(v[e] * inv, v[e + 1] * inv);
+                        w.y = Mma<T>::pack(v[e + 2] * inv, v[e + 3] * inv);
+                        w.z = Mma<T>::pack(v[e + 4] * inv, v[e + 5] * inv);
+                        w.w = Mma<T>::pack(v[e + 6] * inv, v[e + 7] * inv);
+                        *reinterpret_cast<uint4 *>(o + c0 + e) = w;
                     }
                 }
             }
-            fence_proxy_async_smem();              // the cleared rows before the MMA
+            kglob += nsteps;
             tc5_fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                tc5_fence_after_sync();
-                const int st = (int)((kglob + c) % S);
-                const uint32_t vaddr = smem_u32(sKV + (size_t)st * 2 * KVB + KVB);
-#pragma unroll
-                for (int ks = 0; ks < TC_KEYS / 16; ++ks)
-                    tc5_mma_ta(tO, tP + 8 * ks,
-                               tc5_desc_sw128(vaddr + ks * 2048, TC_KEYS * 128, 1024), ID_O,
-                               (c > 0 || ks > 0) ? 1u : 0u);
-                if (c + 1 < nsteps) issued = issue_s(c + 1);
-                else tc5_commit(pv_done);
-            }
+            tc_consumers_sync();                   // sQ and TMEM free for the next item
         }
-        if (!ok) break;
-
-        // -- O / l into out (this thread's row)
-        const bool got = mbar_wait_bounded(pv_done, n_pv & 1, p.err);
-        ++n_pv;
-        if (!__syncthreads_and(got)) { ok = false; break; }
-        tc5_fence_after_sync();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        T *o = reinterpret_cast<T *>(p.out) + ((long long)(q0 + tok) * H + j * G + head) * D;
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float v[32];
-            tc5_ld32(tO + lane_off + c0, v);
-            if (row_ok) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    uint4 w;
-                    w.x = Mma<T>::pack(v[e] * inv, v[e + 1] * inv);
-                    w.y = Mma<T>::pack(v[e + 2] * inv, v[e + 3] * inv);
-                    w.z = Mma<T>::pack(v[e + 4] * inv, v[e + 5] * inv);
-                    w.w = Mma<T>::pack(v[e + 6] * inv, v[e + 7] * inv);
-                    *reinterpret_cast<uint4 *>(o + c0 + e) = w;
-                }
-            }
-        }
-        kglob += nsteps;
-        tc5_fence_before_sync();
-        __syncthreads();                           // sQ and TMEM free for the next item
     }
 
-    // after a timeout: wait (bounded) for the copies still in flight
-    if (!ok && tid == 0)
-        for (long long i = (kglob > S ? kglob - S : 0); i < kglob + S; ++i)
-            mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.err);
     tc5_fence_before_sync();
     __syncthreads();
     if (warp == 0) tc5_dealloc(tmem, TC_TMEM_COLS);
@@ -357,7 +406,7 @@ cudaError_t launch_prefill_tc(const DecodeParams &p, int groups, cudaStream_t st
     if (blocks <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(128, 1, 1);
+    cfg.blockDim = dim3((TC_CONSUMERS + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
