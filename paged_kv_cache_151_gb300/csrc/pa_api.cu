@@ -155,6 +155,25 @@ bool encode_cache_map(CUtensorMap *m, const void *base, int64_t num_blocks, int3
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [rows][H][D] (rows q_row_stride elements apart, 16-bit) as the 3-D tensor
+// (D, H, rows), read in boxes of 64 elements x G heads x 128 / G tokens with
+// the 128-byte swizzle: one box is 128 rows of 128 bytes, row = token * G +
+// head, the layout of one prefill item's Q operand.
+bool encode_q_map(CUtensorMap *m, const void *q, int64_t rows, int32_t num_heads,
+                  int32_t head_dim, int64_t q_row_stride, int32_t G, int32_t dtype) {
+    auto enc = tensor_map_encoder();
+    if (!enc || G <= 0 || pa::PREFILL_TC_ROWS % G != 0 || rows <= 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)q_row_stride * 2};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)(pa::PREFILL_TC_ROWS / G)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(m, dt, 3, const_cast<void *>(q), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Fill the tensor maps the persistent kernel needs for 16-bit and E4M3
 // caches (kv_dtype: the caches' storage type).
 bool prepare_maps(pa::DecodeParams &p, int32_t kv_dtype, int32_t head_dim) {
@@ -433,8 +452,11 @@ int pa_decode_multi(void *out, const void *q, const void *k_cache, const void *v
         cudaError_t e;
         if (PA_PREFILL_TC) {                       // tcgen05: items of 128 rows
             const int groups = (int)((rows + pa::PREFILL_TC_ROWS - 1) / pa::PREFILL_TC_ROWS);
-            e = dtype == PA_BF16 ? pa::prefill_tc_bf16(p, head_dim, G, groups, st)
-                                 : pa::prefill_tc_f16(p, head_dim, G, groups, st);
+            CUtensorMap tmap_q;
+            if (!encode_q_map(&tmap_q, q, num_q_rows, num_heads, head_dim, q_row_stride, G, dtype))
+                return PA_ERR_CUDA;
+            e = dtype == PA_BF16 ? pa::prefill_tc_bf16(p, tmap_q, head_dim, G, groups, st)
+                                 : pa::prefill_tc_f16(p, tmap_q, head_dim, G, groups, st);
         } else {                                   // warp-level MMAs: items of 64 rows
             const int groups = (int)((rows + pa::PREFILL_GROUP_ROWS - 1) / pa::PREFILL_GROUP_ROWS);
             e = dtype == PA_BF16 ? pa::prefill_bf16(p, head_dim, G, groups, st)

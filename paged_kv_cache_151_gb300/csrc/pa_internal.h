@@ -2,6 +2,7 @@
 // library (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (a plain 128-byte descriptor)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,8 +52,12 @@ cudaError_t prefill_bf16(const DecodeParams &p, int D, int G, int groups, cudaSt
 cudaError_t prefill_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
 constexpr int PREFILL_GROUP_ROWS = 64;     // rows of one prefill block (= its minimum)
 constexpr int PREFILL_TC_ROWS = 128;      // rows of one item of the tcgen05 prefill kernel
-cudaError_t prefill_tc_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
-cudaError_t prefill_tc_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st);
+// tmap_q: q [num_q_rows][H][D] as the 3-D tensor (D, H, rows) in boxes of
+// 64 elements x G heads x 128 / G tokens with the 128-byte swizzle
+cudaError_t prefill_tc_bf16(const DecodeParams &p, const CUtensorMap &tmap_q, int D, int G,
+                            int groups, cudaStream_t st);
+cudaError_t prefill_tc_f16(const DecodeParams &p, const CUtensorMap &tmap_q, int D, int G,
+                           int groups, cudaStream_t st);
 cudaError_t merge_f32(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_bf16(const MergeParams &p, int num_seqs, cudaStream_t st);
 cudaError_t merge_f16(const MergeParams &p, int num_seqs, cudaStream_t st);

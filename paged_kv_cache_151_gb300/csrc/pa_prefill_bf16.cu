@@ -10,8 +10,9 @@ cudaError_t prefill_bf16(const DecodeParams &p, int D, int G, int groups, cudaSt
     return dispatch_prefill<__nv_bfloat16>(p, D, G, groups, st);
 }
 
-cudaError_t prefill_tc_bf16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st) {
-    return dispatch_prefill_tc<__nv_bfloat16>(p, D, G, groups, st);
+cudaError_t prefill_tc_bf16(const DecodeParams &p, const CUtensorMap &tmap_q, int D, int G,
+                            int groups, cudaStream_t st) {
+    return dispatch_prefill_tc<__nv_bfloat16>(p, tmap_q, D, G, groups, st);
 }
 
 }  // namespace pa

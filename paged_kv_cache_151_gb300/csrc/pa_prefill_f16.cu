@@ -10,8 +10,9 @@ cudaError_t prefill_f16(const DecodeParams &p, int D, int G, int groups, cudaStr
     return dispatch_prefill<__half>(p, D, G, groups, st);
 }
 
-cudaError_t prefill_tc_f16(const DecodeParams &p, int D, int G, int groups, cudaStream_t st) {
-    return dispatch_prefill_tc<__half>(p, D, G, groups, st);
+cudaError_t prefill_tc_f16(const DecodeParams &p, const CUtensorMap &tmap_q, int D, int G,
+                           int groups, cudaStream_t st) {
+    return dispatch_prefill_tc<__half>(p, tmap_q, D, G, groups, st);
 }
 
 }  // namespace pa

@@ -10,35 +10,36 @@
 //
 // A work item is 128 such rows of one (sequence, KV head) -- the M side of
 // one tcgen05 MMA -- in the order of prefill_schedule (longest sequences
-// first, one item per block).  Per step of 64 keys (four 16-token cache
-// blocks):
+// first).  Per step of 64 keys (four 16-token cache blocks):
 //   1. S = Q K^T: tcgen05.mma, M = 128, N = 64, K = head_dim, both operands
-//      K-major from shared memory (128-byte swizzle): Q written once per item
-//      by the block's threads, the K tiles by tensor-map copies, the four
-//      blocks of a step stacked into one 64-row operand; S lands in TMEM.
-//   2. Each thread owns one row: it reads its 64 scores from TMEM
-//      (tcgen05.ld), masks positions past its causal limit, updates the
-//      online softmax in fp32 (lazy rescaling, as in the warp-level paths),
-//      rescales its row of O in TMEM when its reference level moved, and
-//      writes its probabilities, rounded to the cache type, back into TMEM
-//      (two per 32-bit column, its lane = its row).
+//      K-major in shared memory (128-byte swizzle): Q by one tensor-map copy
+//      per item, the four K blocks of the step by tensor-map copies stacked
+//      into one 64-row operand.  S lands in one of two TMEM buffers (step g
+//      in buffer g % 2), so S of the next step runs under the softmax of this
+//      one.
+//   2. Each softmax thread owns one row (TMEM lane = row): it reads its 64
+//      scores (tcgen05.ld), masks positions past its causal limit (only on
+//      the steps that reach past some row's limit), updates the online
+//      softmax in fp32 (lazy rescaling, as in the warp-level paths; two
+//      lanes per instruction where the arithmetic allows), rescales its row
+//      of O in TMEM when its reference level moved, and writes its
+//      probabilities, rounded to the cache type, over the first 32 columns
+//      of the step's S buffer (two per column).
 //   3. O += P V: tcgen05.mma, M = 128, N = head_dim, K = 64, P read from TMEM,
-//      V from shared memory MN-major (its rows are keys, head_dim
-//      contiguous); O accumulates in TMEM over the whole item and is read
-//      back, normalised, at the end.
-// A producer warp (lane 0) follows the same item order and keeps a ring of
-// K/V stages filled with tensor-map copies, each stage freed by a commit after
-// its P.V; one consumer thread issues the MMAs; completion comes back through
-// mbarriers (tcgen05.commit); the four consumer warps synchronise among
-// themselves on a named barrier.  The MMAs of one thread run in order, so when
-// S of step c+1 is complete, P.V of step c is too: its P tile, its K/V stage
-// and O are then free.  A ring of two K/V stages runs ahead of the MMAs;
-// two blocks share an SM (about 100 KB of shared memory and 256 TMEM columns
-// each), so one block's softmax overlaps the other's MMAs.  The grid is
-// persistent (two blocks per SM); block b takes the items b, 2R-1-b, 2R+b, ...
-// of the cost-sorted list (R blocks), which deals the long items out first.
-// Every wait is bounded; on a timeout the block stops and the error word
-// says so.
+//      V from shared memory MN-major (rows = keys, head_dim contiguous).  O
+//      accumulates in TMEM over the whole item and is read back, normalised,
+//      at the end.
+// Roles: warps 0-3 run the softmax (warp w reaches TMEM lanes 32w..32w+31);
+// warp 4 (lane 0) keeps the copies going -- Q once per item, and rings of two
+// K stages and two V stages (a K stage is free once its S is done, a V stage
+// once its P.V is); warp 5 (lane 0) issues the MMAs in the order S(0), S(1),
+// PV(0), S(2), PV(1), ... and reports their completion through
+// tcgen05.commit on mbarriers.  S(g + 2) overwrites the buffer PV(g) reads
+// its P from, so it is issued once PV(g) is complete.  Two blocks share an
+// SM (about 100 KB of shared memory and 256 TMEM columns each).  The grid is
+// persistent; block b takes the items b, 2R-1-b, 2R+b, ... of the sorted
+// list (R blocks), which deals the long items out first.  Every wait is
+// bounded; on a timeout the block stops and the error word says so.
 #pragma once
 
 #include <climits>
@@ -60,64 +61,69 @@ struct PrefillTcLayout {
     static constexpr int NH = D / 64;                                  // 128-byte groups of a row
     static constexpr size_t Q_BYTES = (size_t)TC_ROWS * D * 2;         // [NH][128 rows][128 B]
     static constexpr size_t KV_BYTES = (size_t)TC_KEYS * D * 2;        // [NH][64 keys][128 B]
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = 2;                                   // of K, and of V
     static constexpr size_t OFF_Q = 0;
-    static constexpr size_t OFF_KV = OFF_Q + Q_BYTES;                  // stage st: K, then V
-    static constexpr size_t OFF_BARS = OFF_KV + (size_t)STAGES * 2 * KV_BYTES;
-    static constexpr size_t OFF_TMEM = OFF_BARS + (size_t)(2 * STAGES + 2) * 8;
+    static constexpr size_t OFF_K = OFF_Q + Q_BYTES;
+    static constexpr size_t OFF_V = OFF_K + (size_t)STAGES * KV_BYTES;
+    static constexpr size_t OFF_BARS = OFF_V + (size_t)STAGES * KV_BYTES;
+    static constexpr int NBARS = 12;
+    static constexpr size_t OFF_TMEM = OFF_BARS + (size_t)NBARS * 8;
     static constexpr size_t BYTES = OFF_TMEM + 16 + 1024;              // + alignment of the base
     static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0,
                   "1024-byte aligned swizzle atoms");
 };
 
-// TMEM columns of a block: S 0..63, P 64..95 (bf16/f16 pairs), O 128..128+D-1
+// TMEM columns of a block: S buffers 0..63 and 64..127 (P over the first 32
+// columns of its buffer), O 128..128+D-1
 constexpr uint32_t TC_TMEM_COLS = 256;
 constexpr int TC_BLOCKS_PER_SM = 2;
-constexpr int TC_CONSUMERS = 4;          // warps of the softmax (one row per thread)
-
-// The consumer warps' own barrier (named barrier 1), plain and with an AND
-// of a predicate.
-__device__ __forceinline__ void tc_consumers_sync() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-__device__ __forceinline__ bool tc_consumers_sync_and(bool pred) {
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                 "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r) : "r"((uint32_t)pred) : "memory");
-    return r != 0;
-}
+constexpr int TC_SOFTMAX_WARPS = 4;      // one row per thread
+constexpr int TC_COPY_WARP = 4;
+constexpr int TC_MMA_WARP = 5;
+constexpr int TC_THREADS = 6 * 32;
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__((TC_CONSUMERS + 1) * 32, TC_BLOCKS_PER_SM)
-prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
+__global__ void __launch_bounds__(TC_THREADS, TC_BLOCKS_PER_SM)
+prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmap_q,
+                  int groups) {
     static_assert(sizeof(T) == 2 && (D == 64 || D == 128), "16-bit caches, head_dim 64 or 128");
+    static_assert(TC_ROWS % G == 0, "an item holds whole tokens");
     using Lay = PrefillTcLayout<T, D>;
-    constexpr int NH = Lay::NH, S = Lay::STAGES;
+    constexpr int NH = Lay::NH;
     constexpr uint32_t KVB = (uint32_t)Lay::KV_BYTES;
+    constexpr int TOKS = TC_ROWS / G;                               // tokens of one item
     constexpr uint32_t ID_S = tc5_idesc<T>(TC_ROWS, TC_KEYS, 0);    // Q K^T: both K-major
     constexpr uint32_t ID_O = tc5_idesc<T>(TC_ROWS, D, 1);          // P V: V MN-major
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem + Lay::OFF_Q;
-    unsigned char *sKV = smem + Lay::OFF_KV;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);   // [S]: a stage landed
-    uint64_t *empty = full + S;                    // [S]: a stage's P.V is done
-    uint64_t *s_done = full + 2 * S;               // S of a step is in TMEM
-    uint64_t *pv_done = full + 2 * S + 1;          // the item's last P.V is done
+    unsigned char *sK = smem + Lay::OFF_K;
+    unsigned char *sV = smem + Lay::OFF_V;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::OFF_BARS);
+    uint64_t *kfull = bars;          // [2] K of step g landed in stage g % 2
+    uint64_t *vfull = bars + 2;      // [2] V of step g landed
+    uint64_t *pv_done = bars + 4;    // [2] P.V of step g (and every MMA before it) done:
+                                     //     V stage g % 2 and S buffer g % 2 free
+    uint64_t *s_full = bars + 6;     // [2] S of step g in TMEM buffer g % 2 (its K stage free)
+    uint64_t *p_full = bars + 8;     // [2] P of step g written (four warp arrivals)
+    uint64_t *q_full = bars + 10;    // Q of the item landed
+    uint64_t *mma_idle = bars + 11;  // after a timeout: the MMAs still running are done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
     __shared__ PrefillSched sched;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hkv = p.num_kv_heads, H = p.num_heads;
 
     if (tid == 0) {
         prefetch_tensormap(&p.tmap_k);
         prefetch_tensormap(&p.tmap_v);
-        for (int i = 0; i < 2 * S; ++i) mbar_init(&full[i], 1);   // full and empty
-        mbar_init(s_done, 1);
-        mbar_init(pv_done, 1);
+        prefetch_tensormap(&tmap_q);
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&p_full[0], TC_SOFTMAX_WARPS);
+        mbar_init(&p_full[1], TC_SOFTMAX_WARPS);
+        mbar_init(q_full, 1);
+        mbar_init(mma_idle, 1);
         fence_mbar_init();
     }
     if (warp == 0) tc5_alloc(tmem_slot, TC_TMEM_COLS);
@@ -125,23 +131,15 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
     __syncthreads();
     tc5_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;   // this warp's TMEM lanes
-    const uint32_t tS = tmem, tP = tmem + 64, tO = tmem + 128;
+    const uint32_t tO = tmem + 128;
 
     const int total = prefill_schedule<G, TC_ROWS>(p, groups, sched);
 
     // the caches (and q, out) only after the kernel before this one is done
     grid_dependency_wait();
 
-    const uint64_t pol = policy_evict_last();      // the sequence's other items reread them
-    // a box past the end of the tensor fills with zeros
-    const int z_none = (int)min((long long)INT_MAX, p.num_blocks * (long long)Hkv);
-    long long kglob = 0;                           // steps through the K/V ring so far
-    uint32_t n_s = 0, n_pv = 0;                    // phases of s_done and pv_done so far
-    bool ok = true;
-
     const int R = (int)gridDim.x, me = (int)blockIdx.x;
-    // The geometry of an item; the producer and the consumers compute it alike.
+    // The geometry of an item; every role computes it alike.
     struct Item {
         int s, j, grp, q0, nq, L, nrows, nsteps, nb_seq;
     };
@@ -160,200 +158,250 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
         return true;
     };
 
-    if (warp == TC_CONSUMERS) {
-        // ---- producer: step kk of the block's items into stage kk % S once its
-        // previous use is done (lane 0 issues)
-        long long kk = 0;
+    if (warp == TC_COPY_WARP) {
+        // ---- copies: Q of item k once S of item k-1's last step is done; K and
+        // V of step g into stage g % 2 once S(g-2), resp. P.V(g-2), is done
+        const uint64_t pol = policy_evict_last();  // the sequence's other items reread them
+        // a box past the end of the tensor fills with zeros
+        const int z_none = (int)min((long long)INT_MAX, p.num_blocks * (long long)Hkv);
+        long long g = 0, nk = 0, nv = 0;           // steps so far; K and V copies issued
+        int nq_issued = 0;
         bool pok = true;
         Item it;
         for (int k = 0; pok && item_at(k, it); ++k) {
-            for (int c = 0; pok && c < it.nsteps; ++c, ++kk) {
-                const int st = (int)(kk % S);
-                bool w = true;
-                if (threadIdx.x % 32 == 0) {
-                    w = kk < S || mbar_wait_bounded(&empty[st], (uint32_t)(((kk / S) - 1) & 1), p.err);
+            bool w = true;
+            if (lane == 0) {
+                if (g > 0) w = mbar_wait_bounded(&s_full[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), p.err);
+                if (w) {
+                    mbar_arrive_expect_tx(q_full, (uint32_t)Lay::Q_BYTES);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        tma_load_3d(sQ + h * (TC_ROWS * 128), &tmap_q, h * 64, it.j * G,
+                                    it.q0 + it.grp * TOKS, q_full, pol);
+                    ++nq_issued;
+                }
+            }
+            pok = __shfl_sync(0xffffffffu, w, 0);
+            for (int c = 0; pok && c < it.nsteps; ++c, ++g) {
+                const int b = (int)(g & 1);
+                const uint32_t ph_prev = (uint32_t)(((g >> 1) - 1) & 1);   // phase of step g - 2
+                w = true;
+                if (lane == 0) {
+                    int z[TC_KEYS / 16];
+#pragma unroll
+                    for (int i = 0; i < TC_KEYS / 16; ++i) {   // independent loads
+                        const int lb = (TC_KEYS / 16) * c + i;
+                        const int pb = lb < it.nb_seq ? p.block_tables[(long long)it.s * p.max_blocks + lb] : -1;
+                        z[i] = z_none;                         // past the sequence: zeros
+                        if (lb < it.nb_seq) {
+                            if (pb >= 0 && (long long)pb < p.num_blocks) z[i] = pb * Hkv + it.j;
+                            else set_error(p.err, ERR_BLOCK_ID);
+                        }
+                    }
+                    w = g < 2 || mbar_wait_bounded(&s_full[b], ph_prev, p.err);
                     if (w) {
-                        int pbs[TC_KEYS / 16];
+                        unsigned char *dK = sK + (size_t)b * KVB;
+                        mbar_arrive_expect_tx(&kfull[b], KVB);
 #pragma unroll
-                        for (int b = 0; b < TC_KEYS / 16; ++b) {   // independent loads
-                            const int lb = (TC_KEYS / 16) * c + b;
-                            pbs[b] = lb < it.nb_seq ? p.block_tables[(long long)it.s * p.max_blocks + lb] : -1;
-                        }
-                        unsigned char *dK = sKV + (size_t)st * 2 * KVB, *dV = dK + KVB;
-                        mbar_arrive_expect_tx(&full[st], 2 * KVB);
+                        for (int i = 0; i < TC_KEYS / 16; ++i)
 #pragma unroll
-                        for (int b = 0; b < TC_KEYS / 16; ++b) {
-                            const int lb = (TC_KEYS / 16) * c + b;
-                            int z = z_none;                // past the sequence: zeros
-                            if (lb < it.nb_seq) {
-                                if (pbs[b] >= 0 && (long long)pbs[b] < p.num_blocks) z = pbs[b] * Hkv + it.j;
-                                else set_error(p.err, ERR_BLOCK_ID);
-                            }
+                            for (int h = 0; h < NH; ++h)
+                                tma_load_3d(dK + h * (TC_KEYS * 128) + i * 2048, &p.tmap_k, h * 64, 0, z[i],
+                                            &kfull[b], pol);
+                        ++nk;
+                        w = g < 2 || mbar_wait_bounded(&pv_done[b], ph_prev, p.err);
+                    }
+                    if (w) {
+                        unsigned char *dV = sV + (size_t)b * KVB;
+                        mbar_arrive_expect_tx(&vfull[b], KVB);
 #pragma unroll
-                            for (int h = 0; h < NH; ++h) {
-                                tma_load_3d(dK + h * (TC_KEYS * 128) + b * 2048, &p.tmap_k, h * 64, 0, z,
-                                            &full[st], pol);
-                                tma_load_3d(dV + h * (TC_KEYS * 128) + b * 2048, &p.tmap_v, h * 64, 0, z,
-                                            &full[st], pol);
-                            }
-                        }
+                        for (int i = 0; i < TC_KEYS / 16; ++i)
+#pragma unroll
+                            for (int h = 0; h < NH; ++h)
+                                tma_load_3d(dV + h * (TC_KEYS * 128) + i * 2048, &p.tmap_v, h * 64, 0, z[i],
+                                            &vfull[b], pol);
+                        ++nv;
                     }
                 }
                 pok = __shfl_sync(0xffffffffu, w, 0);
             }
         }
-        // copies still landing when the block exits: wait (bounded) for the last S
-        if (threadIdx.x % 32 == 0)
-            for (long long i = (kk > S ? kk - S : 0); i < kk; ++i)
-                mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), p.err);
+        // copies still landing when the block exits: wait (bounded) for the
+        // last Q and the last two steps' K and V copies issued
+        if (lane == 0) {
+            if (nq_issued > 0) mbar_wait_bounded(q_full, (uint32_t)((nq_issued - 1) & 1), p.err);
+            for (long long i = (nk > 2 ? nk - 2 : 0); i < nk; ++i)
+                mbar_wait_bounded(&kfull[i & 1], (uint32_t)((i >> 1) & 1), p.err);
+            for (long long i = (nv > 2 ? nv - 2 : 0); i < nv; ++i)
+                mbar_wait_bounded(&vfull[i & 1], (uint32_t)((i >> 1) & 1), p.err);
+        }
+    } else if (warp == TC_MMA_WARP) {
+        // ---- MMAs (lane 0 issues): per item S(g0), S(g0+1), then per step
+        // PV(g) and, once PV(g) is done, S(g+2).  Waiting for every PV keeps
+        // each pv_done barrier at most one phase ahead of its waiters.
+        long long g0 = 0;
+        bool mok = true;
+        Item it;
+        // S of step g into TMEM buffer g % 2, K from stage g % 2
+        auto issue_s = [&](long long g) -> bool {
+            const int b = (int)(g & 1);
+            if (!mbar_wait_bounded(&kfull[b], (uint32_t)((g >> 1) & 1), p.err)) return false;
+            const uint32_t kaddr = smem_u32(sK + (size_t)b * KVB);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t off = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes
+                tc5_mma(tmem + 64 * b,
+                        tc5_desc_sw128(smem_u32(sQ) + (ks >> 2) * (TC_ROWS * 128) + off, 16, 1024),
+                        tc5_desc_sw128(kaddr + (ks >> 2) * (TC_KEYS * 128) + off, 16, 1024),
+                        ID_S, ks > 0);
+            }
+            tc5_commit(&s_full[b]);
+            return true;
+        };
+        for (int k = 0; mok && item_at(k, it); ++k) {
+            const int n = it.nsteps;
+            bool w = true;
+            if (lane == 0) {
+                w = mbar_wait_bounded(q_full, (uint32_t)(k & 1), p.err);
+                for (int c = 0; w && c < min(2, n); ++c) w = issue_s(g0 + c);
+                for (int c = 0; w && c < n; ++c) {
+                    const long long g = g0 + c;
+                    const int b = (int)(g & 1);
+                    const uint32_t ph = (uint32_t)((g >> 1) & 1);
+                    w = mbar_wait_bounded(&p_full[b], ph, p.err) && mbar_wait_bounded(&vfull[b], ph, p.err);
+                    if (!w) break;
+                    tc5_fence_after_sync();
+                    const uint32_t vaddr = smem_u32(sV + (size_t)b * KVB);
+#pragma unroll
+                    for (int ks = 0; ks < TC_KEYS / 16; ++ks)
+                        tc5_mma_ta(tO, tmem + 64 * b + 8 * ks,
+                                   tc5_desc_sw128(vaddr + ks * 2048, TC_KEYS * 128, 1024), ID_O,
+                                   (c > 0 || ks > 0) ? 1u : 0u);
+                    tc5_commit(&pv_done[b]);
+                    w = mbar_wait_bounded(&pv_done[b], ph, p.err);   // P of buffer b read
+                    if (w && c + 2 < n) w = issue_s(g + 2);
+                }
+            }
+            mok = __shfl_sync(0xffffffffu, w, 0);
+            g0 += n;
+        }
+        // after a timeout, MMAs may still be running: wait for them
+        if (lane == 0 && !mok) {
+            tc5_commit(mma_idle);
+            mbar_wait_bounded(mma_idle, 0, p.err);
+        }
     } else {
-        // ---- consumers (thread 0 also issues the MMAs)
+        // ---- softmax: thread tid owns row tid of every item
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;   // this warp's TMEM lanes
+        const float sl2 = p.scale_log2;
+        long long g = 0;
+        bool ok = true;
         Item it;
         for (int k = 0; ok && item_at(k, it); ++k) {
-            const int s = it.s, j = it.j, grp = it.grp, q0 = it.q0, nq = it.nq, L = it.L;
-            const int nrows = it.nrows, nsteps = it.nsteps, nb_seq = it.nb_seq;
-            // this thread's row
+            const int n = it.nsteps;
             const int r = tid;
-            const bool row_ok = r < nrows;
-            const int rr = grp * TC_ROWS + r;
+            const bool row_ok = r < it.nrows;
+            const int rr = it.grp * TC_ROWS + r;
             const int tok = rr / G, head = rr % G;
-            const int lim = L - nq + tok;                         // last visible position
-            (void)s;
-
-            // -- Q rows into sQ ([NH][128 rows][128 B], 128-byte swizzle); zeros past the run
-            {
-                const uint4 *qr = reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const T *>(p.q) + (long long)(q0 + (row_ok ? tok : 0)) * p.q_seq_stride +
-                    (long long)(j * G + head) * D);
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 v = row_ok ? __ldg(qr + c) : make_uint4(0, 0, 0, 0);
-                    const int h = c >> 3, cc = c & 7;
-                    *reinterpret_cast<uint4 *>(sQ + h * (TC_ROWS * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
-                }
-            }
-            fence_proxy_async_smem();              // before the MMAs read sQ
-
-            // -- S of step c (thread 0, after its stage landed); false on a timeout
-            auto issue_s = [&](int c) -> bool {
-                const long long kk = kglob + c;
-                const int st = (int)(kk % S);
-                if (!mbar_wait_bounded(&full[st], (uint32_t)((kk / S) & 1), p.err)) return false;
-                const uint32_t kaddr = smem_u32(sKV + (size_t)st * 2 * KVB);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes
-                    tc5_mma(tS,
-                            tc5_desc_sw128(smem_u32(sQ) + (ks >> 2) * (TC_ROWS * 128) + off, 16, 1024),
-                            tc5_desc_sw128(kaddr + (ks >> 2) * (TC_KEYS * 128) + off, 16, 1024),
-                            ID_S, ks > 0);
-                }
-                tc5_commit(s_done);
-                return true;
-            };
-
+            // last visible position; rows past the run see what its last row sees
+            const int lim = it.L - it.nq + min(tok, it.nq - 1);
             float m_run = -INFINITY, l_run = 0.f;
-            tc5_fence_before_sync();
-            tc_consumers_sync();                   // sQ written
-            bool issued = true;
-            if (tid == 0) {
-                tc5_fence_after_sync();
-                issued = issue_s(0);
-            }
-
-            for (int c = 0; c < nsteps; ++c) {
-                const bool got = issued && mbar_wait_bounded(s_done, n_s & 1, p.err);
-                ++n_s;
-                if (!tc_consumers_sync_and(got)) { ok = false; break; }
+            for (int c = 0; c < n; ++c, ++g) {
+                const int b = (int)(g & 1);
+                const uint32_t ph = (uint32_t)((g >> 1) & 1);
+                const uint32_t tS = tmem + 64 * b + lane_base;
+                const bool got = mbar_wait_bounded(&s_full[b], ph, p.err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 tc5_fence_after_sync();
 
-                // -- this row's 64 scores
+                // -- this row's 64 scores; the causal mask only where some row needs it
                 float sv[TC_KEYS];
-                tc5_ld32(tS + lane_off, *reinterpret_cast<float(*)[32]>(&sv[0]));
-                tc5_ld32(tS + lane_off + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-                const int kb = c * TC_KEYS;
-                float mx = -INFINITY;
+                tc5_ld64u(tS, *reinterpret_cast<uint32_t(*)[TC_KEYS]>(&sv[0]));
+                const int nvis = lim - c * TC_KEYS + 1;      // positions of this step the row sees
+                if (__any_sync(0xffffffffu, nvis < TC_KEYS)) {
 #pragma unroll
-                for (int e = 0; e < TC_KEYS; ++e) {
-                    sv[e] = (row_ok && kb + e <= lim) ? sv[e] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[e]);
+                    for (int e = 0; e < TC_KEYS; ++e) sv[e] = e < nvis ? sv[e] : -INFINITY;
                 }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < TC_KEYS; e += 8) {
+                    m4[0] = max3f(m4[0], sv[e], sv[e + 1]);
+                    m4[1] = max3f(m4[1], sv[e + 2], sv[e + 3]);
+                    m4[2] = max3f(m4[2], sv[e + 4], sv[e + 5]);
+                    m4[3] = max3f(m4[3], sv[e + 6], sv[e + 7]);
+                }
+                const float mxs = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
                 // lazy rescaling: the reference level moves only by more than 2^RESCALE_LOG2
-                const float m_new = mx > m_run + RESCALE_LOG2 ? mx : m_run;
+                const float m_new = mxs > m_run + RESCALE_LOG2 ? mxs : m_run;
                 const float ms = m_new == -INFINITY ? 0.f : m_new;
                 const float alpha = m_new == m_run ? 1.f : ex2(m_run - ms);
+                // probabilities 2^(s * scale_log2 - m), two lanes per instruction
                 uint32_t pw[TC_KEYS / 2];
-                float psum = 0.f;
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
+                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-ms, -ms);
 #pragma unroll
                 for (int e = 0; e < TC_KEYS / 2; ++e) {
-                    pw[e] = Mma<T>::pack(ex2(sv[2 * e] - ms), ex2(sv[2 * e + 1] - ms));
-                    float a, b;
-                    Mma<T>::unpack(pw[e], a, b);
-                    psum += a + b;
+                    const float2 x = fma2(make_float2(sv[2 * e], sv[2 * e + 1]), sc2, nm2);
+                    const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+                    pw[e] = Mma<T>::pack(pe.x, pe.y);
+                    acc[e & 3] = add2(acc[e & 3], pe);
                 }
-                l_run = l_run * alpha + psum;
+                const float2 a2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+                l_run = l_run * alpha + (a2.x + a2.y);
                 m_run = m_new;
-                // this row of O to the new level (O holds nothing before the first P.V)
+                // this row of O to the new level, once P.V(g-1) is done (O holds
+                // nothing before the item's first P.V)
                 if (__any_sync(0xffffffffu, c > 0 && alpha != 1.f)) {
+                    const long long gp = g - 1;
+                    const bool done = mbar_wait_bounded(&pv_done[gp & 1], (uint32_t)((gp >> 1) & 1), p.err);
+                    if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
+                    tc5_fence_after_sync();
                     const float f = c > 0 ? alpha : 1.f;
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         float o[32];
-                        tc5_ld32(tO + lane_off + c0, o);
+                        tc5_ld32(tO + lane_base + c0, o);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] *= f;
-                        tc5_st32(tO + lane_off + c0, o);
+                        tc5_st32(tO + lane_base + c0, o);
                     }
                 }
-                // P row r into TMEM: 64 keys, two per column
-                tc5_st32u(tP + lane_off, pw);
+                // P over the first 32 columns of the S buffer (waits for the store)
+                tc5_st32u(tS, pw);
                 // V rows of the sequence's last block past L hold other tokens' data
-                // (zero-weighted, but 0 * NaN is NaN): clear them
-                {
-                    const int st = (int)((kglob + c) % S);
-                    unsigned char *dV = sKV + (size_t)st * 2 * KVB + KVB;
-                    const int tail = L & 15, lb_last = nb_seq - 1;
-                    const int b = lb_last - (TC_KEYS / 16) * c;
-                    if (tail != 0 && b >= 0 && b < TC_KEYS / 16) {
-                        const int nclr = (16 - tail) * NH * 8;    // 16-byte pieces
-                        for (int i = tid; i < nclr; i += 128) {
-                            const int h = i / ((16 - tail) * 8), rem = i % ((16 - tail) * 8);
-                            const int row = 16 * b + tail + rem / 8;
-                            *reinterpret_cast<uint4 *>(dV + h * (TC_KEYS * 128) + row * 128 + (rem % 8) * 16) =
-                                make_uint4(0, 0, 0, 0);
-                        }
+                // (zero-weighted, but 0 * NaN is NaN): clear them once V has landed
+                const int tail = it.L & 15, bl = it.nb_seq - 1 - (TC_KEYS / 16) * c;
+                if (tail != 0 && bl >= 0 && bl < TC_KEYS / 16) {
+                    const bool landed = mbar_wait_bounded(&vfull[b], ph, p.err);
+                    if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
+                    unsigned char *dV = sV + (size_t)b * KVB;
+                    const int nclr = (16 - tail) * NH * 8;     // 16-byte pieces
+                    for (int i = tid; i < nclr; i += TC_SOFTMAX_WARPS * 32) {
+                        const int h = i / ((16 - tail) * 8), rem = i % ((16 - tail) * 8);
+                        const int row = 16 * bl + tail + rem / 8;
+                        *reinterpret_cast<uint4 *>(dV + h * (TC_KEYS * 128) + row * 128 + (rem % 8) * 16) =
+                            make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async_smem();              // the cleared rows before the MMA
                 }
-                fence_proxy_async_smem();          // the cleared rows before the MMA
                 tc5_fence_before_sync();
-                tc_consumers_sync();
-                if (tid == 0) {
-                    tc5_fence_after_sync();
-                    const int st = (int)((kglob + c) % S);
-                    const uint32_t vaddr = smem_u32(sKV + (size_t)st * 2 * KVB + KVB);
-#pragma unroll
-                    for (int ks = 0; ks < TC_KEYS / 16; ++ks)
-                        tc5_mma_ta(tO, tP + 8 * ks,
-                                   tc5_desc_sw128(vaddr + ks * 2048, TC_KEYS * 128, 1024), ID_O,
-                                   (c > 0 || ks > 0) ? 1u : 0u);
-                    tc5_commit(&empty[st]);        // the stage is free once P.V is done
-                    if (c + 1 < nsteps) issued = issue_s(c + 1);
-                    else tc5_commit(pv_done);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
 
-            // -- O / l into out (this thread's row)
-            const bool got = mbar_wait_bounded(pv_done, n_pv & 1, p.err);
-            ++n_pv;
-            if (!tc_consumers_sync_and(got)) { ok = false; break; }
+            // -- O / l into out (this thread's row), once the item's last P.V is done
+            const long long gl = g - 1;
+            const bool done = mbar_wait_bounded(&pv_done[gl & 1], (uint32_t)((gl >> 1) & 1), p.err);
+            if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
             tc5_fence_after_sync();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            T *o = reinterpret_cast<T *>(p.out) + ((long long)(q0 + tok) * H + j * G + head) * D;
+            T *o = reinterpret_cast<T *>(p.out) + ((long long)(it.q0 + tok) * H + it.j * G + head) * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 float v[32];
-                tc5_ld32(tO + lane_off + c0, v);
+                tc5_ld32(tO + lane_base + c0, v);
                 if (row_ok) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
@@ -366,9 +414,9 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
                     }
                 }
             }
-            kglob += nsteps;
+            // O read before the next item's first P.V overwrites it (that P.V
+            // waits for this warp's next arrival)
             tc5_fence_before_sync();
-            tc_consumers_sync();                   // sQ and TMEM free for the next item
         }
     }
 
@@ -378,10 +426,12 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, int groups) {
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_prefill_tc(const DecodeParams &p, int groups, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const DecodeParams &p, const CUtensorMap &tmap_q, int groups,
+                              cudaStream_t st) {
     using Lay = PrefillTcLayout<T, D>;
     constexpr size_t smem = Lay::BYTES;
-    static_assert(smem + sizeof(PrefillSched) <= 227 * 1024, "shared memory");
+    static_assert(TC_BLOCKS_PER_SM * (smem + sizeof(PrefillSched) + 1024) <= 228 * 1024,
+                  "two blocks per SM");
     auto kern = prefill_tc_kernel<T, D, G>;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -406,7 +456,7 @@ cudaError_t launch_prefill_tc(const DecodeParams &p, int groups, cudaStream_t st
     if (blocks <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3((TC_CONSUMERS + 1) * 32, 1, 1);
+    cfg.blockDim = dim3(TC_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -414,15 +464,16 @@ cudaError_t launch_prefill_tc(const DecodeParams &p, int groups, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p, groups);
+    e = cudaLaunchKernelEx(&cfg, kern, p, tmap_q, groups);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t dispatch_prefill_tc(const DecodeParams &p, int D, int G, int groups, cudaStream_t st) {
+cudaError_t dispatch_prefill_tc(const DecodeParams &p, const CUtensorMap &tmap_q, int D, int G,
+                                int groups, cudaStream_t st) {
 #define PA_CASE(DD, GG) \
-    if (D == DD && G == GG) return launch_prefill_tc<T, DD, GG>(p, groups, st);
+    if (D == DD && G == GG) return launch_prefill_tc<T, DD, GG>(p, tmap_q, groups, st);
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
 #undef PA_CASE
