@@ -30,9 +30,9 @@
 //      accumulates in TMEM over the whole item and is read back, normalised,
 //      at the end.
 // Roles: warps 0-3 run the softmax (warp w reaches TMEM lanes 32w..32w+31);
-// warp 4 (lane 0) keeps the copies going -- Q once per item, and rings of two
-// K stages and two V stages (a K stage is free once its S is done, a V stage
-// once its P.V is); warp 5 (lane 0) issues the MMAs in the order S(0), S(1),
+// warps 4 and 6 keep the copies going -- Q once per item and a ring of two K
+// stages (warp 4; a K stage is free once its S is done), a ring of two V
+// stages (warp 6; free once its P.V is done); warp 5 (lane 0) issues the MMAs in the order S(0), S(1),
 // PV(0), S(2), PV(1), ... and reports their completion through
 // tcgen05.commit on mbarriers.  S(g + 2) overwrites the buffer PV(g) reads
 // its P from, so it is issued once PV(g) is complete.  Two blocks share an
@@ -78,9 +78,10 @@ struct PrefillTcLayout {
 constexpr uint32_t TC_TMEM_COLS = 256;
 constexpr int TC_BLOCKS_PER_SM = 2;
 constexpr int TC_SOFTMAX_WARPS = 4;      // one row per thread
-constexpr int TC_COPY_WARP = 4;
+constexpr int TC_COPY_WARP = 4;        // Q and K copies
 constexpr int TC_MMA_WARP = 5;
-constexpr int TC_THREADS = 6 * 32;
+constexpr int TC_VCOPY_WARP = 6;       // V copies
+constexpr int TC_THREADS = 7 * 32;
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(TC_THREADS, TC_BLOCKS_PER_SM)
@@ -158,19 +159,27 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         return true;
     };
 
-    if (warp == TC_COPY_WARP) {
-        // ---- copies: Q of item k once S of item k-1's last step is done; K and
-        // V of step g into stage g % 2 once S(g-2), resp. P.V(g-2), is done
+    if (warp == TC_COPY_WARP || warp == TC_VCOPY_WARP) {
+        // ---- copies.  Warp TC_COPY_WARP: Q of item k once S of item k-1's
+        // last step is done, and K of step g into stage g % 2 once S(g-2) is
+        // done; warp TC_VCOPY_WARP: V of step g once P.V(g-2) is done.  Two
+        // warps, so that a K copy never waits behind a V stage (S(g-2)
+        // completes well before P.V(g-2)).
+        const bool kside = warp == TC_COPY_WARP;
         const uint64_t pol = policy_evict_last();  // the sequence's other items reread them
+        const CUtensorMap *tmap = kside ? &p.tmap_k : &p.tmap_v;
+        unsigned char *const stage0 = kside ? sK : sV;
+        uint64_t *const full = kside ? kfull : vfull;
+        uint64_t *const empty = kside ? s_full : pv_done;
         // a box past the end of the tensor fills with zeros
         const int z_none = (int)min((long long)INT_MAX, p.num_blocks * (long long)Hkv);
-        long long g = 0, nk = 0, nv = 0;           // steps so far; K and V copies issued
+        long long g = 0, ncopies = 0;              // steps so far; stages issued
         int nq_issued = 0;
         bool pok = true;
         Item it;
         for (int k = 0; pok && item_at(k, it); ++k) {
             bool w = true;
-            if (lane == 0) {
+            if (kside && lane == 0) {
                 if (g > 0) w = mbar_wait_bounded(&s_full[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), p.err);
                 if (w) {
                     mbar_arrive_expect_tx(q_full, (uint32_t)Lay::Q_BYTES);
@@ -182,58 +191,49 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 }
             }
             pok = __shfl_sync(0xffffffffu, w, 0);
+            // Lane i < 4 holds the block-table entry of block i of the step,
+            // read one step ahead so that its latency passes while the warp
+            // waits for a stage; lanes l < 4 * NH then issue one box each
+            // (block l % 4, 64-element half l / 4).
+            const int32_t *row = p.block_tables + (long long)it.s * p.max_blocks;
+            auto fetch = [&](int c) -> int {
+                const int lb = (TC_KEYS / 16) * c + lane;
+                return (lane < TC_KEYS / 16 && c < it.nsteps && lb < it.nb_seq) ? __ldg(row + lb) : -1;
+            };
+            int pb_next = fetch(0);
             for (int c = 0; pok && c < it.nsteps; ++c, ++g) {
                 const int b = (int)(g & 1);
                 const uint32_t ph_prev = (uint32_t)(((g >> 1) - 1) & 1);   // phase of step g - 2
-                w = true;
-                if (lane == 0) {
-                    int z[TC_KEYS / 16];
-#pragma unroll
-                    for (int i = 0; i < TC_KEYS / 16; ++i) {   // independent loads
-                        const int lb = (TC_KEYS / 16) * c + i;
-                        const int pb = lb < it.nb_seq ? p.block_tables[(long long)it.s * p.max_blocks + lb] : -1;
-                        z[i] = z_none;                         // past the sequence: zeros
-                        if (lb < it.nb_seq) {
-                            if (pb >= 0 && (long long)pb < p.num_blocks) z[i] = pb * Hkv + it.j;
-                            else set_error(p.err, ERR_BLOCK_ID);
-                        }
-                    }
-                    w = g < 2 || mbar_wait_bounded(&s_full[b], ph_prev, p.err);
-                    if (w) {
-                        unsigned char *dK = sK + (size_t)b * KVB;
-                        mbar_arrive_expect_tx(&kfull[b], KVB);
-#pragma unroll
-                        for (int i = 0; i < TC_KEYS / 16; ++i)
-#pragma unroll
-                            for (int h = 0; h < NH; ++h)
-                                tma_load_3d(dK + h * (TC_KEYS * 128) + i * 2048, &p.tmap_k, h * 64, 0, z[i],
-                                            &kfull[b], pol);
-                        ++nk;
-                        w = g < 2 || mbar_wait_bounded(&pv_done[b], ph_prev, p.err);
-                    }
-                    if (w) {
-                        unsigned char *dV = sV + (size_t)b * KVB;
-                        mbar_arrive_expect_tx(&vfull[b], KVB);
-#pragma unroll
-                        for (int i = 0; i < TC_KEYS / 16; ++i)
-#pragma unroll
-                            for (int h = 0; h < NH; ++h)
-                                tma_load_3d(dV + h * (TC_KEYS * 128) + i * 2048, &p.tmap_v, h * 64, 0, z[i],
-                                            &vfull[b], pol);
-                        ++nv;
+                int zl = z_none;                       // past the sequence: zeros
+                {
+                    const int lb = (TC_KEYS / 16) * c + lane, pb = pb_next;
+                    if (lane < TC_KEYS / 16 && lb < it.nb_seq) {
+                        if (pb >= 0 && (long long)pb < p.num_blocks) zl = pb * Hkv + it.j;
+                        else if (kside) set_error(p.err, ERR_BLOCK_ID);
                     }
                 }
-                pok = __shfl_sync(0xffffffffu, w, 0);
+                pb_next = fetch(c + 1);
+                const int blk = lane % (TC_KEYS / 16), h = lane / (TC_KEYS / 16);
+                const int z = __shfl_sync(0xffffffffu, zl, blk);
+                w = true;
+                if (lane == 0) {
+                    w = g < 2 || mbar_wait_bounded(&empty[b], ph_prev, p.err);
+                    if (w) mbar_arrive_expect_tx(&full[b], KVB);
+                }
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (w && lane < (TC_KEYS / 16) * NH)
+                    tma_load_3d(stage0 + (size_t)b * KVB + h * (TC_KEYS * 128) + blk * 2048, tmap, h * 64, 0, z,
+                                &full[b], pol);
+                if (w) ++ncopies;
+                pok = w;
             }
         }
         // copies still landing when the block exits: wait (bounded) for the
-        // last Q and the last two steps' K and V copies issued
+        // last Q and the last two stages issued
         if (lane == 0) {
             if (nq_issued > 0) mbar_wait_bounded(q_full, (uint32_t)((nq_issued - 1) & 1), p.err);
-            for (long long i = (nk > 2 ? nk - 2 : 0); i < nk; ++i)
-                mbar_wait_bounded(&kfull[i & 1], (uint32_t)((i >> 1) & 1), p.err);
-            for (long long i = (nv > 2 ? nv - 2 : 0); i < nv; ++i)
-                mbar_wait_bounded(&vfull[i & 1], (uint32_t)((i >> 1) & 1), p.err);
+            for (long long i = (ncopies > 2 ? ncopies - 2 : 0); i < ncopies; ++i)
+                mbar_wait_bounded(&full[i & 1], (uint32_t)((i >> 1) & 1), p.err);
         }
     } else if (warp == TC_MMA_WARP) {
         // ---- MMAs (lane 0 issues): per item S(g0), S(g0+1), then per step
@@ -243,17 +243,22 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         bool mok = true;
         Item it;
         // S of step g into TMEM buffer g % 2, K from stage g % 2
+        // Descriptors of the operands' bases; an offset of a multiple of 16
+        // bytes inside shared memory adds offset / 16 to the start-address
+        // field (addresses stay below 2^18, so the field does not overflow).
+        const uint64_t dq = tc5_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk0 = tc5_desc_sw128(smem_u32(sK), 16, 1024), dk1 = dk0 + (KVB >> 4);
+        const uint64_t dv0 = tc5_desc_sw128(smem_u32(sV), TC_KEYS * 128, 1024), dv1 = dv0 + (KVB >> 4);
         auto issue_s = [&](long long g) -> bool {
             const int b = (int)(g & 1);
             if (!mbar_wait_bounded(&kfull[b], (uint32_t)((g >> 1) & 1), p.err)) return false;
-            const uint32_t kaddr = smem_u32(sK + (size_t)b * KVB);
+            const uint64_t kb = b ? dk1 : dk0;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t off = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes
-                tc5_mma(tmem + 64 * b,
-                        tc5_desc_sw128(smem_u32(sQ) + (ks >> 2) * (TC_ROWS * 128) + off, 16, 1024),
-                        tc5_desc_sw128(kaddr + (ks >> 2) * (TC_KEYS * 128) + off, 16, 1024),
-                        ID_S, ks > 0);
+                // 16 elements = 32 bytes along K inside a 128-byte row; 64 per row group
+                const uint32_t qo = (uint32_t)(((ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32) >> 4);
+                const uint32_t ko = (uint32_t)(((ks >> 2) * (TC_KEYS * 128) + (ks & 3) * 32) >> 4);
+                tc5_mma(tmem + 64 * b, dq + qo, kb + ko, ID_S, ks > 0);
             }
             tc5_commit(&s_full[b]);
             return true;
@@ -271,11 +276,10 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                     w = mbar_wait_bounded(&p_full[b], ph, p.err) && mbar_wait_bounded(&vfull[b], ph, p.err);
                     if (!w) break;
                     tc5_fence_after_sync();
-                    const uint32_t vaddr = smem_u32(sV + (size_t)b * KVB);
+                    const uint64_t vb = b ? dv1 : dv0;
 #pragma unroll
-                    for (int ks = 0; ks < TC_KEYS / 16; ++ks)
-                        tc5_mma_ta(tO, tmem + 64 * b + 8 * ks,
-                                   tc5_desc_sw128(vaddr + ks * 2048, TC_KEYS * 128, 1024), ID_O,
+                    for (int ks = 0; ks < TC_KEYS / 16; ++ks)      // 16 keys = 2048 bytes
+                        tc5_mma_ta(tO, tmem + 64 * b + 8 * ks, vb + (uint32_t)(ks * 2048 >> 4), ID_O,
                                    (c > 0 || ks > 0) ? 1u : 0u);
                     tc5_commit(&pv_done[b]);
                     w = mbar_wait_bounded(&pv_done[b], ph, p.err);   // P of buffer b read
