@@ -66,15 +66,15 @@ struct PrefillTcLayout {
     static constexpr size_t OFF_K = OFF_Q + Q_BYTES;
     static constexpr size_t OFF_V = OFF_K + (size_t)STAGES * KV_BYTES;
     static constexpr size_t OFF_BARS = OFF_V + (size_t)STAGES * KV_BYTES;
-    static constexpr int NBARS = 12;
+    static constexpr int NBARS = 14;
     static constexpr size_t OFF_TMEM = OFF_BARS + (size_t)NBARS * 8;
     static constexpr size_t BYTES = OFF_TMEM + 16 + 1024;              // + alignment of the base
     static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0,
                   "1024-byte aligned swizzle atoms");
 };
 
-// TMEM columns of a block: S buffers 0..63 and 64..127 (P over the first 32
-// columns of its buffer), O 128..128+D-1
+// TMEM columns of a block: S 0..63, P of even steps 64..95, of odd steps
+// 96..127 (two 16-bit probabilities per column), O 128..128+D-1
 constexpr uint32_t TC_TMEM_COLS = 256;
 constexpr int TC_BLOCKS_PER_SM = 2;
 constexpr int TC_SOFTMAX_WARPS = 4;      // one row per thread
@@ -105,11 +105,13 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     uint64_t *kfull = bars;          // [2] K of step g landed in stage g % 2
     uint64_t *vfull = bars + 2;      // [2] V of step g landed
     uint64_t *pv_done = bars + 4;    // [2] P.V of step g (and every MMA before it) done:
-                                     //     V stage g % 2 and S buffer g % 2 free
-    uint64_t *s_full = bars + 6;     // [2] S of step g in TMEM buffer g % 2 (its K stage free)
+                                     //     V stage g % 2 and P buffer g % 2 free
+    uint64_t *kfree = bars + 6;      // [2] S of step g done: K stage g % 2 free
     uint64_t *p_full = bars + 8;     // [2] P of step g written (four warp arrivals)
     uint64_t *q_full = bars + 10;    // Q of the item landed
-    uint64_t *mma_idle = bars + 11;  // after a timeout: the MMAs still running are done
+    uint64_t *mma_idle = bars + 11;  // the block's MMAs are all done
+    uint64_t *s_full = bars + 12;    // S of a step in TMEM (one phase per step)
+    uint64_t *s_free = bars + 13;    // S of a step read by the softmax (four warp arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::OFF_TMEM);
     __shared__ PrefillSched sched;
 
@@ -125,6 +127,8 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         mbar_init(&p_full[1], TC_SOFTMAX_WARPS);
         mbar_init(q_full, 1);
         mbar_init(mma_idle, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, TC_SOFTMAX_WARPS);
         fence_mbar_init();
     }
     if (warp == 0) tc5_alloc(tmem_slot, TC_TMEM_COLS);
@@ -132,7 +136,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     __syncthreads();
     tc5_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 128;
+    const uint32_t tS = tmem, tP = tmem + 64, tO = tmem + 128;
 
     const int total = prefill_schedule<G, TC_ROWS>(p, groups, sched);
 
@@ -170,7 +174,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const CUtensorMap *tmap = kside ? &p.tmap_k : &p.tmap_v;
         unsigned char *const stage0 = kside ? sK : sV;
         uint64_t *const full = kside ? kfull : vfull;
-        uint64_t *const empty = kside ? s_full : pv_done;
+        uint64_t *const empty = kside ? kfree : pv_done;
         // a box past the end of the tensor fills with zeros
         const int z_none = (int)min((long long)INT_MAX, p.num_blocks * (long long)Hkv);
         long long g = 0, ncopies = 0;              // steps so far; stages issued
@@ -180,7 +184,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         for (int k = 0; pok && item_at(k, it); ++k) {
             bool w = true;
             if (kside && lane == 0) {
-                if (g > 0) w = mbar_wait_bounded(&s_full[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), p.err);
+                if (g > 0) w = mbar_wait_bounded(&kfree[(g - 1) & 1], (uint32_t)(((g - 1) >> 1) & 1), p.err);
                 if (w) {
                     mbar_arrive_expect_tx(q_full, (uint32_t)Lay::Q_BYTES);
 #pragma unroll
@@ -236,19 +240,20 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 mbar_wait_bounded(&full[i & 1], (uint32_t)((i >> 1) & 1), p.err);
         }
     } else if (warp == TC_MMA_WARP) {
-        // ---- MMAs (lane 0 issues): per item S(g0), S(g0+1), then per step
-        // PV(g) and, once PV(g) is done, S(g+2).  Waiting for every PV keeps
-        // each pv_done barrier at most one phase ahead of its waiters.
+        // ---- MMAs (lane 0 issues).  Per step g: S(g+1) as soon as the
+        // softmax has read S(g) (one S buffer), then PV(g) once P(g) is
+        // written (P alternates between two buffers, so PV(g) never waits for
+        // an earlier MMA).  This thread waits on no MMA's completion.
         long long g0 = 0;
         bool mok = true;
         Item it;
-        // S of step g into TMEM buffer g % 2, K from stage g % 2
         // Descriptors of the operands' bases; an offset of a multiple of 16
         // bytes inside shared memory adds offset / 16 to the start-address
         // field (addresses stay below 2^18, so the field does not overflow).
         const uint64_t dq = tc5_desc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dk0 = tc5_desc_sw128(smem_u32(sK), 16, 1024), dk1 = dk0 + (KVB >> 4);
         const uint64_t dv0 = tc5_desc_sw128(smem_u32(sV), TC_KEYS * 128, 1024), dv1 = dv0 + (KVB >> 4);
+        // S of step g into the S buffer, K from stage g % 2
         auto issue_s = [&](long long g) -> bool {
             const int b = (int)(g & 1);
             if (!mbar_wait_bounded(&kfull[b], (uint32_t)((g >> 1) & 1), p.err)) return false;
@@ -258,39 +263,50 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                 // 16 elements = 32 bytes along K inside a 128-byte row; 64 per row group
                 const uint32_t qo = (uint32_t)(((ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32) >> 4);
                 const uint32_t ko = (uint32_t)(((ks >> 2) * (TC_KEYS * 128) + (ks & 3) * 32) >> 4);
-                tc5_mma(tmem + 64 * b, dq + qo, kb + ko, ID_S, ks > 0);
+                tc5_mma(tS, dq + qo, kb + ko, ID_S, ks > 0);
             }
-            tc5_commit(&s_full[b]);
+            tc5_commit(s_full);
+            tc5_commit(&kfree[b]);
             return true;
         };
         for (int k = 0; mok && item_at(k, it); ++k) {
             const int n = it.nsteps;
             bool w = true;
             if (lane == 0) {
+                // the item's first S: its Q has landed and the softmax has read the last S
                 w = mbar_wait_bounded(q_full, (uint32_t)(k & 1), p.err);
-                for (int c = 0; w && c < min(2, n); ++c) w = issue_s(g0 + c);
+                if (w && g0 > 0) w = mbar_wait_bounded(s_free, (uint32_t)((g0 - 1) & 1), p.err);
+                if (w) {
+                    tc5_fence_after_sync();
+                    w = issue_s(g0);
+                }
                 for (int c = 0; w && c < n; ++c) {
                     const long long g = g0 + c;
                     const int b = (int)(g & 1);
                     const uint32_t ph = (uint32_t)((g >> 1) & 1);
+                    if (c + 1 < n) {
+                        w = mbar_wait_bounded(s_free, (uint32_t)(g & 1), p.err);
+                        if (!w) break;
+                        tc5_fence_after_sync();
+                        w = issue_s(g + 1);
+                        if (!w) break;
+                    }
                     w = mbar_wait_bounded(&p_full[b], ph, p.err) && mbar_wait_bounded(&vfull[b], ph, p.err);
                     if (!w) break;
                     tc5_fence_after_sync();
                     const uint64_t vb = b ? dv1 : dv0;
 #pragma unroll
                     for (int ks = 0; ks < TC_KEYS / 16; ++ks)      // 16 keys = 2048 bytes
-                        tc5_mma_ta(tO, tmem + 64 * b + 8 * ks, vb + (uint32_t)(ks * 2048 >> 4), ID_O,
+                        tc5_mma_ta(tO, tP + 32 * b + 8 * ks, vb + (uint32_t)(ks * 2048 >> 4), ID_O,
                                    (c > 0 || ks > 0) ? 1u : 0u);
                     tc5_commit(&pv_done[b]);
-                    w = mbar_wait_bounded(&pv_done[b], ph, p.err);   // P of buffer b read
-                    if (w && c + 2 < n) w = issue_s(g + 2);
                 }
             }
             mok = __shfl_sync(0xffffffffu, w, 0);
             g0 += n;
         }
-        // after a timeout, MMAs may still be running: wait for them
-        if (lane == 0 && !mok) {
+        // MMAs may still be running (after a timeout): wait for them
+        if (lane == 0) {
             tc5_commit(mma_idle);
             mbar_wait_bounded(mma_idle, 0, p.err);
         }
@@ -313,14 +329,17 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             for (int c = 0; c < n; ++c, ++g) {
                 const int b = (int)(g & 1);
                 const uint32_t ph = (uint32_t)((g >> 1) & 1);
-                const uint32_t tS = tmem + 64 * b + lane_base;
-                const bool got = mbar_wait_bounded(&s_full[b], ph, p.err);
+                const bool got = mbar_wait_bounded(s_full, (uint32_t)(g & 1), p.err);
                 if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
                 tc5_fence_after_sync();
 
-                // -- this row's 64 scores; the causal mask only where some row needs it
+                // -- this row's 64 scores (then the S buffer is free for the
+                // next step's S); the causal mask only where some row needs it
                 float sv[TC_KEYS];
-                tc5_ld64u(tS, *reinterpret_cast<uint32_t(*)[TC_KEYS]>(&sv[0]));
+                tc5_ld64u(tS + lane_base, *reinterpret_cast<uint32_t(*)[TC_KEYS]>(&sv[0]));
+                tc5_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
                 const int nvis = lim - c * TC_KEYS + 1;      // positions of this step the row sees
                 if (__any_sync(0xffffffffu, nvis < TC_KEYS)) {
 #pragma unroll
@@ -371,8 +390,13 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                         tc5_st32(tO + lane_base + c0, o);
                     }
                 }
-                // P over the first 32 columns of the S buffer (waits for the store)
-                tc5_st32u(tS, pw);
+                // P into buffer b once P.V(g-2) has read it (waits for the store)
+                if (g >= 2) {
+                    const bool freed = mbar_wait_bounded(&pv_done[b], (uint32_t)(((g >> 1) - 1) & 1), p.err);
+                    if (!__all_sync(0xffffffffu, freed)) { ok = false; break; }
+                    tc5_fence_after_sync();
+                }
+                tc5_st32u(tP + 32 * b + lane_base, pw);
                 // V rows of the sequence's last block past L hold other tokens' data
                 // (zero-weighted, but 0 * NaN is NaN): clear them once V has landed
                 const int tail = it.L & 15, bl = it.nb_seq - 1 - (TC_KEYS / 16) * c;
