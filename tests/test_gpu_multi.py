@@ -267,6 +267,24 @@ def test_multi_prefill_more_than_256_sequences(cuda_lib):
     assert_close(out[torch.from_numpy(rows).cuda()], ref, "300 seqs")
 
 
+@pytest.mark.parametrize("dtype,D,G,Hkv", [("bf16", 128, 4, 8), ("f16", 64, 2, 4)],
+                         ids=["bf16-d128-g4", "f16-d64-g2"])
+def test_multi_prefill_many_items_per_block(cuda_lib, dtype, D, G, Hkv):
+    """More 128-row items than the persistent grid has blocks (two per SM), so
+    every block runs several items in turn and the hand-over between items
+    (the next item's Q, the step-indexed TMEM and shared-memory buffers) is
+    exercised; lengths differ so that items of one block differ in steps."""
+    rng = np.random.default_rng(690 + G)
+    nseq = 48
+    n = rng.integers(64 // G * 2, 64 // G * 5, size=nseq)     # 2..5 row groups of 64 rows
+    b = wl.multi_query_batch(690 + D, num_seqs=nseq, min_ctx=0, max_ctx=300, n_new=n,
+                             num_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, dtype=dtype,
+                             device="cuda", keep_seq=False)
+    items = int(sum((int(x) * G + 127) // 128 for x in n)) * Hkv
+    assert items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), f"{dtype} d{D} g{G} {items} items")
+
+
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled sequences against the oracle
 # ---------------------------------------------------------------------------
