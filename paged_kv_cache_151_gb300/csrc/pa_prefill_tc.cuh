@@ -118,6 +118,10 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int Hkv = p.num_kv_heads, H = p.num_heads;
 
+    // the decode kernel launched after this one (the rows of the short runs)
+    // may set up on SMs this grid leaves; it waits for this grid before it
+    // touches the caches or out
+    launch_dependents();
     if (tid == 0) {
         prefetch_tensormap(&p.tmap_k);
         prefetch_tensormap(&p.tmap_v);
