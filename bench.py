@@ -307,6 +307,7 @@ def gpu_arm(args, rank, world, device):
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = e2e_arm(args, b, device, flush, pa)
+    probe = read_probe(device) if world == 1 else None
 
     result = {
         "metric": METRIC,
@@ -346,6 +347,8 @@ def gpu_arm(args, rank, world, device):
             "unit": "GB/s",
             "frac": achieved / peak,
             "frac_of_nominal_8tbs": achieved / 8000.0,
+            "read_probe_gbs": probe["gbs"] if probe else None,
+            "frac_of_read_probe": achieved / probe["gbs"] if probe else None,
             "traffic": recorded_traffic("decode_serving_mix"),
         },
         "e2e": e2e,
@@ -363,7 +366,71 @@ def gpu_arm(args, rank, world, device):
         result["fp8"] = fp8_arm(args, device, flush, pa)
         result["copy_blocks"] = copy_blocks_arm(args, device, flush, pa)
         result["block_manager"] = block_manager_arm(args)
+        result["read_probe"] = probe
+        result["launch_to_launch"] = launch_to_launch_arm(step)
     return result, b
+
+
+def read_probe(device, gib: float = 2.0) -> dict:
+    """Read-only bandwidth probe: a float32 sum over a buffer far larger than
+    L2, best of 10 (the copy peak in MEASURED_PEAKS.json counts a read and a
+    write; decode mostly reads)."""
+    n = int(gib * (1 << 30)) // 4
+    x = torch.ones(n, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        torch.sum(x, dim=0, out=sink)
+    best = None
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        torch.sum(x, dim=0, out=sink)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    gbs = n * 4 / (best * 1e-3) / 1e9
+    del x
+    return {"gbs": gbs, "bytes": n * 4, "how": "torch.sum over a float32 buffer, best of 10"}
+
+
+def launch_to_launch_arm(step, n: int = 50) -> dict:
+    """The serving-mix step (cache write + decode) run n times back to back
+    without L2 flushes: eagerly, each call going through the binding and the
+    C ABI, and replayed from a CUDA graph captured from one step."""
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n * 1e3
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    res = {"steps": n, "l2": "not flushed (steps back to back)", "eager_us_per_step": timed(step)}
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        res["graph_us_per_step"] = timed(g.replay)
+    except Exception as exc:                      # reported, not fatal
+        res["graph_us_per_step"] = None
+        res["graph_error"] = str(exc).splitlines()[0][:200]
+    return res
 
 
 def e2e_arm(args, b, device, flush, pa):
