@@ -361,6 +361,7 @@ def gpu_arm(args, rank, world, device):
     }
     if not args.no_extras and world == 1:
         result["long_context"] = long_context_arm(args, device, flush, pa)
+        result["shared_prefix"] = shared_prefix_arm(args, device, flush, pa)
         result["paging_overhead"] = paging_overhead_arm(args, device, flush, pa)
         result["multi_query"] = multi_query_arm(args, device, flush, pa)
         result["fp8"] = fp8_arm(args, device, flush, pa)
@@ -496,6 +497,37 @@ def long_context_arm(args, device, flush, pa):
             "seqs_per_s": 8 / t, "us_per_call": t * 1e6, "kv_gbs": nb["kv"] / t / 1e9,
             "achieved_gbs": nb["total"] / t / 1e9, "frac_of_peak": nb["total"] / t / 1e9 / peak,
             "peak_kind": kind, "bytes": nb}
+
+
+def shared_prefix_arm(args, device, flush, pa):
+    """pa_decode on the shared-prefix batch: 128 seqs whose tables start with
+    the same 128 physical blocks (a 2048-token prefix), then 64..512 private
+    tokens.  Logical bytes count every sequence's prefix; unique bytes count
+    the prefix blocks once (the rest of a sequence's reads of them can hit
+    L2).  No roofline gate: the logical rate may exceed HBM."""
+    b = wl.shared_prefix(device=device, canary=False)
+    bt, sl, _ = b.torch_tables(device)
+    out = torch.empty_like(b.q)
+
+    def call():
+        pa.pa_decode(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale, b.num_kv_heads)
+    for _ in range(3):
+        call()
+    ms = time_calls(call, 30, flush, torch.cuda.current_stream())
+    nb = decode_bytes(b)
+    es = 2
+    per_tok = 2 * b.num_kv_heads * b.head_dim * es
+    prefix = int(b.meta["prefix_tokens"])
+    unique = nb["total"] - (b.num_seqs - 1) * prefix * per_tok
+    t = statistics.median(ms) * 1e-3
+    peak, kind = measured_peak()
+    del b
+    torch.cuda.empty_cache()
+    return {"workload": "shared_prefix: batch 128, 32/8 x 128 bf16, a 2048-token prefix in 128 "
+                        "shared physical blocks + U[64,512] private tokens",
+            "us_per_call": t * 1e6, "logical_gbs": nb["total"] / t / 1e9,
+            "unique_gbs": unique / t / 1e9, "unique_frac_of_peak": unique / t / 1e9 / peak,
+            "peak_kind": kind, "bytes": {"logical": nb["total"], "unique": unique}}
 
 
 def multi_query_arm(args, device, flush, pa):
