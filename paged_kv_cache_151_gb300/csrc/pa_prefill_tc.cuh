@@ -14,17 +14,16 @@
 //   1. S = Q K^T: tcgen05.mma, M = 128, N = 64, K = head_dim, both operands
 //      K-major in shared memory (128-byte swizzle): Q by one tensor-map copy
 //      per item, the four K blocks of the step by tensor-map copies stacked
-//      into one 64-row operand.  S lands in one of two TMEM buffers (step g
-//      in buffer g % 2), so S of the next step runs under the softmax of this
-//      one.
+//      into one 64-row operand.  S lands in the block's S buffer in TMEM.
 //   2. Each softmax thread owns one row (TMEM lane = row): it reads its 64
-//      scores (tcgen05.ld), masks positions past its causal limit (only on
-//      the steps that reach past some row's limit), updates the online
-//      softmax in fp32 (lazy rescaling, as in the warp-level paths; two
-//      lanes per instruction where the arithmetic allows), rescales its row
-//      of O in TMEM when its reference level moved, and writes its
-//      probabilities, rounded to the cache type, over the first 32 columns
-//      of the step's S buffer (two per column).
+//      scores (tcgen05.ld) -- after which S of the next step may overwrite
+//      the buffer -- masks positions past its causal limit (only on the
+//      steps that reach past some row's limit), updates the online softmax
+//      in fp32 (lazy rescaling, as in the warp-level paths; two lanes per
+//      instruction where the arithmetic allows), rescales its row of O in
+//      TMEM when its reference level moved, and writes its probabilities,
+//      rounded to the cache type, into the step's P buffer (two per column;
+//      even and odd steps alternate between two buffers).
 //   3. O += P V: tcgen05.mma, M = 128, N = head_dim, K = 64, P read from TMEM,
 //      V from shared memory MN-major (rows = keys, head_dim contiguous).  O
 //      accumulates in TMEM over the whole item and is read back, normalised,
@@ -32,14 +31,16 @@
 // Roles: warps 0-3 run the softmax (warp w reaches TMEM lanes 32w..32w+31);
 // warps 4 and 6 keep the copies going -- Q once per item and a ring of two K
 // stages (warp 4; a K stage is free once its S is done), a ring of two V
-// stages (warp 6; free once its P.V is done); warp 5 (lane 0) issues the MMAs in the order S(0), S(1),
-// PV(0), S(2), PV(1), ... and reports their completion through
-// tcgen05.commit on mbarriers.  S(g + 2) overwrites the buffer PV(g) reads
-// its P from, so it is issued once PV(g) is complete.  Two blocks share an
-// SM (about 100 KB of shared memory and 256 TMEM columns each).  The grid is
-// persistent; block b takes the items b, 2R-1-b, 2R+b, ... of the sorted
-// list (R blocks), which deals the long items out first.  Every wait is
-// bounded; on a timeout the block stops and the error word says so.
+// stages (warp 6; free once its P.V is done); warp 5 (lane 0) issues the
+// MMAs in the order S(0), S(1), PV(0), S(2), PV(1), ...: S(g+1) once the
+// softmax has read S(g), PV(g) once P(g) is written.  Completion comes back
+// through tcgen05.commit on mbarriers; the MMA thread itself waits on no
+// MMA (the softmax waits for PV(g-2) before reusing its P buffer, the copy
+// warps for S(g-2) and PV(g-2) before reusing a stage).  Two blocks share
+// an SM (about 104 KB of shared memory and 256 TMEM columns each).  The
+// grid is persistent; block b takes the items b, 2R-1-b, 2R+b, ... of the
+// sorted list (R blocks), which deals the long items out first.  Every wait
+// is bounded; on a timeout the block stops and the error word says so.
 #pragma once
 
 #include <climits>
