@@ -499,6 +499,16 @@ def long_context_arm(args, device, flush, pa):
             "peak_kind": kind, "bytes": nb}
 
 
+def shared_prefix_unique_bytes(b) -> int:
+    """decode_bytes' total with the shared prefix's K/V counted once instead
+    of once per sequence (every sequence's table starts with the same
+    prefix_tokens / 16 physical blocks)."""
+    es = torch.tensor([], dtype=wl.DTYPES[b.dtype]).element_size()
+    per_tok = 2 * b.num_kv_heads * b.head_dim * es
+    prefix = int(b.meta["prefix_tokens"])
+    return decode_bytes(b)["total"] - (b.num_seqs - 1) * prefix * per_tok
+
+
 def shared_prefix_arm(args, device, flush, pa):
     """pa_decode on the shared-prefix batch: 128 seqs whose tables start with
     the same 128 physical blocks (a 2048-token prefix), then 64..512 private
@@ -515,10 +525,7 @@ def shared_prefix_arm(args, device, flush, pa):
         call()
     ms = time_calls(call, 30, flush, torch.cuda.current_stream())
     nb = decode_bytes(b)
-    es = 2
-    per_tok = 2 * b.num_kv_heads * b.head_dim * es
-    prefix = int(b.meta["prefix_tokens"])
-    unique = nb["total"] - (b.num_seqs - 1) * prefix * per_tok
+    unique = shared_prefix_unique_bytes(b)
     t = statistics.median(ms) * 1e-3
     peak, kind = measured_peak()
     del b

@@ -46,3 +46,26 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.aggregate_rate(1, 256, 4, 2.0) == pytest.approx(256 * 4 / 2e-3)
+
+
+def test_shared_prefix_unique_bytes_counts_each_tile_once():
+    """The shared-prefix line's unique bytes equal decode_bytes' total minus
+    the K/V of every repeated (physical block, row) that the tables name
+    more than once: counted here directly from the block tables."""
+    import numpy as np
+
+    import bench
+    from paged_kv_cache_151_gb300 import workloads as wl
+
+    b = wl.shared_prefix(batch=12, prefix_blocks=8, lo=5, hi=40, canary=False)
+    total = bench.decode_bytes(b)["total"]
+    per_tok = 2 * b.num_kv_heads * b.head_dim * 2
+    seen, repeats = set(), 0
+    for s in range(b.num_seqs):
+        for t in range(int(b.seq_lens[s])):
+            key = (int(b.block_tables[s, t // 16]), t % 16)
+            repeats += key in seen
+            seen.add(key)
+    assert repeats == (b.num_seqs - 1) * int(b.meta["prefix_tokens"])
+    assert bench.shared_prefix_unique_bytes(b) == total - repeats * per_tok
+    assert np.all(b.block_tables[:, :8] == b.block_tables[0, :8])
