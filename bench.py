@@ -841,7 +841,14 @@ def single_kernel(args, device):
     torch.cuda.set_device(device)
     pa.load()
     flush, _ = make_flush(device)
-    if args.only == "partitioned":
+    if args.only == "shared_prefix":
+        b = wl.shared_prefix(device=device, canary=False)
+        bt, sl, _ = b.torch_tables(device)
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale, b.num_kv_heads)
+    elif args.only == "partitioned":
         b = wl.long_context(device=device, canary=False)
         bt, sl, _ = b.torch_tables(device)
         msl = 131072
@@ -931,9 +938,9 @@ def main():
                     help="skip the long-context, paging-overhead, multi-query, FP8 and "
                          "copy-on-write measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["decode", "partitioned", "cache_write", "multi_spec",
-                                       "multi_prefill", "decode_fp8", "cache_write_fp8",
-                                       "partitioned_fp8", "copy_blocks"],
+    ap.add_argument("--only", choices=["decode", "shared_prefix", "partitioned", "cache_write",
+                                       "multi_spec", "multi_prefill", "decode_fp8",
+                                       "cache_write_fp8", "partitioned_fp8", "copy_blocks"],
                     help="launch one kernel alone (for profiling); prints timings only")
     args = ap.parse_args()
     if args.warmup < 3:
