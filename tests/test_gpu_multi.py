@@ -209,6 +209,19 @@ def test_multi_prefill_path_parity(cuda_lib, dtype, D, G, Hkv):
     assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), f"{dtype} d{D} g{G}")
 
 
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64)])
+def test_multi_prefill_fewer_rows_than_one_q_box(cuda_lib, dtype, D):
+    """Multi-head attention (G = 1) with one 100-token chunk and two short
+    runs: 103 query rows in all, fewer than the 128 tokens one Q copy of the
+    prefill kernel spans; rows past the end of q are filled with zeros, never
+    read."""
+    b = wl.multi_query_batch(645 + D, num_seqs=3, min_ctx=10, max_ctx=120, n_new=[100, 1, 2],
+                             num_heads=4, num_kv_heads=4, head_dim=D, dtype=dtype, device="cuda",
+                             keep_seq=False)
+    assert b.meta["query_start"][-1] == 103
+    assert_close(gpu_multi(cuda_lib, b), oracle_multi(b), f"{dtype} d{D} 103 rows")
+
+
 def test_multi_prefill_whole_prompt(cuda_lib):
     """A first chunk of 300 tokens with nothing cached: row i sees 0..i, the
     first row exactly its own V."""
