@@ -207,6 +207,10 @@ size_t pa_decode_partitioned_workspace_size(int32_t num_seqs,
  * Requirements as pa_decode, plus partition_size a positive multiple of 16
  * and workspace_bytes >= pa_decode_partitioned_workspace_size(...); the
  * workspace must be 256-byte aligned.
+ *
+ * If pa_device_error reports PA_DEVERR_TIMEOUT after a call, that call's
+ * output is undefined: a partition whose bounded wait ran out is not written,
+ * and the merge then reads whatever the workspace held before the call.
  */
 int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
                           const void *v_cache, const int32_t *block_tables,
@@ -371,13 +375,21 @@ int pa_decode_partitioned_fp8(void *out, const void *q, const void *k_cache,
  * with PA_ERR_WORKSPACE before anything is launched.  Nothing is allocated
  * or freed (no cudaMalloc, cudaFree or allocating library routine).
  *
+ * The arguments are checked in the same order, and bad ones refused with
+ * the same status, as by pa_decode_partitioned.
+ *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
- * capture.  All calls on a device share the one array, which keeps whatever
- * the last call left in it (every entry a call reads is first written by the
- * same call, so nothing needs clearing): calls whose kernels may overlap on
- * the GPU -- on different streams, or from several host threads -- race on
- * it and must be serialised by the caller.
+ * capture.  The cached address belongs to the CUDA context it was looked up
+ * in: after cudaDeviceReset (or anything else that destroys the device's
+ * primary context) it is stale, and this entry point must not be called
+ * again on that device in the same process.  All calls on a device share the
+ * one array, which keeps whatever the last call left in it.  Every entry a
+ * call reads is first written by the same call, so nothing needs clearing --
+ * except after PA_DEVERR_TIMEOUT, when the output is undefined and may mix in
+ * an earlier call's partials (see pa_decode_partitioned).  Calls whose
+ * kernels may overlap on the GPU -- on different streams, or from several
+ * host threads -- race on the array and must be serialised by the caller.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
 

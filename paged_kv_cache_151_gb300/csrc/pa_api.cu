@@ -264,11 +264,19 @@ bool workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
         partition_size <= 0 || partition_size % 16)
         return false;
     const size_t P = (size_t)((max_seq_len + (int64_t)partition_size - 1) / partition_size);
-    const size_t rows = (size_t)num_seqs * num_heads * (P > 0 ? P : 1);
+    // Every product and sum is checked: the arguments allow about 2^71 bytes,
+    // and a wrapped size would pass the workspace checks.
+    size_t rows = 0, o_bytes = 0, ml_bytes = 0;
+    if (__builtin_mul_overflow((size_t)num_seqs, (size_t)num_heads, &rows) ||
+        __builtin_mul_overflow(rows, P > 0 ? P : (size_t)1, &rows) ||
+        __builtin_mul_overflow(rows, (size_t)head_dim * sizeof(float), &o_bytes) ||
+        __builtin_mul_overflow(rows, sizeof(float), &ml_bytes) ||
+        o_bytes > (SIZE_MAX >> 2) || ml_bytes > (SIZE_MAX >> 2))
+        return false;
     w->o = 0;
-    w->m = align_up(rows * head_dim * sizeof(float));
-    w->l = w->m + align_up(rows * sizeof(float));
-    w->total = w->l + align_up(rows * sizeof(float));
+    w->m = align_up(o_bytes);
+    w->l = w->m + align_up(ml_bytes);
+    w->total = w->l + align_up(ml_bytes);
     return true;
 }
 
@@ -686,6 +694,14 @@ extern "C" int pa_decode_partitioned_noalloc(
     int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
     int32_t block_size, int32_t max_blocks_per_seq, int64_t q_seq_stride, float scale,
     int32_t dtype, int32_t partition_size, int32_t max_seq_len, void *stream) {
+    // The same checks, in the same order, as pa_decode_partitioned, so that
+    // both calls give the same status for the same bad input.
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_seq_stride, scale, dtype);
+    if (rc != PA_OK) return rc;
+    if (partition_size <= 0 || partition_size % 16 || max_seq_len < 0)
+        return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     const size_t need = pa_decode_partitioned_workspace_size(num_seqs, num_heads, head_dim,
                                                              max_seq_len, partition_size);

@@ -36,6 +36,7 @@
 // aliasing.
 #pragma once
 
+#include <atomic>
 #include <type_traits>
 
 #include "pa_common.cuh"
@@ -1054,12 +1055,14 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
         return cudaSuccess;
     }
     if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1))) return cudaErrorInvalidValue;
-    static int fitted[64][5];                      // clusters resident per device, per size
+    // clusters resident per device, per size; written once per (device, size)
+    // after the attributes are set, read by any host thread
+    static std::atomic<int> fitted[64][5];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int ci = cluster == 1 ? 0 : cluster == 2 ? 1 : cluster == 4 ? 2 : cluster == 8 ? 3 : 4;
-    int nc = (dev >= 0 && dev < 64) ? fitted[dev][ci] : 0;
+    int nc = (dev >= 0 && dev < 64) ? fitted[dev][ci].load(std::memory_order_acquire) : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(C::NW * 32, 1, 1);
@@ -1087,7 +1090,7 @@ cudaError_t launch_persistent(const DecodeParams &p, long long unit_bound, int c
         e = cudaOccupancyMaxActiveClusters(&nc, kern, &cfg);
         if (e != cudaSuccess) return e;
         if (nc < 1) nc = 1;
-        if (dev >= 0 && dev < 64) fitted[dev][ci] = nc;
+        if (dev >= 0 && dev < 64) fitted[dev][ci].store(nc, std::memory_order_release);
     }
     long long NC = nc;
     const long long need = (unit_bound + C::Lay::NU_MAX - 1) / C::Lay::NU_MAX;

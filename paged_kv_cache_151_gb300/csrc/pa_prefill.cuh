@@ -23,6 +23,8 @@
 // blocks that finish early.
 #pragma once
 
+#include <atomic>
+
 #include "pa_common.cuh"
 #include "pa_decode.cuh"
 #include "pa_internal.h"
@@ -309,14 +311,14 @@ cudaError_t launch_prefill(const DecodeParams &p, int groups, cudaStream_t st) {
     constexpr size_t smem = Lay::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory");
     auto kern = prefill_kernel<T, D, G, PREFILL_NWC, S>;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];    // per device, read by any host thread
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
     }
     // One block per item.  The items are at most the worst case (every
     // sequence with `groups` row groups), and at most 2 * ceil(rows / 64) row

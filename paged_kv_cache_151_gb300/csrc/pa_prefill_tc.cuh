@@ -43,6 +43,7 @@
 // is bounded; on a timeout the block stops and the error word says so.
 #pragma once
 
+#include <atomic>
 #include <climits>
 
 #include "pa_common.cuh"
@@ -466,14 +467,14 @@ cudaError_t launch_prefill_tc(const DecodeParams &p, const CUtensorMap &tmap_q, 
     static_assert(TC_BLOCKS_PER_SM * (smem + sizeof(PrefillSched) + 1024) <= 228 * 1024,
                   "two blocks per SM");
     auto kern = prefill_tc_kernel<T, D, G>;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];    // per device, read by any host thread
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_release);
     }
     // persistent: the resident blocks (two per SM), but no more than the items
     // can be: the worst case, and at most 2 * ceil(rows / 64) items per KV head

@@ -173,3 +173,55 @@ def test_copy_blocks_host_checks(lib):
     assert lib.pa_copy_blocks(arr, 3, None, 5, 10, 4096, None) == -1     # no mapping
     bad = (ctypes.c_void_p * 2)(16, 24)                                  # unaligned cache
     assert lib.pa_copy_blocks(bad, 2, 16, 5, 10, 4096, None) == -1
+
+
+def _partitioned_status(lib, noalloc, **kw):
+    """Status of pa_decode_partitioned (with a workspace of `ws_bytes`) or of
+    pa_decode_partitioned_noalloc for the same arguments."""
+    a = dict(out=16, q=16, k_cache=16, v_cache=16, block_tables=16, seq_lens=16,
+             num_seqs=4, num_heads=8, num_kv_heads=2, head_dim=64, num_blocks=10,
+             block_size=16, max_blocks=4, q_seq_stride=512, scale=0.125, dtype=1,
+             partition_size=512, max_seq_len=64, ws_bytes=1 << 30)
+    a.update(kw)
+    head = [a["out"], a["q"], a["k_cache"], a["v_cache"], a["block_tables"], a["seq_lens"],
+            a["num_seqs"], a["num_heads"], a["num_kv_heads"], a["head_dim"], a["num_blocks"],
+            a["block_size"], a["max_blocks"], a["q_seq_stride"], a["scale"], a["dtype"],
+            a["partition_size"], a["max_seq_len"]]
+    if noalloc:
+        return lib.pa_decode_partitioned_noalloc(*head, None)
+    return lib.pa_decode_partitioned(*head, ctypes.c_void_p(256), a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(num_seqs=0, partition_size=7),            # nothing to do, but a bad partition
+    dict(num_seqs=0, num_heads=0),                 # nothing to do, but no heads
+    dict(num_seqs=0, max_seq_len=-1),
+    dict(out=None),
+    dict(head_dim=96),
+    dict(partition_size=100),
+    dict(num_heads=7),
+    dict(out=None, max_seq_len=1 << 24),           # null pointers on a huge problem
+    dict(num_seqs=0),                              # valid and empty: PA_OK from both
+])
+def test_noalloc_refuses_bad_arguments_like_the_workspace_call(lib, bad):
+    """Both split-KV entry points check their arguments in the same order, so
+    a bad input gets the same status from each; none of these reaches a GPU."""
+    assert (_partitioned_status(lib, True, **bad) ==
+            _partitioned_status(lib, False, **bad))
+
+
+def test_workspace_size_overflow_is_refused(lib):
+    """num_seqs * num_heads * partitions * head_dim * 4 past 2^64 gives 0
+    (invalid), not a wrapped size that a workspace check could accept."""
+    assert pa.pa_decode_partitioned_workspace_size(65535, 8 * 65535, 128, 2**31 - 1, 16) == 0
+    rows = 65535 * 8 * (2**27)                     # large, but no product overflows
+    up = lambda x: (x + 255) // 256 * 256
+    assert (pa.pa_decode_partitioned_workspace_size(65535, 8, 128, 2**31 - 1, 16) ==
+            up(rows * 128 * 4) + 2 * up(rows * 4))
+
+
+def test_noalloc_limit_matches_the_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+PA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "PA_NOALLOC_SCRATCH_BYTES not found in include/pa.h"
+    assert pa.PA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
