@@ -3,9 +3,11 @@ import sys
 
 import pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+for _p in (ROOT, HERE):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
 
 
 def pytest_configure(config):
@@ -22,3 +24,18 @@ def cuda_lib():
     from paged_kv_cache_151_gb300 import pa
     pa.load()
     return pa
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the whole-output parity figures of the full-size workloads."""
+    try:
+        import fullsize
+    except ImportError:
+        return
+    if not fullsize.RESULTS:
+        return
+    tr = terminalreporter
+    tr.section("full-size parity against the fp64 oracle (every output element)")
+    for name, n, err, rel, secs in fullsize.RESULTS:
+        tr.write_line(f"{name:<48} {n:>10} elements  max|err| {err:.3e}  "
+                      f"rel L2 {rel:.3e}  oracle {secs:6.1f} s")

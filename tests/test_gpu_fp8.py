@@ -6,13 +6,13 @@ held to the 16-bit tolerance: the codes convert exactly, so the arithmetic
 error is that of the bf16/f16 path -- max |err| <= 2e-2 and relative L2 error
 <= 5e-3 against the oracle's fp64 attention over the dequantised values.
 """
-import dataclasses
 import math
 
 import numpy as np
 import pytest
 import torch
 
+import fullsize
 import oracle
 from paged_kv_cache_151_gb300 import workloads as wl
 
@@ -244,26 +244,8 @@ def test_decode_fp8_batch_larger_than_one_sort(cuda_lib):
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, sampled (sequence, head) outputs
+# full-size workloads: every output element against the oracle (fullsize.py)
 # ---------------------------------------------------------------------------
-
-def sampled_fp8(b, out, n_samples, seed):
-    rng = np.random.default_rng(seed)
-    ks, vs = scales(b)
-    pr = oracle.problem(b.q.cpu(), b.k_cache.cpu(), b.v_cache.cpu(), b.block_tables,
-                        b.seq_lens, b.scale, b.num_kv_heads, b.dtype,
-                        kv_scales=(ks.cpu(), vs.cpu()))
-    seqs = list(rng.integers(0, b.num_seqs, size=n_samples - 2))
-    seqs += [int(np.argmax(b.seq_lens)), int(np.argmin(b.seq_lens))]
-    got, ref = [], []
-    for s in seqs:
-        h = int(rng.integers(0, b.num_heads))
-        r, _ = oracle.decode_one(s, h, None, None, None, None, None, None, None, b.dtype,
-                                 problem=pr)
-        ref.append(r)
-        got.append(out[s, h].double().cpu().numpy())
-    assert_close(np.stack(got), np.stack(ref), b.name)
-
 
 @pytest.mark.slow
 def test_full_serving_mix_fp8_step(cuda_lib):
@@ -273,17 +255,21 @@ def test_full_serving_mix_fp8_step(cuda_lib):
     kc, vc = b.k_cache.clone(), b.v_cache.clone()
     cuda_lib.pa_reshape_and_cache_fp8(b.k_new, b.v_new, kc, vc, ks, vs, sm)
     out = gpu_decode_fp8(cuda_lib, b, k_cache=kc, v_cache=vc)
-    # the write, checked on the written rows (quotients in binary32)
-    slots = torch.from_numpy(b.slot_mapping).cuda()
-    written = kc[slots // 16, :, slots % 16, :].cpu().numpy()
-    want = oracle.e4m3_encode((b.k_new.float() / ks.view(1, -1, 1)).cpu().numpy())
-    assert np.array_equal(written, want)
-    b2 = dataclasses.replace(b, k_cache=kc, v_cache=vc)
-    sampled_fp8(b2, out, 48, 2)
+    # the write: bit-exact on the whole pool (quotients in binary32)
+    rk, rv, bad = oracle.reshape_and_cache_fp8(b.k_new.cpu(), b.v_new.cpu(), b.k_cache.cpu(),
+                                               b.v_cache.cpu(), b.slot_mapping, b.dtype,
+                                               ks.cpu(), vs.cpu())
+    assert bad == 0
+    assert np.array_equal(kc.cpu().numpy(), rk) and np.array_equal(vc.cpu().numpy(), rv)
+    ref, t = fullsize.decode_all(b, k_cache=kc, v_cache=vc, kv_scales=(ks, vs))
+    fullsize.check("serving_mix_fp8: cache write + pa_decode_fp8", out, ref, b.dtype, t)
 
 
 @pytest.mark.slow
 def test_full_long_context_fp8_partitioned(cuda_lib):
     b = wl.long_context_fp8(device="cuda", canary=False)
     out = gpu_partitioned_fp8(cuda_lib, b, 512, max_seq_len=131072)
-    sampled_fp8(b, out, 10, 4)
+    ref, t = fullsize.decode_all(b, kv_scales=scales(b))
+    fullsize.check("long_context_fp8: pa_decode_partitioned_fp8", out, ref, b.dtype, t)
+    fullsize.check("long_context_fp8: pa_decode_fp8", gpu_decode_fp8(cuda_lib, b), ref,
+                   b.dtype)

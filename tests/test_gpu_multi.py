@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import fullsize
 import oracle
 from paged_kv_cache_151_gb300 import workloads as wl
 
@@ -299,31 +300,20 @@ def test_multi_prefill_many_items_per_block(cuda_lib, dtype, D, G, Hkv):
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, sampled sequences against the oracle
+# full-size workloads: every output element against the oracle (fullsize.py)
 # ---------------------------------------------------------------------------
-
-def sampled_multi(b, out, n_samples, seed):
-    rng = np.random.default_rng(seed)
-    seqs = sorted(set(rng.integers(0, b.num_seqs, size=n_samples - 1).tolist()) |
-                  {int(np.argmax(b.seq_lens))})
-    ref, rows = oracle_multi(b, seqs=np.array(seqs))
-    assert_close(out[torch.from_numpy(rows).cuda()], ref, b.name)
-
 
 @pytest.mark.slow
 def test_full_spec_verify(cuda_lib):
     b = wl.spec_verify(device="cuda")
     out = gpu_multi(cuda_lib, b)
-    assert not torch.isnan(out).any()
-    sampled_multi(b, out, 40, 1)
+    ref, t = fullsize.multi_all(b)
+    fullsize.check("spec_verify: pa_decode_multi (4 rows/seq)", out, ref, b.dtype, t)
 
 
 @pytest.mark.slow
 def test_full_chunked_prefill_mix(cuda_lib):
     b = wl.chunked_prefill_mix(device="cuda")
     out = gpu_multi(cuda_lib, b)
-    assert not torch.isnan(out).any()
-    # every prefill chunk, and a sample of the decodes
-    seqs = list(range(4)) + list(np.random.default_rng(2).integers(4, b.num_seqs, 12))
-    ref, rows = oracle_multi(b, seqs=np.array(sorted(set(int(s) for s in seqs))))
-    assert_close(out[torch.from_numpy(rows).cuda()], ref, b.name)
+    ref, t = fullsize.multi_all(b)
+    fullsize.check("chunked_prefill_mix: pa_decode_multi", out, ref, b.dtype, t)

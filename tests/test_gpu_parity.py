@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import fullsize
 import oracle
 from paged_kv_cache_151_gb300 import workloads as wl
 
@@ -325,31 +326,15 @@ def test_partitioned_seq_len_past_max_is_flagged(cuda_lib):
 
 # ---------------------------------------------------------------------------
 # full-size workloads, in the launch configuration the benchmark times;
-# sampled (sequence, head) outputs against the oracle one by one
+# every output element against the oracle (fullsize.py)
 # ---------------------------------------------------------------------------
-
-def sampled_check(b, out, n_samples, seed, dtype):
-    rng = np.random.default_rng(seed)
-    pr = oracle.problem(b.q.cpu(), b.k_cache.cpu(), b.v_cache.cpu(), b.block_tables,
-                        b.seq_lens, b.scale, b.num_kv_heads, dtype)
-    # always include the longest and the shortest sequence
-    seqs = list(rng.integers(0, b.num_seqs, size=n_samples - 2))
-    seqs += [int(np.argmax(b.seq_lens)), int(np.argmin(b.seq_lens))]
-    got, ref = [], []
-    for s in seqs:
-        h = int(rng.integers(0, b.num_heads))
-        r, _ = oracle.decode_one(s, h, None, None, None, None, None, None, None, dtype,
-                                 problem=pr)
-        ref.append(r)
-        got.append(out[s, h].double().cpu().numpy())
-    assert_close(np.stack(got), np.stack(ref), dtype, b.name)
-
 
 @pytest.mark.slow
 def test_full_llama8b_uniform(cuda_lib):
     b = wl.llama8b_uniform(device="cuda", new_in_pool=True)
     out = gpu_decode(cuda_lib, b)
-    sampled_check(b, out, 48, 1, "bf16")
+    ref, t = fullsize.decode_all(b)
+    fullsize.check("llama8b_uniform: pa_decode", out, ref, "bf16", t)
 
 
 @pytest.mark.slow
@@ -369,15 +354,19 @@ def test_full_serving_mix_step(cuda_lib):
     assert torch.equal(kc.view(torch.int16), ref_k.view(torch.int16))
     b2 = wl.serving_mix(device="cuda", new_in_pool=True)
     assert torch.equal(kc.view(torch.int16), b2.k_cache.view(torch.int16))
-    sampled_check(b2, out, 64, 2, "bf16")
+    assert torch.equal(vc.view(torch.int16), b2.v_cache.view(torch.int16))
+    ref, t = fullsize.decode_all(b2)
+    fullsize.check("serving_mix: cache write + pa_decode", out, ref, "bf16", t)
 
 
 @pytest.mark.slow
 def test_full_shared_prefix(cuda_lib):
     shared = wl.shared_prefix(device="cuda", new_in_pool=True)
     out = gpu_decode(cuda_lib, shared)
-    sampled_check(shared, out, 32, 3, "bf16")
     private = wl.shared_prefix(device="cuda", new_in_pool=True, private_prefix=True)
+    # the oracle on the private-copy layout: the aliased output must equal it
+    ref, t = fullsize.decode_all(private)
+    fullsize.check("shared_prefix: pa_decode (aliased tables)", out, ref, "bf16", t)
     assert torch.equal(out, gpu_decode(cuda_lib, private))
 
 
@@ -385,7 +374,9 @@ def test_full_shared_prefix(cuda_lib):
 def test_full_long_context_partitioned(cuda_lib):
     b = wl.long_context(device="cuda", new_in_pool=True)
     out, _, _ = gpu_partitioned(cuda_lib, b, 512, max_seq_len=131072)
-    sampled_check(b, out, 12, 4, "bf16")
+    ref, t = fullsize.decode_all(b)
+    fullsize.check("long_context: pa_decode_partitioned 512", out, ref, "bf16", t)
+    fullsize.check("long_context: pa_decode", gpu_decode(cuda_lib, b), ref, "bf16")
 
 
 def test_decode_sees_the_cache_write_it_follows(cuda_lib):
