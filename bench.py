@@ -130,6 +130,20 @@ def recorded_traffic(name: str):
         return None
 
 
+def bench_config(b, world: int) -> dict:
+    """The `config` of the bench line, the same for the GPU arm and the
+    reference arm (which runs the same workload on the host)."""
+    return {
+        "workload": WORKLOAD,
+        "global_batch": world * b.num_seqs,
+        "tokens_attended": int(b.seq_lens.sum()),
+        "num_blocks": int(b.num_blocks),
+        "l2": "GPU arm: flushed between steps (twice the L2 size written, then as much "
+              "read, outside the events); the 744 MB pool is larger than L2 anyway",
+        "parallelism": f"replicas x{world}" if world > 1 else "one replica",
+    }
+
+
 # ---------------------------------------------------------------------------
 # ranks: every rank runs its own replica; time = max over ranks
 # ---------------------------------------------------------------------------
@@ -322,16 +336,9 @@ def gpu_arm(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; no dataset)",
-        "config": {
-            "workload": WORKLOAD,
-            "global_batch": world * b.num_seqs,
-            "tokens_attended": int(b.seq_lens.sum()),
-            "num_blocks": b.num_blocks,
-            "l2": f"flushed between steps ({flush_bytes >> 20} MiB write, then "
-                  f"{flush_bytes >> 20} MiB read, outside the events)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "decode_kernel": "persistent (LPT-sorted units, per-warp bulk-copy rings)",
-        },
+        "config": bench_config(b, world),
+        "decode_kernel": "persistent (longest-first units, per-warp bulk-copy rings)",
+        "l2_flush_bytes": flush_bytes,
         "kv_gbs": nbytes["kv"] / (dec_mean * 1e-3) / 1e9,
         "decode_us": dec_mean * 1e3,
         "decode_us_median": statistics.median(dec_ms) * 1e3,
@@ -736,94 +743,74 @@ def paging_overhead_arm(args, device, flush, pa):
 # the oracle on the host cores (CPU baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(n_seqs: int):
-    """The first n_seqs sequences of the serving-mix batch (same seeded
-    lengths), built on the host, plus the full batch's total token count."""
-    rng = np.random.default_rng(3)
-    lens = wl.lognormal_lengths(rng, 256)
-    sel = lens[:n_seqs]
-    fl = wl.FreeList(int(sum(math.ceil(int(x) / 16) for x in sel)) + 8,
-                     np.random.default_rng(33))
-    tables = [fl.allocate(int(x)) for x in sel]
-    b = wl.build_batch("serving_mix_sample", ctx_lens=sel - 1, num_heads=32,
-                       num_kv_heads=8, head_dim=128, dtype="bf16",
-                       num_blocks=len(fl.free) + sum(map(len, tables)), tables=tables,
-                       seed=3, device="cpu", canary=False, new_in_pool=True,
-                       q_std=1.0, kv_std=0.5)
-    return b, int(lens.sum())
-
-
-def run_oracle_timed(b, batch_tokens: int, budget_s: float, threads: int):
-    """Repeat the oracle's decode of the sample until `budget_s` elapsed;
-    scale time per attended token to the full 256-sequence batch."""
+def oracle_step(b, threads: int):
+    """One step of the hot path on the oracle: the cache write of the batch's
+    new tokens, then decode of every (sequence, head) over the written
+    caches, on `threads` host threads.  Returns the step's wall time (s)."""
     import oracle
-    pr = (b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale, b.num_kv_heads,
-          b.dtype)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode(*pr, nthreads=threads)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    sample_tokens = int(b.seq_lens.sum())
-    t_batch = el / reps * batch_tokens / sample_tokens
-    return 256 / t_batch, reps, el
+    t0 = time.perf_counter()
+    kc, vc, _ = oracle.reshape_and_cache(b.k_new, b.v_new, b.k_cache, b.v_cache,
+                                         b.slot_mapping, b.dtype)
+    oracle.decode(b.q, kc, vc, b.block_tables, b.seq_lens, b.scale, b.num_kv_heads,
+                  b.dtype, nthreads=threads)
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(budget_s: float, n_seqs: int = 32):
+def host_serving_mix():
+    """The serving-mix batch built on the host: the same seeded structure
+    (lengths, tables, pool size) as the GPU arm's; values from the host's
+    generator."""
+    return wl.serving_mix(device="cpu", canary=False)
+
+
+def cpu_baseline(budget_s: float):
+    """The oracle on the host cores over the whole serving-mix batch: whole
+    steps (cache write + decode of all 256 sequences) repeated for about
+    `budget_s` seconds on all cores, and one whole step on one thread."""
     import oracle
     oracle.build()
-    b, batch_tokens = oracle_sample(n_seqs)
+    b = host_serving_mix()
     cores = os.cpu_count() or 1
-    v, reps, el = run_oracle_timed(b, batch_tokens, budget_s, cores)
-    v1, reps1, el1 = run_oracle_timed(b, batch_tokens, max(1.0, budget_s / 4), 1)
-    return {"value": v, "unit": "seqs/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {n_seqs} of the 256 serving-mix sequences "
-                      f"({int(b.seq_lens.sum())} of {batch_tokens} tokens), decode only, "
-                      f"{reps} repetitions in {el:.1f} s, scaled per attended token to the "
-                      f"full batch",
-            "single_thread_value": v1}
+    oracle_step(b, cores)                                  # first touch of the buffers
+    times = []
+    while sum(times) < budget_s or len(times) < 2:
+        times.append(oracle_step(b, cores))
+    t1 = oracle_step(b, 1)
+    t = statistics.mean(times)
+    return {"value": b.num_seqs / t, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+            "sample": f"the whole serving-mix batch ({b.num_seqs} sequences, "
+                      f"{int(b.seq_lens.sum())} tokens): {len(times)} steps of fp64 cache "
+                      f"write + decode with {cores} threads, {statistics.mean(times):.2f} s "
+                      f"per step, no scaling",
+            "ms_per_step": t * 1e3,
+            "single_thread_value": b.num_seqs / t1,
+            "single_thread_sample": f"one whole step on one thread ({t1:.2f} s)"}
 
 
 def reference_arm(args):
     """The oracle as the reference implementation, on the host cores.  Each
-    step decodes a sample of the batch, sized so that the whole run takes
-    about --ref-budget seconds."""
+    step is the whole serving-mix step: the cache write of 256 tokens, then
+    decode of all 256 sequences, in fp64 on all host cores; nothing is
+    sampled or scaled."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    probe, _ = oracle_sample(4)
-    t0 = time.perf_counter()
-    oracle.decode(probe.q, probe.k_cache, probe.v_cache, probe.block_tables, probe.seq_lens,
-                  probe.scale, probe.num_kv_heads, probe.dtype, nthreads=cores)
-    per_tok = (time.perf_counter() - t0) / int(probe.seq_lens.sum())
-    mean_tokens = 149625 / 256
-    per_step = args.ref_budget / (args.steps + args.warmup)
-    n = int(max(2, min(args.ref_seqs, per_step / (per_tok * mean_tokens))))
-    b, batch_tokens = oracle_sample(n)
+    b = host_serving_mix()
     for _ in range(args.warmup):
-        oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
-                      b.num_kv_heads, b.dtype, nthreads=cores)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale,
-                      b.num_kv_heads, b.dtype, nthreads=cores)
-        times.append(time.perf_counter() - t0)
-    per_tok = sum(times) / int(b.seq_lens.sum()) / len(times)
-    t_step = per_tok * batch_tokens                 # one full 256-sequence step
-    value = 256 / t_step
-    sample = (f"first {n} of the 256 serving-mix sequences "
-              f"({int(b.seq_lens.sum())} of {batch_tokens} tokens) per step, fp64 oracle "
-              f"decode with {cores} threads, scaled per attended token to the full batch")
+        oracle_step(b, cores)
+    times = [oracle_step(b, cores) for _ in range(args.steps)]
+    t_step = statistics.mean(times)
+    value = b.num_seqs / t_step
+    sample = (f"the whole serving-mix batch every step ({b.num_seqs} sequences, "
+              f"{int(b.seq_lens.sum())} tokens): fp64 oracle cache write + decode with "
+              f"{cores} threads, {args.steps} timed steps after {args.warmup} warm-up")
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; no dataset)",
-        "config": {"workload": WORKLOAD, "global_batch": 256},
+        "config": bench_config(b, 1),
         "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
@@ -930,10 +917,6 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline")
-    ap.add_argument("--ref-seqs", type=int, default=32,
-                    help="at most this many sequences per reference-arm step")
-    ap.add_argument("--ref-budget", type=float, default=90.0,
-                    help="approximate seconds of oracle work for the reference arm")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the long-context, paging-overhead, multi-query, FP8 and "
                          "copy-on-write measurements")
