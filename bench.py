@@ -531,16 +531,39 @@ def shared_prefix_arm(args, device, flush, pa):
     for _ in range(3):
         call()
     ms = time_calls(call, 30, flush, torch.cuda.current_stream())
+    # the same batch through the cascade entry point: the prefix blocks once,
+    # each sequence's own table beside them
+    P = int(b.meta["prefix_tokens"]) // 16
+    prefix, own_tab, own_len = wl.cascade_split(b, P)
+    pt = torch.from_numpy(prefix).to(device)
+    ot = torch.from_numpy(own_tab).to(device)
+    ol = torch.from_numpy(own_len).to(device)
+    ws = torch.empty(pa.pa_decode_cascade_workspace_size(b.num_seqs, b.num_heads, b.head_dim, P,
+                                                         own_tab.shape[1]),
+                     dtype=torch.uint8, device=device)
+    out_c = torch.empty_like(b.q)
+
+    def call_c():
+        pa.pa_decode_cascade(out_c, b.q, b.k_cache, b.v_cache, pt, ot, ol, b.scale,
+                             b.num_kv_heads, ws)
+    for _ in range(3):
+        call_c()
+    ms_c = time_calls(call_c, 30, flush, torch.cuda.current_stream())
     nb = decode_bytes(b)
     unique = shared_prefix_unique_bytes(b)
     t = statistics.median(ms) * 1e-3
+    tc = statistics.median(ms_c) * 1e-3
     peak, kind = measured_peak()
-    del b
+    del b, ws
     torch.cuda.empty_cache()
     return {"workload": "shared_prefix: batch 128, 32/8 x 128 bf16, a 2048-token prefix in 128 "
                         "shared physical blocks + U[64,512] private tokens",
             "us_per_call": t * 1e6, "logical_gbs": nb["total"] / t / 1e9,
             "unique_gbs": unique / t / 1e9, "unique_frac_of_peak": unique / t / 1e9 / peak,
+            "cascade": {"call": "pa_decode_cascade (prefix blocks once + own tables)",
+                        "us_per_call": tc * 1e6, "unique_gbs": unique / tc / 1e9,
+                        "unique_frac_of_peak": unique / tc / 1e9 / peak,
+                        "speedup_over_pa_decode": t / tc},
             "peak_kind": kind, "bytes": {"logical": nb["total"], "unique": unique}}
 
 
@@ -835,6 +858,21 @@ def single_kernel(args, device):
 
         def call():
             pa.pa_decode(out, b.q, b.k_cache, b.v_cache, bt, sl, b.scale, b.num_kv_heads)
+    elif args.only == "cascade":
+        b = wl.shared_prefix(device=device, canary=False)
+        P = int(b.meta["prefix_tokens"]) // 16
+        prefix, own_tab, own_len = wl.cascade_split(b, P)
+        pt = torch.from_numpy(prefix).to(device)
+        ot = torch.from_numpy(own_tab).to(device)
+        ol = torch.from_numpy(own_len).to(device)
+        ws = torch.empty(pa.pa_decode_cascade_workspace_size(
+            b.num_seqs, b.num_heads, b.head_dim, P, own_tab.shape[1]), dtype=torch.uint8,
+            device=device)
+        out = torch.empty_like(b.q)
+
+        def call():
+            pa.pa_decode_cascade(out, b.q, b.k_cache, b.v_cache, pt, ot, ol, b.scale,
+                                 b.num_kv_heads, ws)
     elif args.only == "partitioned":
         b = wl.long_context(device=device, canary=False)
         bt, sl, _ = b.torch_tables(device)
@@ -921,7 +959,8 @@ def main():
                     help="skip the long-context, paging-overhead, multi-query, FP8 and "
                          "copy-on-write measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["decode", "shared_prefix", "partitioned", "cache_write",
+    ap.add_argument("--only", choices=["decode", "shared_prefix", "cascade", "partitioned",
+                                       "cache_write",
                                        "multi_spec", "multi_prefill", "decode_fp8",
                                        "cache_write_fp8", "partitioned_fp8", "copy_blocks"],
                     help="launch one kernel alone (for profiling); prints timings only")

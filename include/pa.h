@@ -14,6 +14,8 @@
  *   pa_decode_multi        several new query tokens per sequence (a
  *                          prompt chunk or speculative positions), causal
  *                          among themselves, over the same paged cache
+ *   pa_decode_cascade      decode of a batch sharing a prompt prefix: the
+ *                          shared blocks read once per KV head
  *   pa_copy_blocks         block copies of copy-on-write, all layers at once
  *   *_fp8                  the cache write, decode and split-KV decode
  *                          over an FP8 (E4M3) cache with per-KV-head scales
@@ -358,6 +360,59 @@ int pa_decode_partitioned_fp8(void *out, const void *q, const void *k_cache,
                               int32_t partition_size, int32_t max_seq_len,
                               void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/*
+ * pa_decode_cascade_workspace_size -- bytes of workspace pa_decode_cascade
+ * needs for these sizes (fp32 partial results in the layout documented at
+ * pa_decode_partitioned_workspace_size, with one partition per prefix chunk
+ * followed by 512-token partitions of each sequence's own blocks).  Returns
+ * 0 on invalid sizes (num_prefix_blocks must be positive).
+ */
+size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                        int32_t head_dim,
+                                        int32_t num_prefix_blocks,
+                                        int32_t max_blocks_per_seq);
+
+/*
+ * pa_decode_cascade -- decode for a batch whose sequences all begin with
+ * the same physical blocks (a shared prompt: "vLLM: High-Throughput Serving
+ * with PagedAttention", *How PagedAttention shares memory*; "vLLM:
+ * Architecture, PagedAttention & Internals", *Prefix caching: reuse KV
+ * across requests*), reading the shared blocks once per KV head instead of
+ * once per sequence.
+ *
+ * Sequence s attends over 16 * num_prefix_blocks prefix tokens, held in the
+ * physical blocks prefix_blocks[0 .. num_prefix_blocks) (int32, device),
+ * followed by seq_lens[s] tokens of its own, held in block_tables[s][0 ..].
+ * The result equals pa_decode over the concatenated table
+ * (prefix_blocks ++ block_tables[s]) with seq_len 16 * num_prefix_blocks +
+ * seq_lens[s].  The caller states the sharing (the block manager knows which
+ * leading blocks a batch shares); nothing here compares tables.
+ *
+ * Work: the prefix is cut into chunks; per (chunk, KV head) the query heads
+ * of all sequences, 128 (sequence, head) rows at a time, are multiplied
+ * against the chunk's keys and values on the tensor cores (tcgen05); each
+ * sequence's own blocks are decoded as 512-token split-KV partitions; a last
+ * kernel merges every (sequence, head)'s partials by log-sum-exp.  Three
+ * launches on `stream`.
+ *
+ * Requirements as pa_decode, plus: dtype PA_BF16 or PA_F16 (PA_F32:
+ * PA_ERR_UNSUPPORTED when num_prefix_blocks > 0), q rows and out 16-byte
+ * aligned, workspace_bytes >= pa_decode_cascade_workspace_size(...) with a
+ * 256-byte aligned workspace.  num_prefix_blocks == 0 is pa_decode (no
+ * workspace needed).  A prefix block id outside the pool is skipped and
+ * flagged PA_DEVERR_BLOCK_ID; a seq_len past max_blocks_per_seq * 16 is
+ * clamped and flagged PA_DEVERR_SEQ_LEN.
+ */
+int pa_decode_cascade(void *out, const void *q, const void *k_cache,
+                      const void *v_cache, const int32_t *prefix_blocks,
+                      int32_t num_prefix_blocks, const int32_t *block_tables,
+                      const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int64_t num_blocks, int32_t block_size,
+                      int32_t max_blocks_per_seq, int64_t q_seq_stride,
+                      float scale, int32_t dtype, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * pa_decode_partitioned_noalloc -- pa_decode_partitioned without a caller

@@ -116,6 +116,15 @@ int32_t pa_bm_refcount(const pa_bm *bm, int32_t block);
 int pa_bm_batch(const pa_bm *bm, const int64_t *seq_ids, int32_t n, int32_t *tables,
                 int32_t width, int32_t pad, int32_t *seq_lens);
 
+/*
+ * Leading blocks every sequence of seq_ids[0 .. n) shares: the largest P such
+ * that all their tables hold the same physical block at each of positions
+ * 0 .. P-1 and every one of them holds at least block_size * P tokens (the
+ * prefix a cascade decode, pa_decode_cascade, reads once).  0 for n == 0 or when
+ * nothing is shared; PA_ERR_INVALID_ARG for an unknown id.
+ */
+int32_t pa_bm_common_prefix(const pa_bm *bm, const int64_t *seq_ids, int32_t n);
+
 /* ---- serving loop ----------------------------------------------------------
  *
  * The pages' toy serving loop over a block manager (which it does not own;

@@ -33,6 +33,7 @@ def _lib():
             "pa_bm_seq_len": (i64, [P, i64]),
             "pa_bm_refcount": (i32, [P, i32]),
             "pa_bm_batch": (ctypes.c_int, [P, P, i32, P, i32, i32, P]),
+            "pa_bm_common_prefix": (i32, [P, P, i32]),
             "pa_loop_create": (P, [P]),
             "pa_loop_destroy": (None, [P]),
             "pa_loop_submit": (ctypes.c_int, [P, i64, i64, i64]),
@@ -138,6 +139,16 @@ class BlockManager:
         self._check("pa_bm_batch", self._l.pa_bm_batch(
             self._h, _ptr(ids), ids.size, _ptr(tables), int(width), int(pad), _ptr(lens)))
         return tables, lens
+
+    def common_prefix(self, seq_ids) -> int:
+        """Leading blocks all of ``seq_ids`` share, each full in every one of
+        them (the prefix block list of a cascade decode is the first of their
+        tables cut to this length)."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = int(self._l.pa_bm_common_prefix(self._h, _ptr(ids), ids.size))
+        if n < 0:
+            raise KeyError("unknown sequence id")
+        return n
 
 
 class ServingLoop:

@@ -284,7 +284,7 @@ bool workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
 
 extern "C" {
 
-int pa_abi_version(void) { return 2; }
+int pa_abi_version(void) { return 3; }
 
 const char *pa_status_string(int status) {
     switch (status) {
@@ -405,6 +405,7 @@ int pa_decode_partitioned(void *out, const void *q, const void *k_cache,
     if (e != cudaSuccess) return PA_ERR_CUDA;
 
     pa::MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);
     mp.out = out;
     mp.part_o = p.part_o; mp.part_m = p.part_m; mp.part_l = p.part_l;
     mp.seq_lens = seq_lens;
@@ -604,6 +605,7 @@ int decode_fp8_common(void *out, const void *q, const void *k_cache, const void 
     if (e != cudaSuccess) return PA_ERR_CUDA;
     if (!partial) return PA_OK;
     pa::MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);
     mp.out = out;
     mp.part_o = p.part_o; mp.part_m = p.part_m; mp.part_l = p.part_l;
     mp.seq_lens = seq_lens;
@@ -723,6 +725,146 @@ int pa_device_error(uint32_t *flags, int clear) {
     unsigned int f = 0;
     cudaError_t e = pa::read_device_error(&f, clear != 0);
     *flags = f;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---- cascade decode over a shared prefix -----------------------------------
+//
+// Sequences whose block tables begin with the same physical blocks (a shared
+// prompt, prefix caching) attend to those blocks once: the prefix's keys and
+// values are read once per KV head and multiplied against the query heads
+// of every sequence at once (128 (sequence, head) rows per tensor-core tile),
+// then each sequence's own blocks are decoded as split-KV partitions, and the
+// two are merged by log-sum-exp.
+
+namespace {
+
+// Prefix chunks of the cascade: at least 16 blocks (256 keys) each, at most
+// 16 chunks; the sequences' own blocks in partitions of 512 tokens.
+constexpr int32_t kCascadeSuffixPart = 512;
+
+int32_t cascade_chunk_blocks(int32_t num_prefix_blocks) {
+    int32_t c = (num_prefix_blocks + 15) / 16;
+    c = (c + 3) / 4 * 4;
+    return c < 16 ? 16 : c;
+}
+
+// Partitions of the cascade workspace: the prefix chunks, then the sequence's.
+bool cascade_parts(int32_t num_prefix_blocks, int32_t max_blocks_per_seq, int32_t *nch,
+                   int32_t *parts) {
+    if (num_prefix_blocks <= 0 || max_blocks_per_seq < 0) return false;
+    const int32_t cb = cascade_chunk_blocks(num_prefix_blocks);
+    *nch = (num_prefix_blocks + cb - 1) / cb;
+    const int64_t ps = ((int64_t)max_blocks_per_seq * 16 + kCascadeSuffixPart - 1) / kCascadeSuffixPart;
+    const int64_t total = *nch + (ps > 0 ? ps : 1);
+    if (total * kCascadeSuffixPart > INT32_MAX) return false;
+    *parts = (int32_t)total;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                        int32_t num_prefix_blocks, int32_t max_blocks_per_seq) {
+    int32_t nch = 0, P = 0;
+    if (!cascade_parts(num_prefix_blocks, max_blocks_per_seq, &nch, &P)) return 0;
+    WorkspaceLayout w;
+    if (!workspace_layout(num_seqs, num_heads, head_dim, P * kCascadeSuffixPart,
+                          kCascadeSuffixPart, &w))
+        return 0;
+    return w.total;
+}
+
+int pa_decode_cascade(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *prefix_blocks, int32_t num_prefix_blocks,
+                      const int32_t *block_tables, const int32_t *seq_lens, int32_t num_seqs,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int64_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                      int64_t q_seq_stride, float scale, int32_t dtype, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+    int rc = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, q_seq_stride, scale, dtype);
+    if (rc != PA_OK) return rc;
+    if (num_prefix_blocks < 0 || (num_prefix_blocks > 0 && !prefix_blocks))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_prefix_blocks == 0)                              // nothing shared: plain decode
+        return pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
+                         num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                         q_seq_stride, scale, dtype, stream);
+    if (dtype == PA_F32) return PA_ERR_UNSUPPORTED;         // the prefix runs on 16-bit MMAs
+    if (!q_rows_aligned(q, q_seq_stride, dtype) || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    int32_t nch = 0, P = 0;
+    if (!cascade_parts(num_prefix_blocks, max_blocks_per_seq, &nch, &P)) return PA_ERR_UNSUPPORTED;
+    WorkspaceLayout w;
+    if (!workspace_layout(num_seqs, num_heads, head_dim, P * kCascadeSuffixPart,
+                          kCascadeSuffixPart, &w))
+        return PA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < w.total ||
+        (reinterpret_cast<uintptr_t>(workspace) % kAlign))
+        return PA_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const int G = num_heads / num_kv_heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    pa::DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.out = out; p.q = q; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.block_tables = block_tables; p.seq_lens = seq_lens;
+    p.part_o = reinterpret_cast<float *>(ws + w.o);
+    p.part_m = reinterpret_cast<float *>(ws + w.m);
+    p.part_l = reinterpret_cast<float *>(ws + w.l);
+    p.num_blocks = num_blocks; p.q_seq_stride = q_seq_stride;
+    p.num_seqs = num_seqs; p.num_heads = num_heads; p.num_kv_heads = num_kv_heads;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_parts = P;
+    p.scale_log2 = scale * pa::LOG2E;
+    if (pa::device_error_ptr(&p.err) != cudaSuccess) return PA_ERR_CUDA;
+    if (!prepare_maps(p, dtype, head_dim)) return PA_ERR_CUDA;
+
+    // 1. the shared prefix: partitions 0 .. nch-1, on the tcgen05 kernel
+    {
+        pa::DecodeParams pp = p;
+        pp.prefix_blocks = prefix_blocks;
+        pp.prefix_nblocks = num_prefix_blocks;
+        pp.prefix_chunk_blocks = cascade_chunk_blocks(num_prefix_blocks);
+        CUtensorMap tmap_q;
+        if (!encode_q_map(&tmap_q, q, num_seqs, num_heads, head_dim, q_seq_stride, G, dtype))
+            return PA_ERR_CUDA;
+        cudaError_t e = dtype == PA_BF16 ? pa::prefill_tc_bf16(pp, tmap_q, head_dim, G, 1, st)
+                                         : pa::prefill_tc_f16(pp, tmap_q, head_dim, G, 1, st);
+        if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    // 2. each sequence's own blocks: split-KV partitions nch .. P-1
+    {
+        pa::DecodeParams ps = p;
+        ps.part_o = p.part_o + (size_t)nch * head_dim;
+        ps.part_m = p.part_m + nch;
+        ps.part_l = p.part_l + nch;
+        ps.partition_blocks = kCascadeSuffixPart / 16;
+        ps.max_seq_len = max_blocks_per_seq * 16;
+        cudaError_t e = run_persistent(ps, dtype, head_dim, G, true,
+                                       (long long)num_seqs * num_kv_heads * (P - nch), st);
+        if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    // 3. log-sum-exp merge of the prefix chunks and the sequence's partitions
+    pa::MergeParams mp;
+    std::memset(&mp, 0, sizeof mp);
+    mp.out = out;
+    mp.part_o = p.part_o; mp.part_m = p.part_m; mp.part_l = p.part_l;
+    mp.seq_lens = seq_lens;
+    mp.num_heads = num_heads; mp.head_dim = head_dim;
+    mp.max_parts = P; mp.partition_size = kCascadeSuffixPart;
+    mp.seq_cap = max_blocks_per_seq * 16;
+    mp.prefix_parts = nch;
+    cudaError_t e = run_merge(mp, dtype, num_seqs, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

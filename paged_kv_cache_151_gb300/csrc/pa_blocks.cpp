@@ -335,6 +335,29 @@ int pa_bm_batch(const pa_bm *bm, const int64_t *seq_ids, int32_t n, int32_t *tab
     return PA_OK;
 }
 
+int32_t pa_bm_common_prefix(const pa_bm *bm, const int64_t *seq_ids, int32_t n) {
+    if (!bm || n < 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID_ARG;
+    if (n == 0) return 0;
+    const std::vector<int32_t> *first = nullptr;
+    size_t common = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end()) return PA_ERR_INVALID_ARG;
+        const auto &t = it->second.table;
+        const size_t full = it->second.tokens.size() / (size_t)bm->bs;
+        if (!first) {
+            first = &t;
+            common = full < t.size() ? full : t.size();
+            continue;
+        }
+        size_t k = 0;
+        const size_t lim = common < full ? common : full;
+        while (k < lim && k < t.size() && t[k] == (*first)[k]) ++k;
+        common = k;
+    }
+    return (int32_t)common;
+}
+
 }  // extern "C"
 
 // ---- serving loop ---------------------------------------------------------

@@ -71,6 +71,13 @@ struct DecodeParams {
     int num_q_rows;           // multi-token queries: rows of q and out
     int mq_split_rows;        // multi-token queries: > 0: sequences with at least this
                               // many (token, head) rows are left to the prefill kernel
+    // cascade prefix (prefill_tc_kernel): prefix_nblocks > 0 attends the G
+    // heads of every sequence to the shared prefix blocks prefix_blocks[0..n),
+    // in chunks of prefix_chunk_blocks blocks; chunk c's (m, l, o) per
+    // (sequence, head) go to partition c of part_o / part_m / part_l
+    const int32_t *prefix_blocks;
+    int prefix_nblocks;
+    int prefix_chunk_blocks;
     const float *k_scale;     // E4M3 caches: [num_kv_heads] dequantisation scales
     const float *v_scale;
     float scale_log2;         // scale * log2(e)
@@ -320,6 +327,8 @@ struct MergeParams {
     int max_parts;
     int partition_size;
     int seq_cap;              // min(max_seq_len, max_blocks*16)
+    int prefix_parts;         // cascade: leading parts of the shared prefix, always
+                              // present; the sequence's own partitions follow them
 };
 
 template <typename T>
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     const int h = blockIdx.x, s = blockIdx.y;
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.seq_cap ? p.seq_cap : L);
-    const int n = (L + p.partition_size - 1) / p.partition_size;
+    const int n = p.prefix_parts + (L + p.partition_size - 1) / p.partition_size;
     const long long row = ((long long)s * p.num_heads + h) * p.max_parts;
     const float *m = p.part_m + row;
     const float *l = p.part_l + row;

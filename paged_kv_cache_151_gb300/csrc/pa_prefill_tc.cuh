@@ -144,7 +144,17 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tP = tmem + 64, tO = tmem + 128;
 
-    const int total = prefill_schedule<G, TC_ROWS>(p, groups, sched);
+    // Cascade prefix (p.prefix_nblocks > 0): an item is (prefix chunk, KV
+    // head, 128 rows of (sequence, head) pairs) -- row r of row group grp is
+    // head (grp*128 + r) % G of sequence (grp*128 + r) / G, every row sees
+    // every key of the chunk, and the item writes the rows' (m, l, o) of the
+    // chunk as a partition of the split-KV workspace.  Row groups of one
+    // (chunk, KV head) are consecutive items, so their K/V come from L2.
+    const bool cascade = p.prefix_nblocks > 0;
+    const int nrg = (p.num_seqs * G + TC_ROWS - 1) / TC_ROWS;     // cascade row groups
+    const int total = cascade
+        ? ((p.prefix_nblocks + p.prefix_chunk_blocks - 1) / p.prefix_chunk_blocks) * Hkv * nrg
+        : prefill_schedule<G, TC_ROWS>(p, groups, sched);
 
     // the caches (and q, out) only after the kernel before this one is done
     grid_dependency_wait();
@@ -157,6 +167,22 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     auto item_at = [&](int k, Item &it) -> bool {  // all lanes of a warp
         const long long xl = (long long)k * R + ((k & 1) ? (R - 1 - me) : me);   // snake
         if (xl >= total) return false;
+        if (cascade) {
+            // it.s: the chunk; rows: (sequence, head) pairs of all sequences
+            const int per = Hkv * nrg, x = (int)xl;
+            it.s = x / per;
+            it.j = (x % per) / nrg;
+            it.grp = (x % per) % nrg;
+            const int b0 = it.s * p.prefix_chunk_blocks;
+            const int nbk = min(p.prefix_chunk_blocks, p.prefix_nblocks - b0);
+            it.q0 = 0;
+            it.nq = p.num_seqs;
+            it.L = 16 * nbk;                                         // keys of the chunk
+            it.nrows = min(TC_ROWS, p.num_seqs * G - it.grp * TC_ROWS);
+            it.nsteps = (it.L + TC_KEYS - 1) / TC_KEYS;
+            it.nb_seq = nbk;
+            return true;
+        }
         prefill_item<G, TC_ROWS>(p, groups, sched, (int)xl, it.s, it.j, it.grp);
         it.q0 = p.query_start[it.s];
         it.nq = p.query_start[it.s + 1] - it.q0;
@@ -205,7 +231,9 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             // read one step ahead so that its latency passes while the warp
             // waits for a stage; lanes l < 4 * NH then issue one box each
             // (block l % 4, 64-element half l / 4).
-            const int32_t *row = p.block_tables + (long long)it.s * p.max_blocks;
+            const int32_t *row = cascade
+                ? p.prefix_blocks + (long long)it.s * p.prefix_chunk_blocks
+                : p.block_tables + (long long)it.s * p.max_blocks;
             auto fetch = [&](int c) -> int {
                 const int lb = (TC_KEYS / 16) * c + lane;
                 return (lane < TC_KEYS / 16 && c < it.nsteps && lb < it.nb_seq) ? __ldg(row + lb) : -1;
@@ -329,9 +357,11 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             const bool row_ok = r < it.nrows;
             const int rr = it.grp * TC_ROWS + r;
             const int tok = rr / G, head = rr % G;
-            // last visible position; rows past the run see what its last row sees
-            const int lim = it.L - it.nq + min(tok, it.nq - 1);
+            // last visible position; rows past the run see what its last row
+            // sees; in a cascade chunk every row sees every key
+            const int lim = cascade ? it.L - 1 : it.L - it.nq + min(tok, it.nq - 1);
             float m_run = -INFINITY, l_run = 0.f;
+            float m_max = -INFINITY;               // largest score (log2 units, scaled)
             for (int c = 0; c < n; ++c, ++g) {
                 const int b = (int)(g & 1);
                 const uint32_t ph = (uint32_t)((g >> 1) & 1);
@@ -360,6 +390,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
                     m4[3] = max3f(m4[3], sv[e + 6], sv[e + 7]);
                 }
                 const float mxs = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;
+                m_max = fmaxf(m_max, mxs);
                 // lazy rescaling: the reference level moves only by more than 2^RESCALE_LOG2
                 const float m_new = mxs > m_run + RESCALE_LOG2 ? mxs : m_run;
                 const float ms = m_new == -INFINITY ? 0.f : m_new;
@@ -431,6 +462,29 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
             tc5_fence_after_sync();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            if (cascade) {
+                // chunk it.s of (sequence tok, head j*G + head): o = O / l, and
+                // (m, l) taken to the true maximum, m in natural units
+                const long long prow = ((long long)tok * H + it.j * G + head) * p.max_parts + it.s;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float v[32];
+                    tc5_ld32(tO + lane_base + c0, v);
+                    if (row_ok) {
+                        float *po = p.part_o + prow * D + c0;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4 *>(po + e) =
+                                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+                    }
+                }
+                if (row_ok) {
+                    p.part_m[prow] = m_max * LN2;
+                    p.part_l[prow] = l_run * ex2(m_run - m_max);
+                }
+                tc5_fence_before_sync();
+                continue;
+            }
             T *o = reinterpret_cast<T *>(p.out) + ((long long)(it.q0 + tok) * H + it.j * G + head) * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -485,8 +539,14 @@ cudaError_t launch_prefill_tc(const DecodeParams &p, const CUtensorMap &tmap_q, 
         (long long)p.num_kv_heads * 2 * ((rows_all + PREFILL_GROUP_ROWS - 1) / PREFILL_GROUP_ROWS);
     const int sms = sm_count_of_current_device();
     long long blocks = (long long)(sms > 0 ? sms : 152) * TC_BLOCKS_PER_SM;
-    if (blocks > worst) blocks = worst;
-    if (blocks > bound) blocks = bound;
+    if (p.prefix_nblocks > 0) {                    // cascade prefix: its items
+        const long long nrg = ((long long)p.num_seqs * G + TC_ROWS - 1) / TC_ROWS;
+        const long long nch = (p.prefix_nblocks + p.prefix_chunk_blocks - 1) / p.prefix_chunk_blocks;
+        if (blocks > nch * p.num_kv_heads * nrg) blocks = nch * p.num_kv_heads * nrg;
+    } else {
+        if (blocks > worst) blocks = worst;
+        if (blocks > bound) blocks = bound;
+    }
     if (blocks <= 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, 1, 1);

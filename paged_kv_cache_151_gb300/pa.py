@@ -69,6 +69,11 @@ def load():
         lib.pa_decode_partitioned.argtypes = dec + [i32, i32, P, sz, P]
         lib.pa_decode_partitioned_noalloc.restype = ctypes.c_int
         lib.pa_decode_partitioned_noalloc.argtypes = dec + [i32, i32, P]
+        lib.pa_decode_cascade_workspace_size.restype = sz
+        lib.pa_decode_cascade_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.pa_decode_cascade.restype = ctypes.c_int
+        lib.pa_decode_cascade.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i64, i32,
+                                          i32, i64, f32, i32, P, sz, P]
         lib.pa_decode_multi.restype = ctypes.c_int
         lib.pa_decode_multi.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                         i64, i32, i32, i64, f32, i32, P]
@@ -212,6 +217,38 @@ def pa_decode_partitioned(out, q, k_cache, v_cache, block_tables, seq_lens, scal
                                       int(partition_size), int(max_seq_len),
                                       workspace.data_ptr(), nbytes, _stream(stream))
     _check("pa_decode_partitioned", rc)
+
+
+def pa_decode_cascade_workspace_size(num_seqs, num_heads, head_dim, num_prefix_blocks,
+                                     max_blocks_per_seq) -> int:
+    return int(load().pa_decode_cascade_workspace_size(
+        int(num_seqs), int(num_heads), int(head_dim), int(num_prefix_blocks),
+        int(max_blocks_per_seq)))
+
+
+def pa_decode_cascade(out, q, k_cache, v_cache, prefix_blocks, block_tables, seq_lens, scale,
+                      num_kv_heads, workspace, stream=None):
+    """Decode for sequences that all begin with the physical blocks
+    ``prefix_blocks`` (int32 [P], on the device): sequence s attends over the
+    16 * P prefix tokens, then seq_lens[s] tokens of its own in
+    block_tables[s].  ``workspace``: a CUDA uint8 tensor of at least
+    ``pa_decode_cascade_workspace_size(...)`` bytes, 256-byte aligned."""
+    args = _decode_args(out, q, k_cache, v_cache, block_tables, seq_lens)
+    if num_kv_heads != k_cache.shape[1]:
+        raise ValueError("num_kv_heads does not match the cache")
+    _dev(prefix_blocks, "prefix_blocks")
+    if prefix_blocks.dtype != torch.int32 or prefix_blocks.dim() != 1 or \
+            not prefix_blocks.is_contiguous():
+        raise ValueError("prefix_blocks must be a contiguous int32 [num_prefix_blocks]")
+    _dev(workspace, "workspace")
+    nbytes = workspace.numel() * workspace.element_size()
+    out_p, q_p, kc, vc, bt, sl = args[:6]
+    rest = args[6:]                                # B, H, Hkv, D, N, bs, max_blocks, q stride
+    rc = load().pa_decode_cascade(out_p, q_p, kc, vc, prefix_blocks.data_ptr(),
+                                  prefix_blocks.shape[0], bt, sl, *rest, float(scale),
+                                  _DTYPE[q.dtype], workspace.data_ptr(), nbytes,
+                                  _stream(stream))
+    _check("pa_decode_cascade", rc)
 
 
 # Bytes of the workspace built into the library for the call below.
@@ -421,6 +458,7 @@ __all__ = [
     "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_partitioned_workspace_size", "pa_decode_partitioned", "pa_decode_multi",
     "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",
+    "pa_decode_cascade", "pa_decode_cascade_workspace_size",
     "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_partitioned_fp8",
     "pa_copy_blocks",
     "pa_device_error", "workspace_views",

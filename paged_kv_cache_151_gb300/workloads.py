@@ -366,6 +366,27 @@ def _build_shared(tables, shared, fl, seq_lens, prefix_tokens, seed,
         meta={"shared_blocks": list(shared), "prefix_tokens": prefix_tokens})
 
 
+def cascade_split(b: PagedBatch, prefix_blocks: int):
+    """The cascade layout of a batch whose tables all begin with the same
+    ``prefix_blocks`` physical blocks: (prefix block ids int32 [P], each
+    sequence's own table int32 [B, W - P] (padded), own lengths int32 [B] =
+    seq_lens - 16 P).  Raises ValueError if the tables do not share those
+    leading blocks or a sequence is shorter than the prefix."""
+    P = int(prefix_blocks)
+    bt = np.asarray(b.block_tables)
+    if P <= 0 or P > bt.shape[1]:
+        raise ValueError("prefix_blocks out of range")
+    prefix = bt[0, :P]
+    if not (bt[:, :P] == prefix[None, :]).all():
+        raise ValueError("the tables do not share their first prefix_blocks entries")
+    own = np.asarray(b.seq_lens, dtype=np.int64) - BLOCK_SIZE * P
+    if (own < 0).any():
+        raise ValueError("a sequence is shorter than the prefix")
+    rest = bt[:, P:] if bt.shape[1] > P else np.full((bt.shape[0], 1), PAD, np.int32)
+    return (np.ascontiguousarray(prefix, dtype=np.int32),
+            np.ascontiguousarray(rest, dtype=np.int32), own.astype(np.int32))
+
+
 def long_context(device="cpu", canary=True, keep_seq=False, batch=8,
                  lo=32768, hi=131072, seed=5, slack=1.02,
                  new_in_pool=False) -> PagedBatch:

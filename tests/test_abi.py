@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert pa.pa_abi_version() == 2
+    assert pa.pa_abi_version() == 3
     assert pa.pa_status_string(0) == "ok"
     assert "invalid" in pa.pa_status_string(-1)
     assert "unsupported" in pa.pa_status_string(-2)
@@ -225,3 +225,45 @@ def test_noalloc_limit_matches_the_header():
     m = re.search(r"#define\s+PA_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "PA_NOALLOC_SCRATCH_BYTES not found in include/pa.h"
     assert pa.PA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def _cascade_status(lib, **kw):
+    a = dict(out=16, q=16, k_cache=16, v_cache=16, prefix=16, n_prefix=8, block_tables=16,
+             seq_lens=16, num_seqs=4, num_heads=8, num_kv_heads=2, head_dim=64, num_blocks=100,
+             block_size=16, max_blocks=4, q_seq_stride=512, scale=0.125, dtype=1,
+             ws=256, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.pa_decode_cascade(a["out"], a["q"], a["k_cache"], a["v_cache"], a["prefix"],
+                                 a["n_prefix"], a["block_tables"], a["seq_lens"], a["num_seqs"],
+                                 a["num_heads"], a["num_kv_heads"], a["head_dim"],
+                                 a["num_blocks"], a["block_size"], a["max_blocks"],
+                                 a["q_seq_stride"], a["scale"], a["dtype"],
+                                 ctypes.c_void_p(a["ws"]), a["ws_bytes"], None)
+
+
+def test_cascade_host_checks(lib):
+    """Refusals of pa_decode_cascade that come before any launch."""
+    assert _cascade_status(lib, prefix=None) == -1            # no prefix list
+    assert _cascade_status(lib, n_prefix=-1) == -1
+    assert _cascade_status(lib, dtype=0) == -2                # fp32 with a prefix
+    assert _cascade_status(lib, ws_bytes=16) == -3            # workspace too small
+    assert _cascade_status(lib, ws=None) == -3
+    assert _cascade_status(lib, ws=128) == -3                 # not 256-byte aligned
+    assert _cascade_status(lib, q=8) == -1                    # q not 16-byte aligned
+    assert _cascade_status(lib, num_seqs=0) == 0              # nothing to do
+    assert _cascade_status(lib, head_dim=96) == -2
+
+
+def test_cascade_workspace_size(lib):
+    def up(x):
+        return (x + 255) // 256 * 256
+    # 128 prefix blocks: chunks of 16 blocks -> 8 parts; own blocks up to 32 -> 1 part
+    B, H, D = 128, 32, 128
+    rows = B * H * (8 + 1)
+    assert pa.pa_decode_cascade_workspace_size(B, H, D, 128, 32) == \
+        up(rows * D * 4) + 2 * up(rows * 4)
+    # 300 prefix blocks: chunks of 20 -> 15 parts; 70 own blocks -> 3 parts of 512 tokens
+    rows = 2 * 8 * (15 + 3)
+    assert pa.pa_decode_cascade_workspace_size(2, 8, 64, 300, 70) == \
+        up(rows * 64 * 4) + 2 * up(rows * 4)
+    assert pa.pa_decode_cascade_workspace_size(B, H, D, 0, 32) == 0

@@ -137,3 +137,50 @@ def test_batch_export_and_errors():
     loop.submit(0, 100, 5)                     # can never fit
     with pytest.raises(Exception):
         loop.step()
+
+
+def brute_common_prefix(bm, ids, bs):
+    """The leading blocks all of `ids` share, each full in all of them, from
+    their exported tables and lengths (position by position)."""
+    tabs = [bm.table(i) for i in ids]
+    full = min(bm.seq_len(i) // bs for i in ids)
+    p = 0
+    while p < full and all(p < len(t) and t[p] == tabs[0][p] for t in tabs):
+        p += 1
+    return p
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_common_prefix_matches_brute_force(seed):
+    """Prompts sharing 0..3 blocks of a system prompt (prefix caching), forks
+    sharing a partial last block, appends; random subsets of the live
+    sequences against a position-by-position count."""
+    rng = np.random.default_rng(seed)
+    bs = 16
+    bm = blocks.BlockManager(4000, bs, prefix_caching=True)
+    system = list(range(100000, 100000 + 3 * bs + 5))
+    live = []
+    for i in range(40):
+        cut = int(rng.integers(0, len(system) + 1))
+        own = (rng.integers(0, 1000, size=int(rng.integers(1, 60))) + 1000 * i).tolist()
+        assert bm.add_sequence(i, system[:cut] + own) is not None
+        live.append(i)
+    for i in range(40, 50):
+        parent = int(rng.choice(live))
+        bm.fork(parent, i)
+        live.append(i)
+    for _ in range(200):
+        sid = int(rng.choice(live))
+        bm.append(sid, int(rng.integers(0, 50000)))
+    assert bm.common_prefix([]) == 0
+    for _ in range(300):
+        k = int(rng.integers(1, 8))
+        ids = [int(x) for x in rng.choice(live, size=k, replace=False)]
+        assert bm.common_prefix(ids) == brute_common_prefix(bm, ids, bs), ids
+    # everything that shares the whole system prompt's three full blocks
+    whole = [i for i in live if bm.seq_len(i) >= 3 * bs and
+             bm.table(i)[:3] == bm.table(live[0])[:3]]
+    if len(whole) > 1:
+        assert bm.common_prefix(whole) == brute_common_prefix(bm, whole, bs)
+    with pytest.raises(KeyError):
+        bm.common_prefix([0, 12345])
