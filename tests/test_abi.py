@@ -257,13 +257,17 @@ def test_cascade_host_checks(lib):
 def test_cascade_workspace_size(lib):
     def up(x):
         return (x + 255) // 256 * 256
-    # 128 prefix blocks: chunks of 16 blocks -> 8 parts; own blocks up to 32 -> 1 part
+    # 128 prefix blocks: chunks of 32 blocks -> 4 parts; 32 own blocks -> 1 part of 512 tokens
     B, H, D = 128, 32, 128
-    rows = B * H * (8 + 1)
+    rows = B * H * (4 + 1)
     assert pa.pa_decode_cascade_workspace_size(B, H, D, 128, 32) == \
         up(rows * D * 4) + 2 * up(rows * 4)
-    # 300 prefix blocks: chunks of 20 -> 15 parts; 70 own blocks -> 3 parts of 512 tokens
-    rows = 2 * 8 * (15 + 3)
+    # 300 prefix blocks: chunks of 32 -> 10 parts; 70 own blocks -> 3 parts of 512 tokens
+    rows = 2 * 8 * (10 + 3)
     assert pa.pa_decode_cascade_workspace_size(2, 8, 64, 300, 70) == \
+        up(rows * 64 * 4) + 2 * up(rows * 4)
+    # 1000 prefix blocks: chunks of 64 (at most 16 chunks)
+    rows = 2 * 8 * (16 + 1)
+    assert pa.pa_decode_cascade_workspace_size(2, 8, 64, 1000, 1) == \
         up(rows * 64 * 4) + 2 * up(rows * 4)
     assert pa.pa_decode_cascade_workspace_size(B, H, D, 0, 32) == 0

@@ -94,11 +94,11 @@ def oracle_whole_tables(b):
 
 CASES = [
     # dtype, D, G, Hkv, num_seqs, prefix blocks, own tokens lo..hi
-    ("bf16", 128, 4, 2, 37, 20, 0, 70),      # 2 chunks (16 + 4 blocks), empty own parts
+    ("bf16", 128, 4, 2, 37, 20, 0, 70),      # one partial chunk (20 blocks), empty own parts
     ("f16", 64, 2, 4, 5, 1, 1, 40),          # one prefix block, one partial step
-    ("bf16", 128, 8, 1, 64, 300, 0, 1100),   # 15 chunks, own parts over 3 partitions
-    ("bf16", 64, 1, 4, 130, 17, 0, 3),       # 2 row groups (130 rows), 16 + 1 blocks
-    ("f16", 128, 4, 8, 3, 64, 500, 520),     # few sequences, 8 KV heads
+    ("bf16", 128, 8, 1, 64, 300, 0, 1100),   # 10 chunks (9 x 32 + 12), own parts over 3 partitions
+    ("bf16", 64, 1, 4, 130, 17, 0, 3),       # 2 row groups (130 rows), one 17-block chunk
+    ("f16", 128, 4, 8, 3, 64, 500, 520),     # few sequences, 8 KV heads, 2 chunks
 ]
 
 
