@@ -805,6 +805,10 @@ int pa_decode_cascade(void *out, const void *q, const void *k_cache, const void 
     if (!q_rows_aligned(q, q_seq_stride, dtype) || !aligned16(out)) return PA_ERR_INVALID_ARG;
     int32_t nch = 0, P = 0;
     if (!cascade_parts(num_prefix_blocks, max_blocks_per_seq, &nch, &P)) return PA_ERR_UNSUPPORTED;
+    // the prefix kernel numbers its items (chunk, KV head, 128-row group) in an int
+    const int G = num_heads / num_kv_heads;
+    const int64_t row_groups = ((int64_t)num_seqs * G + pa::PREFILL_TC_ROWS - 1) / pa::PREFILL_TC_ROWS;
+    if ((int64_t)nch * num_kv_heads * row_groups > INT32_MAX) return PA_ERR_UNSUPPORTED;
     WorkspaceLayout w;
     if (!workspace_layout(num_seqs, num_heads, head_dim, P * kCascadeSuffixPart,
                           kCascadeSuffixPart, &w))
@@ -813,7 +817,6 @@ int pa_decode_cascade(void *out, const void *q, const void *k_cache, const void 
         (reinterpret_cast<uintptr_t>(workspace) % kAlign))
         return PA_ERR_WORKSPACE;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    const int G = num_heads / num_kv_heads;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     pa::DecodeParams p;

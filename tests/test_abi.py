@@ -271,3 +271,9 @@ def test_cascade_workspace_size(lib):
     assert pa.pa_decode_cascade_workspace_size(2, 8, 64, 1000, 1) == \
         up(rows * 64 * 4) + 2 * up(rows * 4)
     assert pa.pa_decode_cascade_workspace_size(B, H, D, 0, 32) == 0
+
+
+def test_cascade_refuses_more_prefix_items_than_an_int_counts(lib):
+    # 16 chunks x 65535 KV heads x 4096 row groups of 128 rows: past 2^31 items
+    assert _cascade_status(lib, num_seqs=65535, num_heads=8 * 65535, num_kv_heads=65535,
+                           n_prefix=10000, q_seq_stride=8 * 65535 * 64) == -2

@@ -165,3 +165,54 @@ def test_full_shared_prefix_cascade(cuda_lib):
     out = run_cascade(cuda_lib, b, P)
     ref, t = fullsize.decode_all(b)
     fullsize.check("shared_prefix: pa_decode_cascade", out, ref, b.dtype, t)
+
+
+def test_cascade_batch_larger_than_one_sort(cuda_lib):
+    """More sequences than the split-KV kernel orders in one block: its own
+    blocks' pass runs as consecutive slices, each writing the partitions of
+    its sequences; prefix rows span many row groups."""
+    b = shared_batch(1104, num_seqs=5000, prefix_blocks=3, own_lo=0, own_hi=40, num_heads=8,
+                     num_kv_heads=2, head_dim=64, dtype="bf16", extra_blocks=16)
+    out = run_cascade(cuda_lib, b, 3)
+    assert_close(out, oracle_whole_tables(b), "cascade 5000 sequences")
+
+
+def test_cascade_driven_by_the_block_manager(cuda_lib):
+    """Requests sharing a system prompt are admitted with prefix caching; the
+    block manager reports the leading blocks the batch shares, the batch is
+    decoded through the cascade and through pa_decode, and both match the
+    oracle over the requests' own tables."""
+    from paged_kv_cache_151_gb300 import blocks
+    H, Hkv, D, BS = 16, 4, 128, 16
+    rng = np.random.default_rng(1105)
+    bm = blocks.BlockManager(4096, BS, prefix_caching=True)
+    system = list(range(500000, 500000 + 5 * BS + 7))           # 5 full shared blocks + 7
+    ids = list(range(24))
+    for i in ids:
+        own = (rng.integers(0, 30000, size=int(rng.integers(1, 90))) + 40000 * (i + 1)).tolist()
+        assert bm.add_sequence(i, system + own) is not None
+    P = bm.common_prefix(ids)
+    assert P == 5
+    width = max(len(bm.table(i)) for i in ids)
+    tables, lens = bm.batch(ids, width)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1105)
+    kc = (torch.randn((4096, Hkv, BS, D), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    vc = (torch.randn((4096, Hkv, BS, D), generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    q = torch.randn((len(ids), H, D), generator=g, device="cuda").to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle.decode(q.cpu(), kc.cpu(), vc.cpu(), tables, lens, scale, Hkv, "bf16", nthreads=8)
+    bt = torch.from_numpy(tables).cuda()
+    sl = torch.from_numpy(lens).cuda()
+    plain = torch.empty_like(q)
+    cuda_lib.pa_decode(plain, q, kc, vc, bt, sl, scale, Hkv)
+    prefix = torch.from_numpy(np.ascontiguousarray(tables[0, :P])).cuda()
+    own_t = torch.from_numpy(np.ascontiguousarray(tables[:, P:])).cuda()
+    own_l = torch.from_numpy((lens - BS * P).astype(np.int32)).cuda()
+    ws = torch.empty(cuda_lib.pa_decode_cascade_workspace_size(len(ids), H, D, P, width - P),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    cuda_lib.pa_decode_cascade(out, q, kc, vc, prefix, own_t, own_l, scale, Hkv, ws)
+    torch.cuda.synchronize()
+    assert_close(out, ref, "cascade from the block manager")
+    assert_close(plain, ref, "pa_decode from the block manager")
