@@ -331,28 +331,64 @@ struct MergeParams {
                               // present; the sequence's own partitions follow them
 };
 
+// One block of 128 threads per (head, sequence) row.  The weight of
+// partition q, c_q = l_q * 2^((m_q - M) log2 e) with M the largest m_q, is
+// formed once (threads over partitions, 128 at a time) into shared memory;
+// thread d then sums c_q * o_q[d] and c_q over the partitions in partition
+// order, eight loads in flight.
 template <typename T>
 __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
-    const int h = blockIdx.x, s = blockIdx.y;
+    constexpr int NT = 128, UNR = 8;
+    __shared__ float cw[NT];
+    __shared__ float wmax[NT / 32];
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    // launched right behind the split-KV kernel that writes the partials, which
+    // lets it start early: wait for that kernel before reading anything
+    grid_dependency_wait();
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.seq_cap ? p.seq_cap : L);
     const int n = p.prefix_parts + (L + p.partition_size - 1) / p.partition_size;
     const long long row = ((long long)s * p.num_heads + h) * p.max_parts;
     const float *m = p.part_m + row;
     const float *l = p.part_l + row;
-    const float *o = p.part_o + row * p.head_dim;
-    float M = -INFINITY;
-    for (int q = 0; q < n; ++q) M = fmaxf(M, m[q]);
-    T *out = reinterpret_cast<T *>(p.out) + ((long long)s * p.num_heads + h) * p.head_dim;
-    for (int d = threadIdx.x; d < p.head_dim; d += blockDim.x) {
-        float O = 0.f, S = 0.f;
-        for (int q = 0; q < n; ++q) {
-            const float cq = l[q] * ex2((m[q] - M) * LOG2E);
-            S += cq;
-            O = fmaf(cq, o[(long long)q * p.head_dim + d], O);
+    const int D = p.head_dim;                      // <= NT
+    const bool dv = tid < D;
+    const float *o = p.part_o + row * D + tid;
+    float mx = -INFINITY;
+    for (int q = tid; q < n; q += NT) mx = fmaxf(mx, m[q]);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    float O = 0.f, S = 0.f;
+    for (int q0 = 0; q0 < n; q0 += NT) {
+        const int q = q0 + tid;
+        const float c = q < n ? l[q] * ex2((m[q] - M) * LOG2E) : 0.f;
+        __syncthreads();                           // the previous weights are used up
+        cw[tid] = c;
+        __syncthreads();
+        const int nc = min(NT, n - q0);
+        const float *oq = o + (long long)q0 * D;
+        int j = 0;
+        for (; j + UNR <= nc; j += UNR) {
+            float ov[UNR];
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) ov[u] = dv ? oq[(long long)(j + u) * D] : 0.f;
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                S += cw[j + u];
+                O = fmaf(cw[j + u], ov[u], O);
+            }
         }
-        Elem<T>::store1(out + d, n > 0 ? O / S : 0.f);
+        for (; j < nc; ++j) {
+            const float ov = dv ? oq[(long long)j * D] : 0.f;
+            S += cw[j];
+            O = fmaf(cw[j], ov, O);
+        }
     }
+    T *out = reinterpret_cast<T *>(p.out) + ((long long)s * p.num_heads + h) * D;
+    if (dv) Elem<T>::store1(out + tid, n > 0 ? O / S : 0.f);
 }
 
 // ---- host-side launch helpers ------------------------------------------------
@@ -391,7 +427,20 @@ cudaError_t launch_split(const DecodeParams &p, dim3 grid, int splits, cudaStrea
 
 template <typename T>
 cudaError_t launch_merge(const MergeParams &p, int num_seqs, cudaStream_t st) {
-    lse_merge_kernel<T><<<dim3(p.num_heads, num_seqs, 1), 128, 0, st>>>(p);
+    // programmatic dependent launch: the blocks may become resident while the
+    // split-KV kernel (which signals its dependents at entry) still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.num_heads, (unsigned)num_seqs, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel<T>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

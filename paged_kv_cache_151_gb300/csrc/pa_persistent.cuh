@@ -355,6 +355,10 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     const int NWC = C * NW;                  // warps of the cluster
     const int gw = rank * NW + warp;         // this warp's index in the cluster
 
+    // split-KV partitions are always followed by their merge, which waits for
+    // this whole grid before it reads anything: let it become resident early
+    if constexpr (PARTIAL) launch_dependents();
+
     // ---- 0. barriers, and the first reads after the set-up started early -----
     if (tid == 0) {
         if constexpr (TC) {                        // fetch the descriptors early
