@@ -31,12 +31,16 @@
 // Roles: warps 0-3 run the softmax (warp w reaches TMEM lanes 32w..32w+31);
 // warps 4 and 6 keep the copies going -- Q once per item and a ring of two K
 // stages (warp 4; a K stage is free once its S is done), a ring of two V
-// stages (warp 6; free once its P.V is done); warp 5 (lane 0) issues the
-// MMAs in the order S(0), S(1), PV(0), S(2), PV(1), ...: S(g+1) once the
-// softmax has read S(g), PV(g) once P(g) is written.  Completion comes back
-// through tcgen05.commit on mbarriers; the MMA thread itself waits on no
-// MMA (the softmax waits for PV(g-2) before reusing its P buffer, the copy
-// warps for S(g-2) and PV(g-2) before reusing a stage).  Two blocks share
+// stages (warp 6; free once its P.V is done); lane 0 of warp 5 issues the
+// S MMAs (S(g+1) once the softmax has read S(g) and K(g+1) has landed) and
+// lane 0 of warp 7 the P.V MMAs (PV(g) once P(g) is written).  An MMA issue
+// blocks while the tensor pipe, which the SM's two blocks share, is busy;
+// with two issuers a P.V that is ready never waits behind S MMAs, or the
+// reverse.  S and P.V write disjoint TMEM columns, and each issuer's
+// commits track its own MMAs.  Completion comes back through tcgen05.commit
+// on mbarriers; neither MMA thread waits on an MMA's completion (the
+// softmax waits for PV(g-2) before reusing its P buffer, the copy warps for
+// S(g-2) and PV(g-2) before reusing a stage).  Two blocks share
 // an SM (about 104 KB of shared memory and 256 TMEM columns each).  The
 // grid is persistent; block b takes the items b, 2R-1-b, 2R+b, ... of the
 // sorted list (R blocks), which deals the long items out first.  Every wait
@@ -81,9 +85,10 @@ constexpr uint32_t TC_TMEM_COLS = 256;
 constexpr int TC_BLOCKS_PER_SM = 2;
 constexpr int TC_SOFTMAX_WARPS = 4;      // one row per thread
 constexpr int TC_COPY_WARP = 4;        // Q and K copies
-constexpr int TC_MMA_WARP = 5;
+constexpr int TC_MMA_WARP = 5;        // S MMAs
+constexpr int TC_PV_WARP = 7;         // P.V MMAs
 constexpr int TC_VCOPY_WARP = 6;       // V copies
-constexpr int TC_THREADS = 7 * 32;
+constexpr int TC_THREADS = 8 * 32;
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(TC_THREADS, TC_BLOCKS_PER_SM)
@@ -132,7 +137,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         mbar_init(&p_full[0], TC_SOFTMAX_WARPS);
         mbar_init(&p_full[1], TC_SOFTMAX_WARPS);
         mbar_init(q_full, 1);
-        mbar_init(mma_idle, 1);
+        mbar_init(mma_idle, 2);
         mbar_init(s_full, 1);
         mbar_init(s_free, TC_SOFTMAX_WARPS);
         fence_mbar_init();
@@ -273,11 +278,14 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             for (long long i = (ncopies > 2 ? ncopies - 2 : 0); i < ncopies; ++i)
                 mbar_wait_bounded(&full[i & 1], (uint32_t)((i >> 1) & 1), p.err);
         }
-    } else if (warp == TC_MMA_WARP) {
-        // ---- MMAs (lane 0 issues).  Per step g: S(g+1) as soon as the
-        // softmax has read S(g) (one S buffer), then PV(g) once P(g) is
-        // written (P alternates between two buffers, so PV(g) never waits for
-        // an earlier MMA).  This thread waits on no MMA's completion.
+    } else if (warp == TC_MMA_WARP || warp == TC_PV_WARP) {
+        // ---- MMAs, issued by lane 0 of two warps so that a P.V that is ready
+        // never waits behind S MMAs blocked on the busy pipe (or the reverse).
+        // Warp TC_MMA_WARP: S(g) once K(g) has landed and the softmax has read
+        // S(g-1) (one S buffer).  Warp TC_PV_WARP: PV(g) once P(g) is written
+        // (P alternates between two buffers).  S and P.V use disjoint TMEM
+        // columns; each warp's commits track its own MMAs.
+        const bool sside = warp == TC_MMA_WARP;
         long long g0 = 0;
         bool mok = true;
         Item it;
@@ -287,44 +295,36 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
         const uint64_t dq = tc5_desc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dk0 = tc5_desc_sw128(smem_u32(sK), 16, 1024), dk1 = dk0 + (KVB >> 4);
         const uint64_t dv0 = tc5_desc_sw128(smem_u32(sV), TC_KEYS * 128, 1024), dv1 = dv0 + (KVB >> 4);
-        // S of step g into the S buffer, K from stage g % 2
-        auto issue_s = [&](long long g) -> bool {
-            const int b = (int)(g & 1);
-            if (!mbar_wait_bounded(&kfull[b], (uint32_t)((g >> 1) & 1), p.err)) return false;
-            const uint64_t kb = b ? dk1 : dk0;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                // 16 elements = 32 bytes along K inside a 128-byte row; 64 per row group
-                const uint32_t qo = (uint32_t)(((ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32) >> 4);
-                const uint32_t ko = (uint32_t)(((ks >> 2) * (TC_KEYS * 128) + (ks & 3) * 32) >> 4);
-                tc5_mma(tS, dq + qo, kb + ko, ID_S, ks > 0);
-            }
-            tc5_commit(s_full);
-            tc5_commit(&kfree[b]);
-            return true;
-        };
         for (int k = 0; mok && item_at(k, it); ++k) {
             const int n = it.nsteps;
             bool w = true;
-            if (lane == 0) {
-                // the item's first S: its Q has landed and the softmax has read the last S
+            if (lane == 0 && sside) {
+                // the item's Q has landed
                 w = mbar_wait_bounded(q_full, (uint32_t)(k & 1), p.err);
-                if (w && g0 > 0) w = mbar_wait_bounded(s_free, (uint32_t)((g0 - 1) & 1), p.err);
-                if (w) {
+                for (int c = 0; w && c < n; ++c) {
+                    const long long g = g0 + c;
+                    const int b = (int)(g & 1);
+                    // the softmax has read S(g-1); K(g) has landed
+                    w = (g == 0 || mbar_wait_bounded(s_free, (uint32_t)((g - 1) & 1), p.err)) &&
+                        mbar_wait_bounded(&kfull[b], (uint32_t)((g >> 1) & 1), p.err);
+                    if (!w) break;
                     tc5_fence_after_sync();
-                    w = issue_s(g0);
+                    const uint64_t kb = b ? dk1 : dk0;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        // 16 elements = 32 bytes along K inside a 128-byte row; 64 per row group
+                        const uint32_t qo = (uint32_t)(((ks >> 2) * (TC_ROWS * 128) + (ks & 3) * 32) >> 4);
+                        const uint32_t ko = (uint32_t)(((ks >> 2) * (TC_KEYS * 128) + (ks & 3) * 32) >> 4);
+                        tc5_mma(tS, dq + qo, kb + ko, ID_S, ks > 0);
+                    }
+                    tc5_commit(s_full);
+                    tc5_commit(&kfree[b]);
                 }
+            } else if (lane == 0) {
                 for (int c = 0; w && c < n; ++c) {
                     const long long g = g0 + c;
                     const int b = (int)(g & 1);
                     const uint32_t ph = (uint32_t)((g >> 1) & 1);
-                    if (c + 1 < n) {
-                        w = mbar_wait_bounded(s_free, (uint32_t)(g & 1), p.err);
-                        if (!w) break;
-                        tc5_fence_after_sync();
-                        w = issue_s(g + 1);
-                        if (!w) break;
-                    }
                     w = mbar_wait_bounded(&p_full[b], ph, p.err) && mbar_wait_bounded(&vfull[b], ph, p.err);
                     if (!w) break;
                     tc5_fence_after_sync();
@@ -339,7 +339,7 @@ prefill_tc_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
             mok = __shfl_sync(0xffffffffu, w, 0);
             g0 += n;
         }
-        // MMAs may still be running (after a timeout): wait for them
+        // MMAs may still be running (after a timeout): wait for them (both warps)
         if (lane == 0) {
             tc5_commit(mma_idle);
             mbar_wait_bounded(mma_idle, 0, p.err);
