@@ -468,6 +468,17 @@ const char *pa_status_string(int status);
  */
 int pa_device_error(uint32_t *flags, int clear);
 
+/*
+ * pa_test_stall_next_decode -- test hook for the kernels' bounded waits.  The
+ * next decode call (any pa_decode* entry point, from any host thread) makes
+ * the first copy of every warp of its persistent kernel expect 16 bytes more
+ * than it delivers, so the wait for that copy runs out at its 1 s limit: the
+ * kernel sets PA_DEVERR_TIMEOUT, waits (bounded) for its copies in flight and
+ * returns, leaving that call's output incomplete (the call takes ~2 s).  The
+ * context stays usable.  For tests of the error path only.  Returns PA_OK.
+ */
+int pa_test_stall_next_decode(void);
+
 /* ABI version of this header (increments on any signature change or addition). */
 int pa_abi_version(void);
 

@@ -174,9 +174,14 @@ bool encode_q_map(CUtensorMap *m, const void *q, int64_t rows, int32_t num_heads
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One-shot test hook armed by pa_test_stall_next_decode, taken by the next
+// decode call that prepares its parameters here.
+std::atomic<int> g_test_stall{0};
+
 // Fill the tensor maps the persistent kernel needs for 16-bit and E4M3
 // caches (kv_dtype: the caches' storage type).
 bool prepare_maps(pa::DecodeParams &p, int32_t kv_dtype, int32_t head_dim) {
+    p.test_stall = g_test_stall.exchange(0, std::memory_order_acq_rel);
     if (kv_dtype == PA_F32) return true;
     if (p.num_blocks <= 0) return true;            // nothing can be read
     if (!encode_cache_map(&p.tmap_k, p.k_cache, p.num_blocks, p.num_kv_heads, head_dim,
@@ -284,7 +289,12 @@ bool workspace_layout(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
 
 extern "C" {
 
-int pa_abi_version(void) { return 3; }
+int pa_abi_version(void) { return 4; }
+
+int pa_test_stall_next_decode(void) {
+    g_test_stall.store(1, std::memory_order_release);
+    return PA_OK;
+}
 
 const char *pa_status_string(int status) {
     switch (status) {

@@ -81,6 +81,8 @@ struct DecodeParams {
     const float *k_scale;     // E4M3 caches: [num_kv_heads] dequantisation scales
     const float *v_scale;
     float scale_log2;         // scale * log2(e)
+    int test_stall = 0;       // test hook (pa_test_stall_next_decode): each warp's
+                              // first copy expects 16 bytes it never gets
     unsigned int *err;        // device error word
     // 16-bit and E4M3 caches, persistent kernel: the caches as 3-D tensors
     // [num_blocks*num_kv_heads][16 rows][head_dim], read in swizzled boxes

@@ -619,8 +619,11 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
     const uint64_t pol = policy_evict_first();
     const unsigned char *kbase = reinterpret_cast<const unsigned char *>(p.k_cache);
     const unsigned char *vbase = reinterpret_cast<const unsigned char *>(p.v_cache);
+    // test hook: each warp's first stage never completes, so its wait runs out
+    const uint32_t stall = p.test_stall ? 16u : 0u;
     auto issue = [&](int k, int ui, int pbk) {     // lane 0 only
         uint64_t *bar = &my_bars[k % S];
+        const uint32_t extra = k == 0 ? stall : 0u;
         if (pbk < 0 || (long long)pbk >= p.num_blocks) {
             set_error(p.err, ERR_BLOCK_ID);
             mbar_arrive(bar);
@@ -630,7 +633,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         if constexpr (F8) {
             // whole 16-row tiles, one box of 16 rows x D bytes each
             const int z = pbk * Hkv + units[ui].j;
-            mbar_arrive_expect_tx(bar, 2 * TILE);
+            mbar_arrive_expect_tx(bar, 2 * TILE + extra);
             tma_load_3d(dst, &p.tmap_k, 0, 0, z, bar, pol);
             tma_load_3d(dst + TILE, &p.tmap_v, 0, 0, z, bar, pol);
         } else if constexpr (TC) {
@@ -639,7 +642,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
             // stale rows, which the block math masks or clears)
             const int z = pbk * Hkv + units[ui].j;
             const bool half = rows_of(k, ui) <= 8;
-            mbar_arrive_expect_tx(bar, half ? TILE : 2 * TILE);
+            mbar_arrive_expect_tx(bar, (half ? TILE : 2 * TILE) + extra);
             const CUtensorMap *mk = half ? &p.tmap_k8 : &p.tmap_k;
             const CUtensorMap *mv = half ? &p.tmap_v8 : &p.tmap_v;
 #pragma unroll
@@ -650,7 +653,7 @@ decode_persistent_kernel(const __grid_constant__ DecodeParams p) {
         } else {
             const uint32_t bytes = (uint32_t)(rows_of(k, ui) * ROWB);
             const size_t off = ((size_t)pbk * Hkv + units[ui].j) * TILE;
-            mbar_arrive_expect_tx(bar, 2 * bytes);
+            mbar_arrive_expect_tx(bar, 2 * bytes + extra);
             bulk_g2s(dst, kbase + off, bytes, bar, pol);
             bulk_g2s(dst + TILE, vbase + off, bytes, bar, pol);
         }

@@ -53,6 +53,8 @@ def load():
                                 ctypes.c_float, ctypes.c_size_t)
         lib.pa_abi_version.restype = ctypes.c_int
         lib.pa_abi_version.argtypes = []
+        lib.pa_test_stall_next_decode.restype = ctypes.c_int
+        lib.pa_test_stall_next_decode.argtypes = []
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_reshape_and_cache.restype = ctypes.c_int
@@ -446,6 +448,12 @@ def workspace_views(workspace, num_seqs, num_heads, head_dim, max_seq_len, parti
     return o, m, l
 
 
+def pa_test_stall_next_decode() -> None:
+    """Test hook: in the next decode call each warp's first copy never completes,
+    so its bounded wait runs out and the call sets PA_DEVERR_TIMEOUT."""
+    _check("pa_test_stall_next_decode", load().pa_test_stall_next_decode())
+
+
 def pa_device_error(clear: bool = True) -> int:
     """Sticky device error bits (PA_DEVERR_*); synchronises the device."""
     flags = ctypes.c_uint32(0)
@@ -455,6 +463,7 @@ def pa_device_error(clear: bool = True) -> int:
 
 __all__ = [
     "PAError", "load", "library_path", "pa_status_string", "pa_abi_version",
+    "pa_test_stall_next_decode",
     "pa_reshape_and_cache", "pa_decode", "pa_decode_split",
     "pa_decode_partitioned_workspace_size", "pa_decode_partitioned", "pa_decode_multi",
     "pa_decode_partitioned_noalloc", "PA_NOALLOC_SCRATCH_BYTES",

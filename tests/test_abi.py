@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert pa.pa_abi_version() == 3
+    assert pa.pa_abi_version() == 4
     assert pa.pa_status_string(0) == "ok"
     assert "invalid" in pa.pa_status_string(-1)
     assert "unsupported" in pa.pa_status_string(-2)
