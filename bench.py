@@ -672,13 +672,14 @@ def multi_query_arm(args, device, flush, pa):
         def call():
             pa.pa_decode_multi(out, b.q, b.k_cache, b.v_cache, bt, sl, qs, mq, b.scale,
                                b.num_kv_heads)
-        for _ in range(3):
+        for _ in range(5):
             call()
-        ms = time_calls(call, 20, flush, torch.cuda.current_stream())
+        ms = time_calls(call, 40, flush, torch.cuda.current_stream())
         t = statistics.mean(ms) * 1e-3
         nb = multi_bytes(b)
         res[name] = {"workload": make.__doc__.split("\n\n")[0].replace("\n", " "),
-                     "us_per_call": t * 1e6, "rows_per_s": nb["rows"] / t,
+                     "us_per_call": t * 1e6, "us_per_call_median": statistics.median(ms) * 1e3,
+                     "calls": len(ms), "rows_per_s": nb["rows"] / t,
                      "kv_gbs": nb["kv"] / t / 1e9,
                      "achieved_gbs": nb["total"] / t / 1e9,
                      "frac_of_peak": nb["total"] / t / 1e9 / peak, "peak_kind": kind,
